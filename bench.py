@@ -1,0 +1,428 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 speculative-sampling verifier.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config c5] [--impl ours|reference]
+
+One step = one verification call (target-row pass, accept scan, race) over
+one batch of the chosen workload, inputs resident in HBM. Prints one JSON
+line with the metric "verified draft positions/sec and achieved HBM GB/s":
+``value`` is sum(gamma_r) per second over all ranks; ``e2e`` is the same
+metric through the public API with the inputs copied from pinned host memory
+and the outputs copied back inside the timed region; ``roofline`` is the
+dominant kernel (the target-row pass) timed live with the library's phase
+events, set against the measured HBM copy bandwidth; ``cpu_baseline`` is the
+CPU oracle (single thread, as written) on a bounded sample of the same
+workload. ``--impl reference`` times that oracle alone.
+
+Multi-GPU: one process per GPU (torchrun); every rank verifies its own batch
+of the workload (requests numbered rank * B + r), no collective on the data
+path; timing is the max over ranks (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+L2_BYTES = 129 * 2 ** 20
+WORKLOADS = {
+    "c2": "B=8 gamma=3 V=32000 fp32 logits N(0,2^2)+3 boosted tokens, probabilistic draft, T=1",
+    "c3": ("B=64 gamma=5 V=128256 bf16 logits N(0,3^2)+Zipf(1.1), probabilistic draft, "
+           "T in {0,0.7,1}, top_k=50 / top_p=0.9 / none by thirds"),
+    "c4": ("B=256 gamma=4 V=151936 bf16 logits N(0,2.5^2)+Zipf(1.0), one-hot greedy draft "
+           "(no draft_probs), T=1, top_p=0.95"),
+    "c5": ("B=1024 ragged gamma U{1..7} V=256000 bf16 logits N(0,2^2)+Zipf(1.2), half T=0 "
+           "(argmax path), half T=0.8 with probabilistic draft"),
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default="c5", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def rank_request_base(rank: int, B: int) -> int:
+    """Global index of this rank's first request (weak scaling: each rank
+    verifies its own B requests)."""
+    return rank * B
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def algorithmic_bytes(batch, num_accepted) -> dict:
+    """Bytes the method must move for one call, from the call's outcome: every
+    target row once, the draft_probs row of each rejected probabilistic
+    request, the per-position gathers and the outputs."""
+    B, V = batch["B"], batch["V"]
+    cu = batch["cu_num_draft"]
+    gam = np.diff(cu)
+    N = int(cu[-1])
+    R = N + B
+    esize = 2 if batch["logits_dtype"] == "bf16" else 4
+    T = batch["temperature"]
+    rows = R * V * esize
+    q_rows = 0
+    judged_q = 0
+    if batch["draft_probs"] is not None:
+        hot = (T > 0)
+        rejected = hot & (num_accepted < gam)
+        q_rows = int(rejected.sum()) * V * 4
+        judged_q = int(np.minimum(num_accepted + 1, gam)[hot].sum()) * 4
+    small = (B + 1) * 4 + N * 4 + B * 4 * 3 + judged_q + (N + B) * 4 + B * 4
+    return dict(row_pass=rows, race_q=q_rows, small=small, total=rows + q_rows + small)
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.out = None
+        self.device = device_index
+
+    def _gpu_id(self):
+        try:
+            import torch
+            u = torch.cuda.get_device_properties(self.device).uuid
+            return "GPU-" + str(u)
+        except Exception:
+            return str(self.device)
+
+    def start(self):
+        try:
+            self.out = open(self._path(), "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self._gpu_id(), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def _path(self):
+        d = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) \
+            else "/tmp"
+        return os.path.join(d, f"clocks_{os.getpid()}.csv")
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self._path()) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "speculative_decoding_rejection_02_gb300", "csrc")
+    for fn in sorted(os.listdir(d)):
+        with open(os.path.join(d, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when there is none for this kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t.get(config)
+        if e and e.get("source_sha") == kernel_source_sha():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+def cpu_oracle_rate(batch, seconds: float, steps: int = 1):
+    """Time the CPU oracle on a bounded sample of requests; returns
+    (positions/s, description, seconds used)."""
+    import oracle
+    cu = batch["cu_num_draft"]
+    gam = np.diff(cu)
+    B = batch["B"]
+    t0 = time.perf_counter()
+    oracle.verify(batch, requests=[0, 1])
+    per_req = max((time.perf_counter() - t0) / 2, 1e-4)
+    n = int(max(1, min(B, seconds / per_req)))
+    reqs = list(range(n))
+    t0 = time.perf_counter()
+    oracle.verify(batch, requests=reqs)
+    dt = time.perf_counter() - t0
+    pos = int(gam[:n].sum())
+    return pos / dt, f"first {n} of {B} requests ({pos} draft positions), one thread", dt
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    batch = synth.make(args.config)
+    import oracle
+    cu = batch["cu_num_draft"]
+    gam = np.diff(cu)
+    budget = 90.0
+    t0 = time.perf_counter()
+    oracle.verify(batch, requests=[0, 1])
+    per_req = max((time.perf_counter() - t0) / 2, 1e-4)
+    per_step = max(1, int(budget / max(1, args.steps + args.warmup) / per_req))
+    per_step = min(per_step, batch["B"])
+    B = batch["B"]
+
+    def step(i):
+        lo = (i * per_step) % B
+        reqs = [(lo + t) % B for t in range(per_step)]
+        oracle.verify(batch, requests=reqs)
+        return int(gam[reqs].sum())
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    pos = 0
+    for i in range(args.steps):
+        pos += step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    v = pos / dt
+    line = {
+        "impl": "reference", "metric": "verified draft positions/sec", "value": v,
+        "unit": "draft_positions/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.config}: {WORKLOADS[args.config]}",
+                   "sample": f"{per_step} requests per step"},
+        "cpu_baseline": {"value": v, "unit": "draft_positions/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{per_step} requests per step of {args.config}, one thread"},
+        "e2e": {"value": v, "unit": "draft_positions/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    import torch.distributed as dist
+
+    import speculative_decoding_rejection_02_gb300 as sv
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    batch = synth.make(args.config)
+    B, V = batch["B"], batch["V"]
+    batch["request_base"] = rank_request_base(rank, B)
+    cu = batch["cu_num_draft"]
+    N = int(cu[-1])
+    R = N + B
+    positions = N
+
+    ver = sv.Verifier(max_batch=B, max_rows=R, max_vocab=V, device=local)
+    db = sv.upload(batch, dev, with_p=False)
+    stream = torch.cuda.current_stream(dev)
+    in_bytes = sum(v for v in synth.batch_bytes(batch).values())
+    flush = None
+    if batch["target_logits"].nbytes < 2 * L2_BYTES:
+        flush = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    # Warm-up (also fixes the deterministic outcome used for the byte count).
+    for _ in range(max(3, args.warmup)):
+        ver.run(db, stream)
+    torch.cuda.synchronize(dev)
+    assert ver.status() == 0, "device status bits set"
+    n_acc = db.num_accepted.cpu().numpy()
+    bytes_ = algorithmic_bytes(batch, n_acc)
+
+    # Timed region: K calls, per-call events and per-phase events.
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    ph = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    for i in range(K):
+        if flush is not None:
+            flush.zero_()
+        ver.set_phase_events(ph[i])
+        ev[i][0].record(stream)
+        ver.run(db, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    clock_info = clocks.stop()
+    ver.set_phase_events(None)
+    if world > 1:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    rows_ms = [p[0].elapsed_time(p[1]) for p in ph]
+    accept_ms = [p[1].elapsed_time(p[2]) for p in ph]
+    race_ms = [p[2].elapsed_time(p[3]) for p in ph]
+    total_ms = sum(step_ms)
+    total_ms = max_over_ranks(total_ms, dev)
+    ms_per_step = total_ms / K
+    value = world * positions / (ms_per_step * 1e-3)
+    rows_avg = sum(rows_ms) / K
+
+    peak, peak_kind = measured_hbm_peak()
+    achieved = bytes_["row_pass"] / (rows_avg * 1e-3) / 1e9
+    step_gbs = bytes_["total"] / (ms_per_step * 1e-3) / 1e9
+
+    # End to end through the public API with host buffers.
+    e2e = None
+    if args.e2e_steps > 0:
+        host = {}
+        for k in ("cu_num_draft", "draft_token_ids", "target_logits", "draft_probs",
+                  "temperature", "top_k", "top_p"):
+            a = batch.get(k)
+            if a is None:
+                continue
+            if k == "target_logits" and batch["logits_dtype"] == "bf16":
+                a = np.ascontiguousarray(a).view(np.int16)
+            host[k] = torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        dst = {"cu_num_draft": db.cu_num_draft, "draft_token_ids": db.draft_token_ids,
+               "target_logits": db.target_logits, "draft_probs": db.draft_probs,
+               "temperature": db.temperature, "top_k": db.top_k, "top_p": db.top_p}
+        out_tok = torch.empty(R, dtype=torch.int32).pin_memory()
+        out_acc = torch.empty(B, dtype=torch.int32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_tok.numel() * 4 + out_acc.numel() * 4
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            for k, t in host.items():
+                d = dst[k]
+                d.view(t.dtype).reshape(-1).copy_(t.reshape(-1), non_blocking=True)
+            ver.run(db, stream)
+            out_tok.copy_(db.out_tokens, non_blocking=True)
+            out_acc.copy_(db.num_accepted, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev) / args.e2e_steps
+        e2e = {"value": world * positions / (e2e_ms * 1e-3), "unit": "draft_positions/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, desc, secs = cpu_oracle_rate(batch, args.cpu_seconds)
+        cpu = {"value": rate, "unit": "draft_positions/s", "cores": 1, "kind": "oracle",
+               "sample": desc, "seconds": round(secs, 2)}
+
+    launches_per_step = 3 + (1 if (batch.get("top_k") is not None or
+                                   batch.get("top_p") is not None) else 0)
+    if rank == 0:
+        line = {
+            "metric": "verified draft positions/sec and achieved HBM GB/s (fraction of GB300 peak)",
+            "value": value, "unit": "draft_positions/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{args.config}: {WORKLOADS[args.config]}", "B": B, "V": V,
+                       "target_rows": R, "draft_positions": positions,
+                       "logits_dtype": batch["logits_dtype"], "input_bytes": int(in_bytes),
+                       "l2": ("inputs larger than L2" if flush is None
+                              else "L2 flushed between timed calls (512 MB write)"),
+                       "parallelism": f"replicas x{world}"},
+            "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak,
+            "algorithmic_bytes_per_step": bytes_,
+            "phases_ms": {"rows": rows_avg, "accept": sum(accept_ms) / K,
+                          "race": sum(race_ms) / K},
+            "roofline": {"bound": "hbm", "kernel": "target-row pass", "achieved": achieved,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)",
+                         "traffic": ncu_traffic(args.config)},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": K * launches_per_step,
+            "clocks": clock_info,
+        }
+        print(json.dumps(line), flush=True)
+    ver.close()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * spec_verify.h — C ABI of the GB300 speculative-sampling verifier.
+ *
+ * One call verifies a ragged batch of draft-then-verify rounds: for request r
+ * with gamma_r = cu_num_draft[r+1] - cu_num_draft[r] draft tokens it reads the
+ * target's logits at gamma_r + 1 positions, applies the request's temperature,
+ * top-k and top-p to get p, accepts draft token x_i while u_i <= p_i(x_i) /
+ * q_i(x_i), resamples the first rejected position from norm(max(0, p - q)) by
+ * the exponential race argmax_j w_j / E_j, and emits a bonus token from
+ * p_{gamma+1} when every draft token is accepted. Temperature-0 requests accept
+ * while the draft equals the target argmax and emit the argmax.
+ *
+ * Sources of the operation (web pages; titles and sections):
+ *  - velog, "vLLM speculative decoding이 기각 토큰을 다시 뽑는 이유":
+ *      "드래프트가 제안하고 타깃이 판정한다" (accept rule, bonus token),
+ *      "왜 하필 max(p − q, 0)인가" (residual distribution, App. A.1),
+ *      "vLLM 커널은 이 규칙을 어떻게 옮겼나" (output = accepted + recovered +
+ *        bonus tokens; float64 uniforms; exponential race; temperature / top-k /
+ *        top-p applied before the judgement),
+ *      "기본값 greedy 드래프트에서도 분포가 지켜질까" (draft_probs absent = one-hot
+ *        draft; temperature-0 requests judged by argmax agreement).
+ *  - cortexys.team, "초안 모델로 생성 속도를 높이는 추측 디코딩", section 방법
+ *      (Algorithm 1: gamma drafts, one parallel target pass over gamma + 1
+ *      positions, left-to-right verification).
+ *  - mlxcel, "투기적 디코딩", section 기본 라운드 (a round emits 1 .. K + 1
+ *      tokens).
+ *
+ * Randomness. Every random number is a Philox4x32-10 draw (Salmon et al.,
+ * SC'11) with key = seed and counter = (c0, position, global request, tag):
+ *   accept uniform of position i:  c0 = 0, tag 0; the top 52 bits m of words
+ *     0..1 give u = (2m + 1) 2^-53 in (0, 1) as a double (never 0, so a
+ *     p = 0 token is never accepted);
+ *   race uniform of vocabulary entry j at position k: c0 = j / 4, tag 1,
+ *     word j mod 4; U = (2 (w >> 9) + 1) 2^-24 in (0, 1), E = -ln U.
+ * "global request" = request_base + r, so a batch split across calls (or
+ * GPUs) draws exactly what the whole batch would.
+ *
+ * Conventions for every entry point:
+ *  - All array arguments are DEVICE pointers unless stated; the caller owns
+ *    them. The library owns only the workspace it allocates in
+ *    spec_verify_init (row statistics, per-request scratch, status word).
+ *  - Calls are asynchronous on the given stream and never synchronise the
+ *    host. Errors found on the device (bad offsets, bad token ids, non-finite
+ *    logits) set bits in a device status word; nothing traps. Read the word
+ *    with spec_verify_status after synchronising the stream.
+ *  - Return value: SPEC_OK (0) or a negative SPEC_ERR_* code. Argument errors
+ *    are detected on the host before anything is enqueued; nothing is
+ *    enqueued when a call fails.
+ *  - A handle is not thread-safe and its workspace serves one call at a time:
+ *    use one handle per stream (calls on one stream are ordered).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define SPEC_OK 0
+#define SPEC_ERR_INVALID_ARG (-1)   /* null pointer, negative size, bad enum */
+#define SPEC_ERR_UNSUPPORTED (-2)   /* device is not sm_103 */
+#define SPEC_ERR_CUDA (-3)          /* a CUDA runtime call failed */
+#define SPEC_ERR_NOT_INIT (-4)      /* null handle */
+#define SPEC_ERR_CAPACITY (-5)      /* batch exceeds the handle's maxima */
+#define SPEC_ERR_DEVICE_STATUS (-6) /* spec_verify_status: device bits set */
+
+/* Device status bits (spec_verify_status). */
+#define SPEC_STATUS_NONFINITE 0x1u      /* NaN or +inf logit in a T > 0 row */
+#define SPEC_STATUS_NO_FINITE 0x2u      /* T > 0 row whose logits are all -inf */
+#define SPEC_STATUS_BAD_TOKEN 0x4u      /* draft token id outside [0, V) */
+#define SPEC_STATUS_EMPTY_RESIDUAL 0x8u /* all residual weights 0: raced on p */
+#define SPEC_STATUS_BAD_OFFSETS 0x10u   /* cu_num_draft not 0 .. N, non-decreasing */
+
+/* Batch flags. */
+#define SPEC_FLAG_NAIVE 0x1u /* negative control: resample rejected positions
+                                from p instead of the residual (biased; for
+                                tests of the statistics only) */
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+typedef struct spec_verify_handle spec_verify_handle; /* opaque */
+
+typedef struct {
+  int device;          /* CUDA device ordinal */
+  int max_batch;       /* largest B of any call */
+  long long max_rows;  /* largest N + B (target rows) of any call */
+  int max_vocab;       /* largest V of any call */
+  unsigned flags;      /* reserved: 0 */
+} spec_verify_config;
+
+typedef struct {
+  int B;                       /* requests in the batch, >= 0 */
+  int V;                       /* vocabulary size, >= 1 */
+  int N;                       /* total draft tokens = cu_num_draft[B] (host copy) */
+  const int* cu_num_draft;     /* [B+1] device; cu[0] = 0, non-decreasing,
+                                  cu[B] = N; gamma_r = cu[r+1] - cu[r] */
+  const int* draft_token_ids;  /* [N] device; x of request r, position i at
+                                  cu[r] + i */
+  const void* target_logits;   /* [(N+B) x V] device, row-major, dtype below;
+                                  the gamma_r + 1 rows of request r are rows
+                                  cu[r] + r .. cu[r+1] + r */
+  spec_dtype logits_dtype;     /* SPEC_F32 or SPEC_BF16 */
+  const float* draft_probs;    /* [N x V] device fp32 (row cu[r] + i is q_i of
+                                  request r), or NULL: one-hot greedy draft,
+                                  q_i(x_i) = 1 */
+  const float* temperature;    /* [B] device; 0 => argmax-match path; > 0 */
+  const int* top_k;            /* [B] device or NULL; <= 0 or >= V => off */
+  const float* top_p;          /* [B] device or NULL; >= 1 => off; in (0, 1] */
+  unsigned long long seed;     /* Philox key */
+  long long request_base;      /* global index of request 0 (RNG counter) */
+  unsigned flags;              /* SPEC_FLAG_* */
+  int* out_tokens;             /* [N+B] device out; slots cu[r]+r .. cu[r+1]+r:
+                                  the accepted drafts, then the recovered or
+                                  bonus token, then -1 */
+  int* num_accepted;           /* [B] device out; accepted drafts per request */
+  float* p_at_draft;           /* [N] device out or NULL: p_i(x_i) for every
+                                  draft position (at T = 0: 1 if x_i is the
+                                  argmax else 0) */
+} spec_verify_batch;
+
+/*
+ * spec_verify_init — create a handle on cfg->device and allocate its
+ * workspace for batches up to the configured maxima.
+ *   h   [out] receives the handle (NULL on failure).
+ *   cfg [in]  host pointer; maxima must be >= 1.
+ * Returns SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_UNSUPPORTED (not an sm_103
+ * device) or SPEC_ERR_CUDA. Synchronous.
+ */
+int spec_verify_init(spec_verify_handle** h, const spec_verify_config* cfg);
+
+/*
+ * spec_verify_run — verify one batch (velog sections above; cortexys 방법).
+ * Every request uses its own temperature / top-k / top-p; temperature-0
+ * requests take the argmax-match path, the others the probabilistic one.
+ *   h [in] handle; b [in] host pointer to the batch description (device
+ *   arrays inside); stream [in] a cudaStream_t (NULL = legacy default stream).
+ * Returns SPEC_OK, SPEC_ERR_NOT_INIT, SPEC_ERR_INVALID_ARG, SPEC_ERR_CAPACITY
+ * or SPEC_ERR_CUDA (launch failure). Asynchronous.
+ */
+int spec_verify_run(spec_verify_handle* h, const spec_verify_batch* b,
+                    void* stream);
+
+/*
+ * spec_verify_greedy — the temperature-0 verification for the whole batch
+ * (velog, "기본값 greedy 드래프트에서도 분포가 지켜질까": accept while the draft
+ * equals the target argmax; emit the argmax of the first mismatching row, or
+ * of the last row). Ignores temperature, top_k, top_p, draft_probs, seed and
+ * flags (those pointers may be NULL). Same returns as spec_verify_run.
+ */
+int spec_verify_greedy(spec_verify_handle* h, const spec_verify_batch* b,
+                       void* stream);
+
+/*
+ * spec_verify_status — read and clear the device status word (a bitwise OR of
+ * SPEC_STATUS_* over every call since the last read). Synchronises the
+ * handle's device. *device_error_bits receives the bits (host pointer).
+ * Returns SPEC_OK when no bit is set, SPEC_ERR_DEVICE_STATUS when some are,
+ * SPEC_ERR_NOT_INIT or SPEC_ERR_CUDA.
+ */
+int spec_verify_status(spec_verify_handle* h, unsigned* device_error_bits);
+
+/*
+ * spec_verify_check_batch — the host-side argument checks of spec_verify_run,
+ * without a handle or a device: null pointers, sizes, dtype, and the maxima of
+ * cfg. Returns SPEC_OK, SPEC_ERR_INVALID_ARG or SPEC_ERR_CAPACITY.
+ */
+int spec_verify_check_batch(const spec_verify_config* cfg,
+                            const spec_verify_batch* b);
+
+/*
+ * spec_verify_set_phase_events — timing hook for profiling. With n >= 4
+ * events set (cudaEvent_t values cast to void*, created by the caller on the
+ * handle's device), every later run / greedy call records, on its stream,
+ * events[0] before its first kernel, events[1] after the target-row pass,
+ * events[2] after the accept scan and events[3] after the race (equal to
+ * events[2] for spec_verify_greedy). n = 0 (events may be NULL) turns the
+ * hook off. The caller keeps ownership of the events.
+ * Returns SPEC_OK, SPEC_ERR_NOT_INIT or SPEC_ERR_INVALID_ARG.
+ */
+int spec_verify_set_phase_events(spec_verify_handle* h, void* const* events, int n);
+
+/* spec_verify_destroy — free the workspace and the handle (NULL is a no-op).
+ * Synchronises the handle's device first. */
+void spec_verify_destroy(spec_verify_handle* h);
+
+/* spec_verify_strerror — static description of a return code. */
+const char* spec_verify_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

@@ -350,6 +350,8 @@ static void or_verify_one(const or_batch* b, int r, const or_outputs* o) {
   const int gamma = b->cu_num_draft[r + 1] - c0;
   const int64_t row0 = (int64_t)c0 + r;  // first target row of request r
   const int64_t greq = b->request_base + r;
+  // Reading: a temperature that is not > 0 (0, negative, NaN) takes the
+  // temperature-0 path.
   const double T = (double)b->temperature[r];
   const int tk = b->top_k ? b->top_k[r] : 0;
   const double tp = b->top_p ? (double)b->top_p[r] : 1.0;
@@ -380,7 +382,7 @@ static void or_verify_one(const or_batch* b, int r, const or_outputs* o) {
   // draft position gets p_i(x_i), whether or not the scan reaches it.
   for (int i = 0; i <= gamma; ++i) {
     load_row(i);
-    if (T == 0.0) {
+    if (!(T > 0.0)) {
       argmax_row[i] = or_argmax(l.data(), V);
       if (i < gamma) o->p_at_draft[c0 + i] = (draft(i) == argmax_row[i]) ? 1.0 : 0.0;
       continue;
@@ -401,7 +403,7 @@ static void or_verify_one(const or_batch* b, int r, const or_outputs* o) {
   for (int i = 0; i < gamma; ++i) {
     int x = draft(i);
     bool ok;
-    if (T == 0.0) {
+    if (!(T > 0.0)) {
       ok = (x == argmax_row[i]);
     } else {
       double p_x = o->p_at_draft[c0 + i];
@@ -421,7 +423,7 @@ static void or_verify_one(const or_batch* b, int r, const or_outputs* o) {
   // Step 3: the token at k*: the argmax at temperature 0; otherwise a race
   // over the residual (first rejection) or over p (bonus, all accepted).
   int out_token;
-  if (T == 0.0) {
+  if (!(T > 0.0)) {
     out_token = argmax_row[k_star];
   } else {
     load_row(k_star);

@@ -1,0 +1,350 @@
+// Target-row pass: the sampling constraints and row statistics of every
+// target row (velog "vLLM 커널은 이 규칙을 어떻게 옮겼나": temperature, top-k
+// and top-p turn the target logits into p before the judgement; "기본값 greedy
+// 드래프트에서도 분포가 지켜질까": temperature-0 rows need only the argmax).
+//
+// Two kernels share the work by row class:
+//  * k_rows_stream — argmax-only and plain-softmax rows. Each row is cut into
+//    slices; one CTA streams one slice once from HBM with 16-byte loads and
+//    reduces (max, lowest argmax, sum of exp2((l - m) log2e / T)) in
+//    registers and warp shuffles. The last CTA of a row (atomic counter)
+//    merges the slice partials and evaluates p at the row's draft token.
+//  * k_rows_filtered — rows with top-k and/or top-p. One CTA per row finds
+//    the thresholds exactly by bisection over order-preserving keys (counts
+//    for top-k, probability mass for top-p), re-reading the row each step.
+#pragma once
+#include "common.cuh"
+
+namespace sv {
+
+constexpr int kStreamThreads = 256;
+constexpr int kStreamChunks = 8;  // 16-byte loads per thread per slice
+constexpr int kSliceBf16 = kStreamThreads * kStreamChunks * 8;  // 16384
+constexpr int kSliceF32 = kStreamThreads * kStreamChunks * 4;   // 8192
+
+__device__ __forceinline__ int unpack_chunk(uint4 v, int bf16, float* f) {
+  if (bf16) {
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+    return 8;
+  }
+  f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+  f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+  return 4;
+}
+
+// Partials written by other CTAs of the row: read through L2, not L1.
+__device__ __forceinline__ SlicePartial load_partial(const SlicePartial* p) {
+  const int4 v = __ldcg(reinterpret_cast<const int4*>(p));
+  SlicePartial q;
+  q.m = __int_as_float(v.x);
+  q.s = __int_as_float(v.y);
+  q.argmax = v.z;
+  q.pad = v.w;
+  return q;
+}
+
+// Write the statistics of one finished row and p at its draft token.
+__device__ void finish_row(const Params& P, long long row, int r, int cls, float m, int argmax,
+                           float z, float theta, float c) {
+  unsigned st = 0;
+  if (cls != kArgmaxOnly) {
+    if (m == INFINITY || !(z == z)) st |= SPEC_STATUS_NONFINITE;
+    else if (m == -INFINITY) st |= SPEC_STATUS_NO_FINITE;
+  }
+  float p_x = 0.f;
+  const int c0 = __ldg(P.cu + r);
+  const int gamma = __ldg(P.cu + r + 1) - c0;
+  const long long i = row - ((long long)c0 + r);
+  if (i >= 0 && i < gamma && c0 + i < P.N) {
+    const int x = __ldg(P.ids + c0 + i);
+    if (x >= 0 && x < P.V) {
+      if (cls == kArgmaxOnly) {
+        p_x = (x == argmax) ? 1.f : 0.f;
+      } else if (st == 0) {
+        const float lx = load_logit(P, row, x);
+        p_x = (lx >= theta) ? exp2f((lx - m) * c) / z : 0.f;
+      }
+    }
+  }
+  RowStats s;
+  s.m = m;
+  s.c = c;
+  s.inv_z = 1.f / z;
+  s.theta = theta;
+  s.argmax = argmax;
+  s.p_x = p_x;
+  s.status = st;
+  s.z = z;
+  P.rows[row] = s;
+  if (st) atomicOr(P.status, st);
+}
+
+// Row lookup shared by both kernels; returns false (and flags the status
+// word) when the offsets do not place `row` inside its request.
+__device__ __forceinline__ bool locate_row(const Params& P, long long row, int& r) {
+  r = request_of_row(P.cu, P.B, row);
+  const int c0 = __ldg(P.cu + r), c1 = __ldg(P.cu + r + 1);
+  const long long i = row - ((long long)c0 + r);
+  if (c0 < 0 || c1 < c0 || c1 > P.N || i < 0 || i > c1 - c0) {
+    atomicOr(P.status, SPEC_STATUS_BAD_OFFSETS);
+    return false;
+  }
+  return true;
+}
+
+__global__ void __launch_bounds__(kStreamThreads)
+k_rows_stream(Params P) {
+  const int spr = P.slices_per_row;
+  const long long row = (long long)blockIdx.x / spr;
+  const int slice = (int)(blockIdx.x % spr);
+  __shared__ int s_req, s_cls, s_ok, s_last;
+  if (threadIdx.x == 0) {
+    int r = 0;
+    s_ok = locate_row(P, row, r);
+    s_req = r;
+    s_cls = s_ok ? row_class(P, r) : kArgmaxOnly;
+  }
+  __syncthreads();
+  if (!s_ok || s_cls == kFiltered) return;
+  const int r = s_req, cls = s_cls;
+  const int V = P.V;
+  const int esize = P.bf16 ? 2 : 4;
+  const int slice_elems = P.bf16 ? kSliceBf16 : kSliceF32;
+  const int j0 = slice * slice_elems;
+  const int j1 = min(V, j0 + slice_elems);
+  const float c = (cls == kSoftmax) ? kLog2e / __ldg(P.temp + r) : 0.f;
+  const char* rowp = (const char*)P.logits + row * (long long)V * esize;
+
+  float vmax = -INFINITY;
+  int imax = kNoIndex;
+  uint4 v[kStreamChunks];
+  int nchunk = 0, jt = j0;
+  const bool aligned = ((reinterpret_cast<uintptr_t>(rowp) & 15) == 0);
+  if (aligned) {
+    const int epc = 16 / esize;
+    nchunk = (j1 - j0) / epc;
+    jt = j0 + nchunk * epc;
+    const char* base = rowp + (long long)j0 * esize;
+#pragma unroll
+    for (int k = 0; k < kStreamChunks; ++k) {
+      const int ch = threadIdx.x + k * kStreamThreads;
+      v[k] = ch < nchunk ? ldg_stream(base + (long long)ch * 16) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < kStreamChunks; ++k) {
+      const int ch = threadIdx.x + k * kStreamThreads;
+      if (ch < nchunk) {
+        float f[8];
+        const int n = unpack_chunk(v[k], P.bf16, f);
+        float m8 = f[0];
+#pragma unroll
+        for (int e = 1; e < 8; ++e)
+          if (e < n) m8 = fmaxf(m8, f[e]);
+        if (m8 > vmax || (imax == kNoIndex && m8 == m8)) {
+          int e = 0;
+          while (e < n - 1 && !(f[e] == m8)) ++e;
+          vmax = m8;
+          imax = j0 + ch * epc + e;
+        }
+      }
+    }
+  }
+  // Scalar part: a misaligned row, or the tail after the last full chunk.
+  for (int j = jt + threadIdx.x; j < j1; j += kStreamThreads) {
+    const float f = load_logit(P, row, j);
+    if (f > vmax || (imax == kNoIndex && f == f)) {
+      vmax = f;
+      imax = j;
+    }
+  }
+  float m = vmax;
+  int am = imax;
+  block_argmax(m, am);
+
+  float s = 0.f;
+  if (cls == kSoftmax && m > -INFINITY) {
+    if (aligned) {
+#pragma unroll
+      for (int k = 0; k < kStreamChunks; ++k) {
+        const int ch = threadIdx.x + k * kStreamThreads;
+        if (ch < nchunk) {
+          float f[8];
+          const int n = unpack_chunk(v[k], P.bf16, f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (e < n) s += exp2f((f[e] - m) * c);
+        }
+      }
+    }
+    for (int j = jt + threadIdx.x; j < j1; j += kStreamThreads)
+      s += exp2f((load_logit(P, row, j) - m) * c);
+    s = block_sum(s);
+  }
+
+  if (threadIdx.x == 0) {
+    SlicePartial part;
+    part.m = m;
+    part.s = s;
+    part.argmax = am;
+    part.pad = 0;
+    P.partials[row * spr + slice] = part;
+    __threadfence();
+    const unsigned prev = atomicAdd(P.row_counter + row, 1u);
+    s_last = (prev == (unsigned)spr - 1u);
+  }
+  __syncthreads();
+  if (!s_last || threadIdx.x >= 32) return;
+
+  // Last slice of the row: merge the partials (warp 0).
+  __threadfence();
+  const int lane = threadIdx.x;
+  float mm = -INFINITY;
+  int aa = kNoIndex;
+  for (int t = lane; t < spr; t += 32) {
+    const SlicePartial q = load_partial(P.partials + row * spr + t);
+    argmax_combine(mm, aa, q.m, q.argmax);
+  }
+  warp_argmax(mm, aa);
+  float z = 0.f;
+  if (cls == kSoftmax) {
+    for (int t = lane; t < spr; t += 32) {
+      const SlicePartial q = load_partial(P.partials + row * spr + t);
+      if (q.m > -INFINITY) z += q.s * exp2f((q.m - mm) * c);
+    }
+    z = warp_sum(z);
+  }
+  if (lane == 0) {
+    if (aa == kNoIndex) aa = 0;
+    P.row_counter[row] = 0u;
+    finish_row(P, row, r, cls, mm, aa, z, -INFINITY, c);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Filtered rows: exact thresholds by bisection on order-preserving keys.
+// ---------------------------------------------------------------------------
+constexpr int kFilterThreads = 512;
+
+// Visit every element (value, index) of a row, in increasing index per thread.
+template <typename F>
+__device__ __forceinline__ void row_for_each(const Params& P, long long row, F&& f) {
+  const int V = P.V;
+  const int esize = P.bf16 ? 2 : 4;
+  const char* rowp = (const char*)P.logits + row * (long long)V * esize;
+  int jt = 0;
+  if ((reinterpret_cast<uintptr_t>(rowp) & 15) == 0) {
+    const int epc = 16 / esize;
+    const int nchunk = V / epc;
+    jt = nchunk * epc;
+    for (int ch = threadIdx.x; ch < nchunk; ch += blockDim.x) {
+      float e[8];
+      const int n = unpack_chunk(__ldg((const uint4*)rowp + ch), P.bf16, e);
+      for (int t = 0; t < n; ++t) f(e[t], ch * epc + t);
+    }
+  }
+  for (int j = jt + threadIdx.x; j < V; j += blockDim.x) f(load_logit(P, row, j), j);
+}
+
+__device__ __forceinline__ uint32_t elem_key(float v, int bf16) {
+  const uint32_t k = float_key(v);
+  return bf16 ? (k >> 16) : k;
+}
+
+// Smallest float whose key is `k` (key width 16 for bf16, 32 for fp32).
+__device__ __forceinline__ float key_threshold(uint32_t k, int bf16) {
+  if (bf16) {
+    const uint32_t k32 = (k << 16) | ((k & 0x8000u) ? 0u : 0xFFFFu);
+    return key_float(k32);
+  }
+  return key_float(k);
+}
+
+__global__ void __launch_bounds__(kFilterThreads)
+k_rows_filtered(Params P) {
+  const long long row = blockIdx.x;
+  __shared__ int s_req, s_cls, s_ok;
+  if (threadIdx.x == 0) {
+    int r = 0;
+    s_ok = locate_row(P, row, r);
+    s_req = r;
+    s_cls = s_ok ? row_class(P, r) : kArgmaxOnly;
+  }
+  __syncthreads();
+  if (!s_ok || s_cls != kFiltered) return;
+  const int r = s_req;
+  const int bf16 = P.bf16;
+  const float c = kLog2e / __ldg(P.temp + r);
+  const int tk = P.top_k ? __ldg(P.top_k + r) : 0;
+  const float tp = P.top_p ? __ldg(P.top_p + r) : 1.f;
+  const bool topk_on = (tk > 0 && tk < P.V);
+  const bool topp_on = (tp < 1.f);
+
+  float vmax = -INFINITY;
+  int imax = kNoIndex;
+  int nan_seen = 0;
+  row_for_each(P, row, [&](float v, int j) {
+    if (v > vmax || (imax == kNoIndex && v == v)) { vmax = v; imax = j; }
+    nan_seen |= (v != v);
+  });
+  float m = vmax;
+  int am = imax;
+  block_argmax(m, am);
+  nan_seen = block_sum(nan_seen);
+  if (am == kNoIndex) am = 0;
+  if (nan_seen || m == INFINITY || m == -INFINITY) {
+    if (threadIdx.x == 0)
+      finish_row(P, row, r, kFiltered, nan_seen ? NAN : m, am,
+                 (nan_seen || m == INFINITY) ? NAN : 0.f, -INFINITY, c);
+    return;
+  }
+
+  const long long key_space = bf16 ? (1ll << 16) : (1ll << 32);
+  long long kk = 0;  // top-k key threshold (keep key >= kk)
+  if (topk_on) {
+    long long lo = 0, hi = key_space;  // count(key >= lo) >= k > count(key >= hi)
+    while (hi - lo > 1) {
+      const long long mid = (lo + hi) >> 1;
+      int cnt = 0;
+      row_for_each(P, row, [&](float v, int) { cnt += ((long long)elem_key(v, bf16) >= mid); });
+      cnt = block_sum(cnt);
+      if (cnt >= tk) lo = mid; else hi = mid;
+    }
+    kk = lo;
+  }
+  float zk = 0.f;
+  row_for_each(P, row, [&](float v, int) {
+    if ((long long)elem_key(v, bf16) >= kk) zk += exp2f((v - m) * c);
+  });
+  zk = block_sum(zk);
+
+  long long kp = kk;  // final key threshold
+  if (topp_on) {
+    const float thr = tp * zk;
+    long long lo = kk - 1, hi = (long long)elem_key(m, bf16);  // A(lo) >= thr > A(hi)
+    while (hi - lo > 1) {
+      const long long mid = (lo + hi) >> 1;
+      float a = 0.f;
+      row_for_each(P, row, [&](float v, int) {
+        const long long k = elem_key(v, bf16);
+        if (k > mid && k >= kk) a += exp2f((v - m) * c);
+      });
+      a = block_sum(a);
+      if (a < thr) hi = mid; else lo = mid;
+    }
+    kp = hi;
+  }
+  float z = 0.f;
+  row_for_each(P, row, [&](float v, int) {
+    if ((long long)elem_key(v, bf16) >= kp) z += exp2f((v - m) * c);
+  });
+  z = block_sum(z);
+  if (threadIdx.x == 0) {
+    const float theta = (kp <= 0) ? -INFINITY : key_threshold((uint32_t)kp, bf16);
+    finish_row(P, row, r, kFiltered, m, am, z, theta, c);
+  }
+}
+
+}  // namespace sv

@@ -1,0 +1,222 @@
+// C ABI of the verifier library (declared in include/spec_verify.h): handle
+// and workspace management, host-side argument checks, and the launch
+// sequence of one verification call.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <new>
+
+#include "../../include/spec_verify.h"
+#include "accept.cuh"
+#include "common.cuh"
+#include "philox.cuh"
+#include "race.cuh"
+#include "rows.cuh"
+
+struct spec_verify_handle {
+  spec_verify_config cfg;
+  int sm_count;
+  void* ws;  // one allocation for everything below
+  sv::RowStats* rows;
+  sv::SlicePartial* partials;
+  unsigned* row_counter;
+  sv::RaceDesc* race;
+  unsigned long long* race_best;
+  unsigned* race_counter;
+  unsigned* status;
+  int max_slices;
+  cudaEvent_t phase[4];
+  int n_phase;
+};
+
+namespace {
+
+size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
+
+int check_batch(const spec_verify_config* cfg, const spec_verify_batch* b, bool greedy) {
+  if (!cfg || !b) return SPEC_ERR_INVALID_ARG;
+  if (b->B < 0 || b->N < 0 || b->V < 1) return SPEC_ERR_INVALID_ARG;
+  if (b->logits_dtype != SPEC_F32 && b->logits_dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+  if (b->B == 0) return SPEC_OK;
+  if (!b->cu_num_draft || !b->target_logits || !b->out_tokens || !b->num_accepted)
+    return SPEC_ERR_INVALID_ARG;
+  if (b->N > 0 && !b->draft_token_ids) return SPEC_ERR_INVALID_ARG;
+  if (!greedy && !b->temperature) return SPEC_ERR_INVALID_ARG;
+  if (b->B > cfg->max_batch || b->V > cfg->max_vocab ||
+      (long long)b->N + b->B > cfg->max_rows)
+    return SPEC_ERR_CAPACITY;
+  return SPEC_OK;
+}
+
+int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t stream, bool greedy) {
+  if (!h) return SPEC_ERR_NOT_INIT;
+  int rc = check_batch(&h->cfg, b, greedy);
+  if (rc != SPEC_OK) return rc;
+  if (b->B == 0) return SPEC_OK;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return SPEC_ERR_CUDA;
+
+  sv::Params P;
+  P.B = b->B;
+  P.V = b->V;
+  P.N = b->N;
+  P.cu = b->cu_num_draft;
+  P.ids = b->draft_token_ids;
+  P.logits = b->target_logits;
+  P.bf16 = (b->logits_dtype == SPEC_BF16) ? 1 : 0;
+  P.q = greedy ? nullptr : b->draft_probs;
+  P.temp = b->temperature;
+  P.top_k = greedy ? nullptr : b->top_k;
+  P.top_p = greedy ? nullptr : b->top_p;
+  P.seed = b->seed;
+  P.req_base = b->request_base;
+  P.flags = greedy ? 0u : b->flags;
+  P.greedy_call = greedy ? 1 : 0;
+  P.out_tokens = b->out_tokens;
+  P.num_accepted = b->num_accepted;
+  P.p_at_draft = b->p_at_draft;
+  P.rows = h->rows;
+  P.partials = h->partials;
+  P.row_counter = h->row_counter;
+  P.race = h->race;
+  P.race_best = h->race_best;
+  P.race_counter = h->race_counter;
+  P.status = h->status;
+  const int slice = P.bf16 ? sv::kSliceBf16 : sv::kSliceF32;
+  P.slices_per_row = (b->V + slice - 1) / slice;
+  P.race_slices = (b->V + sv::kRaceSlice - 1) / sv::kRaceSlice;
+
+  const long long R = (long long)b->N + b->B;
+  if (R * P.slices_per_row > 0x7FFFFFFFll || (long long)b->B * P.race_slices > 0x7FFFFFFFll)
+    return SPEC_ERR_CAPACITY;
+  const bool timed = h->n_phase >= 4;
+  if (timed) cudaEventRecord(h->phase[0], stream);
+  sv::k_rows_stream<<<(unsigned)(R * P.slices_per_row), sv::kStreamThreads, 0, stream>>>(P);
+  if (!greedy && (P.top_k || P.top_p))
+    sv::k_rows_filtered<<<(unsigned)R, sv::kFilterThreads, 0, stream>>>(P);
+  if (timed) cudaEventRecord(h->phase[1], stream);
+  sv::k_accept<<<(b->B + 127) / 128, 128, 0, stream>>>(P);
+  if (timed) cudaEventRecord(h->phase[2], stream);
+  if (!greedy)
+    sv::k_race<<<(unsigned)((long long)b->B * P.race_slices), sv::kRaceThreads, 0, stream>>>(P);
+  if (timed) cudaEventRecord(h->phase[3], stream);
+  if (cudaPeekAtLastError() != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_CUDA;
+  }
+  return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_verify_check_batch(const spec_verify_config* cfg, const spec_verify_batch* b) {
+  return check_batch(cfg, b, false);
+}
+
+int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
+  if (!out) return SPEC_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg || cfg->max_batch < 1 || cfg->max_rows < 1 || cfg->max_vocab < 1)
+    return SPEC_ERR_INVALID_ARG;
+  if (cfg->max_rows < cfg->max_batch) return SPEC_ERR_INVALID_ARG;
+  if (cudaSetDevice(cfg->device) != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, cfg->device) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (!(prop.major == 10 && prop.minor == 3)) return SPEC_ERR_UNSUPPORTED;
+
+  spec_verify_handle* h = new (std::nothrow) spec_verify_handle();
+  if (!h) return SPEC_ERR_CUDA;
+  h->cfg = *cfg;
+  h->sm_count = prop.multiProcessorCount;
+  h->max_slices = (cfg->max_vocab + sv::kSliceF32 - 1) / sv::kSliceF32;
+
+  const size_t n_rows = (size_t)cfg->max_rows, n_b = (size_t)cfg->max_batch;
+  const size_t sz_rows = align_up(n_rows * sizeof(sv::RowStats));
+  const size_t sz_part = align_up(n_rows * h->max_slices * sizeof(sv::SlicePartial));
+  const size_t sz_rcnt = align_up(n_rows * sizeof(unsigned));
+  const size_t sz_race = align_up(n_b * sizeof(sv::RaceDesc));
+  const size_t sz_best = align_up(n_b * sizeof(unsigned long long));
+  const size_t sz_rccnt = align_up(n_b * sizeof(unsigned));
+  const size_t sz_stat = align_up(sizeof(unsigned));
+  const size_t total = sz_rows + sz_part + sz_rcnt + sz_race + sz_best + sz_rccnt + sz_stat;
+  if (cudaMalloc(&h->ws, total) != cudaSuccess) {
+    delete h;
+    return SPEC_ERR_CUDA;
+  }
+  if (cudaMemset(h->ws, 0, total) != cudaSuccess) {
+    cudaFree(h->ws);
+    delete h;
+    return SPEC_ERR_CUDA;
+  }
+  char* p = (char*)h->ws;
+  h->rows = (sv::RowStats*)p; p += sz_rows;
+  h->partials = (sv::SlicePartial*)p; p += sz_part;
+  h->row_counter = (unsigned*)p; p += sz_rcnt;
+  h->race = (sv::RaceDesc*)p; p += sz_race;
+  h->race_best = (unsigned long long*)p; p += sz_best;
+  h->race_counter = (unsigned*)p; p += sz_rccnt;
+  h->status = (unsigned*)p;
+  *out = h;
+  return SPEC_OK;
+}
+
+int spec_verify_run(spec_verify_handle* h, const spec_verify_batch* b, void* stream) {
+  return launch(h, b, (cudaStream_t)stream, false);
+}
+
+int spec_verify_greedy(spec_verify_handle* h, const spec_verify_batch* b, void* stream) {
+  return launch(h, b, (cudaStream_t)stream, true);
+}
+
+int spec_verify_status(spec_verify_handle* h, unsigned* bits) {
+  if (!h) return SPEC_ERR_NOT_INIT;
+  if (!bits) return SPEC_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SPEC_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, h->status, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  if (cudaMemset(h->status, 0, sizeof v) != cudaSuccess) return SPEC_ERR_CUDA;
+  *bits = v;
+  return v ? SPEC_ERR_DEVICE_STATUS : SPEC_OK;
+}
+
+int spec_verify_set_phase_events(spec_verify_handle* h, void* const* events, int n) {
+  if (!h) return SPEC_ERR_NOT_INIT;
+  if (n == 0) {
+    h->n_phase = 0;
+    return SPEC_OK;
+  }
+  if (n < 4 || !events) return SPEC_ERR_INVALID_ARG;
+  for (int i = 0; i < 4; ++i) {
+    if (!events[i]) return SPEC_ERR_INVALID_ARG;
+    h->phase[i] = (cudaEvent_t)events[i];
+  }
+  h->n_phase = 4;
+  return SPEC_OK;
+}
+
+void spec_verify_destroy(spec_verify_handle* h) {
+  if (!h) return;
+  cudaSetDevice(h->cfg.device);
+  cudaDeviceSynchronize();
+  cudaFree(h->ws);
+  delete h;
+}
+
+const char* spec_verify_strerror(int code) {
+  switch (code) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_UNSUPPORTED: return "unsupported device (needs sm_103)";
+    case SPEC_ERR_CUDA: return "CUDA runtime error";
+    case SPEC_ERR_NOT_INIT: return "null handle";
+    case SPEC_ERR_CAPACITY: return "batch exceeds the handle's maxima";
+    case SPEC_ERR_DEVICE_STATUS: return "device status bits set";
+    default: return "unknown error code";
+  }
+}
+
+}  // extern "C"

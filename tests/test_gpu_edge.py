@@ -1,0 +1,149 @@
+"""Edge cases of the GPU verifier, each checked against the oracle or the
+documented status bits."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity import assert_parity, check_structure, compare, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def make_batch(logits, gammas, ids, temps, q=None, top_k=None, top_p=None, dtype="f32", seed=3,
+               flags=0):
+    gammas = np.asarray(gammas, np.int32)
+    B = gammas.size
+    cu = np.zeros(B + 1, np.int32)
+    np.cumsum(gammas, out=cu[1:])
+    logits = np.asarray(logits, np.float32)
+    if dtype == "bf16":
+        logits = synth.f32_to_bf16_bits(logits)
+    return dict(B=B, V=logits.shape[1], cu_num_draft=cu,
+                draft_token_ids=np.asarray(ids, np.int32).reshape(-1),
+                target_logits=logits, logits_dtype=dtype,
+                draft_probs=None if q is None else np.asarray(q, np.float32),
+                temperature=np.asarray(temps, np.float32),
+                top_k=None if top_k is None else np.asarray(top_k, np.int32),
+                top_p=None if top_p is None else np.asarray(top_p, np.float32),
+                seed=seed, request_base=0, flags=flags)
+
+
+def random_case(seed, B=40, V=300, gmax=6, dtype="f32", prob=True, ties=False):
+    rng = np.random.default_rng(seed)
+    g = rng.integers(0, gmax + 1, size=B)
+    N = int(g.sum())
+    logits = rng.normal(0, 2, size=(N + B, V))
+    if ties:
+        logits = np.round(logits)
+    q = rng.random((N, V)) ** 3
+    q /= q.sum(1, keepdims=True)
+    ids = np.array([rng.choice(V, p=q[n]) for n in range(N)], np.int32)
+    temps = rng.choice([0.0, 0.01, 0.5, 1.0, 3.0, 100.0], size=B)
+    tk = rng.choice([0, 1, 2, 7, V, V + 5], size=B)
+    tp = rng.choice([1.0, 0.001, 0.5, 0.9, 0.99], size=B)
+    return make_batch(logits, g, ids, temps, q if prob else None, tk, tp, dtype=dtype, seed=seed)
+
+
+def check(b, greedy=False):
+    gpu = run_gpu(b, greedy=greedy)
+    ref = oracle.verify(b)
+    check_structure(b, gpu)
+    assert_parity(compare(b, gpu, ref))
+    return gpu, ref
+
+
+@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("prob", [True, False])
+def test_random_mixed_settings(seed, dtype, prob):
+    gpu, _ = check(random_case(seed, dtype=dtype, prob=prob, ties=seed % 2 == 1))
+    assert gpu["status"] & ~np.uint32(0x8) == 0
+
+
+def test_empty_batch():
+    import torch
+
+    import speculative_decoding_rejection_02_gb300 as sv
+    ver = sv.Verifier(max_batch=4, max_rows=8, max_vocab=16)
+    dev = "cuda:0"
+    db = sv.DeviceBatch(cu_num_draft=torch.zeros(1, dtype=torch.int32, device=dev),
+                        draft_token_ids=torch.zeros(0, dtype=torch.int32, device=dev),
+                        target_logits=torch.zeros(0, 16, device=dev), draft_probs=None,
+                        temperature=torch.zeros(0, device=dev), N=0, V=16)
+    ver.run(db)
+    ver.greedy(db)
+    torch.cuda.synchronize()
+    assert ver.status() == 0
+    ver.close()
+
+
+def test_no_draft_tokens_bonus_only():
+    b = random_case(1, B=50, gmax=0)
+    assert int(b["cu_num_draft"][-1]) == 0
+    check(b)
+
+
+def test_single_token_vocabulary():
+    b = random_case(2, B=20, V=1)
+    gpu, _ = check(b)
+    assert np.all(gpu["out_tokens"][gpu["out_tokens"] >= 0] == 0)
+
+
+def test_long_rounds():
+    check(random_case(3, B=12, gmax=40, V=500))
+
+
+def test_minus_inf_logits():
+    rng = np.random.default_rng(4)
+    b = random_case(4, B=30, V=64)
+    logits = b["target_logits"]
+    logits[rng.random(logits.shape) < 0.7] = -np.inf
+    logits[:, 5] = 0.25  # every row keeps one finite logit
+    check(b)
+
+
+def test_uniform_rows_and_top_p():
+    b = random_case(5, B=30, V=100, dtype="bf16")
+    b["target_logits"][:] = synth.f32_to_bf16_bits(np.float32(1.5))
+    check(b)
+
+
+def test_invalid_token_ids_set_status():
+    b = random_case(6, B=30, V=80)
+    ids = b["draft_token_ids"]
+    ids[::5] = -1
+    ids[1::7] = 80
+    gpu, ref = check(b)
+    assert gpu["status"] & 0x4
+
+
+def test_nonfinite_rows_set_status():
+    b = random_case(7, B=30, V=80)
+    b["temperature"][:] = 1.0
+    b["target_logits"][3, 10] = np.nan
+    b["target_logits"][9, 1] = np.inf
+    gpu = run_gpu(b)
+    ref = oracle.verify(b)
+    assert gpu["status"] & 0x1
+    bad = (ref["req_status"] & 1) != 0
+    assert bad.sum() >= 1
+    for r in np.nonzero(bad)[0]:
+        assert gpu["num_accepted"][r] == 0
+    assert_parity(compare(b, gpu, ref, requests=np.nonzero(~bad)[0]))
+
+
+def test_bad_offsets_set_status():
+    b = random_case(8, B=6, V=50)
+    cu = b["cu_num_draft"].copy()
+    cu[2], cu[3] = cu[3], cu[2] - 1 if cu[2] > 0 else 0
+    b["cu_num_draft"] = cu
+    gpu = run_gpu(b)
+    assert gpu["status"] & 0x10
+
+
+def test_temperature_zero_ignores_draft_probs():
+    b = random_case(9, B=40, V=200)
+    b["temperature"][:] = 0
+    b["draft_probs"][:] = 0  # must never be read at temperature 0
+    check(b)
