@@ -73,6 +73,8 @@ extern "C" {
 #define SPEC_STATUS_BAD_TOKEN 0x4u      /* draft token id outside [0, V) */
 #define SPEC_STATUS_EMPTY_RESIDUAL 0x8u /* all residual weights 0: raced on p */
 #define SPEC_STATUS_BAD_OFFSETS 0x10u   /* cu_num_draft not 0 .. N, non-decreasing */
+#define SPEC_STATUS_TIMEOUT 0x20u       /* an on-chip pipeline wait gave up (the
+                                           outputs of the call are not valid) */
 
 /* Batch flags. */
 #define SPEC_FLAG_NAIVE 0x1u /* negative control: resample rejected positions

@@ -26,6 +26,7 @@ STATUS_NO_FINITE = 0x2
 STATUS_BAD_TOKEN = 0x4
 STATUS_EMPTY_RESIDUAL = 0x8
 STATUS_BAD_OFFSETS = 0x10
+STATUS_TIMEOUT = 0x20
 
 FLAG_NAIVE = 0x1
 

@@ -46,27 +46,21 @@ __device__ __forceinline__ SlicePartial load_partial(const SlicePartial* p) {
   return q;
 }
 
-// Write the statistics of one finished row and p at its draft token.
-__device__ void finish_row(const Params& P, long long row, int r, int cls, float m, int argmax,
-                           float z, float theta, float c) {
+// Write the statistics of one finished row and p at its draft token x
+// (x < 0: the row has no draft token; lx is the logit at x when 0 <= x < V).
+__device__ void finish_row_x(const Params& P, long long row, int cls, float m, int argmax,
+                             float z, float theta, float c, int x, float lx) {
   unsigned st = 0;
   if (cls != kArgmaxOnly) {
     if (m == INFINITY || !(z == z)) st |= SPEC_STATUS_NONFINITE;
     else if (m == -INFINITY) st |= SPEC_STATUS_NO_FINITE;
   }
   float p_x = 0.f;
-  const int c0 = __ldg(P.cu + r);
-  const int gamma = __ldg(P.cu + r + 1) - c0;
-  const long long i = row - ((long long)c0 + r);
-  if (i >= 0 && i < gamma && c0 + i < P.N) {
-    const int x = __ldg(P.ids + c0 + i);
-    if (x >= 0 && x < P.V) {
-      if (cls == kArgmaxOnly) {
-        p_x = (x == argmax) ? 1.f : 0.f;
-      } else if (st == 0) {
-        const float lx = load_logit(P, row, x);
-        p_x = (lx >= theta) ? exp2f((lx - m) * c) / z : 0.f;
-      }
+  if (x >= 0 && x < P.V) {
+    if (cls == kArgmaxOnly) {
+      p_x = (x == argmax) ? 1.f : 0.f;
+    } else if (st == 0) {
+      p_x = (lx >= theta) ? exp2f((lx - m) * c) / z : 0.f;
     }
   }
   RowStats s;
@@ -80,6 +74,21 @@ __device__ void finish_row(const Params& P, long long row, int r, int cls, float
   s.z = z;
   P.rows[row] = s;
   if (st) atomicOr(P.status, st);
+}
+
+// The draft token of target row `row` of request r (-1 for the last row).
+__device__ __forceinline__ int draft_of_row(const Params& P, long long row, int r) {
+  const int c0 = __ldg(P.cu + r);
+  const int gamma = __ldg(P.cu + r + 1) - c0;
+  const long long i = row - ((long long)c0 + r);
+  return (i >= 0 && i < gamma && c0 + i < P.N) ? __ldg(P.ids + c0 + i) : -1;
+}
+
+__device__ void finish_row(const Params& P, long long row, int r, int cls, float m, int argmax,
+                           float z, float theta, float c) {
+  const int x = draft_of_row(P, row, r);
+  const float lx = (x >= 0 && x < P.V) ? load_logit(P, row, x) : 0.f;
+  finish_row_x(P, row, cls, m, argmax, z, theta, c, x, lx);
 }
 
 // Row lookup shared by both kernels; returns false (and flags the status

@@ -1,0 +1,296 @@
+// Persistent, bulk-copy pipelined target-row pass for argmax-only and
+// plain-softmax rows (the same statistics as k_rows_stream, for rows whose
+// byte length is a multiple of 16).
+//
+// Each CTA owns rows blockIdx.x, blockIdx.x + gridDim.x, ... and streams
+// every row exactly once from HBM through a ring of shared-memory stages:
+//  * warp 8 (producer) looks up the next row's request and settings with
+//    warp-parallel loads while the current row streams, and lane 0 issues
+//    one 1-D bulk copy (TMA) per 16 KB stage, signalling an mbarrier;
+//  * warps 0..7 (consumers) wait on the stage, fold it into per-thread
+//    (max, lowest argmax, online sum of exp2((l - m) log2e / T)) in
+//    registers, capture the logit at the row's draft token, release the
+//    stage, and at the row's end reduce over the 256 consumers and write the
+//    row statistics and p(x).
+// No slice partials and no atomics: a row never leaves its CTA.
+#pragma once
+#include "common.cuh"
+#include "pipe.cuh"
+#include "rows.cuh"
+
+namespace sv {
+
+constexpr int kTmaConsumerWarps = 8;
+constexpr int kTmaConsumers = kTmaConsumerWarps * 32;
+constexpr int kTmaThreads = kTmaConsumers + 32;
+constexpr int kTmaStageBytes = 16384;
+constexpr int kTmaStages = 6;
+
+struct StageMeta {
+  long long row;  // -1: end of work
+  int cls;
+  float c;
+  int x;     // draft token of the row (-1: none)
+  int j0;    // first element of the stage within the row
+  int n;     // elements in the stage
+  int last;  // 1 on the row's last stage
+};
+
+constexpr size_t kTmaSmemBytes =
+    (size_t)kTmaStages * kTmaStageBytes + 2 * kTmaStages * sizeof(uint64_t) +
+    kTmaStages * sizeof(StageMeta);
+
+struct RowInfo {
+  long long row;
+  int cls;  // -1: skip this row
+  float c;
+  int x;
+};
+
+// Warp-parallel lookup of the request owning `row` and its settings (all 32
+// lanes call it; every lane gets the result). Two or three dependent rounds
+// of loads instead of a serial binary search.
+__device__ RowInfo warp_row_info(const Params& P, long long row) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, hi = P.B;  // answer in [lo, hi)
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) / 32;
+    const int probe = lo + lane * step;
+    const bool le = probe < hi && ((long long)__ldg(P.cu + probe) + probe <= row);
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, le);
+    const int last = m ? 31 - __clz(m) : 0;
+    lo = lo + last * step;
+    hi = min(hi, lo + step);
+  }
+  const int r = lo;
+  RowInfo info;
+  info.row = row;
+  int c0 = 0, c1 = 0, cls = kArgmaxOnly;
+  float T = 0.f;
+  if (lane == 0) {
+    c0 = __ldg(P.cu + r);
+    c1 = __ldg(P.cu + r + 1);
+    if (!P.greedy_call) T = __ldg(P.temp + r);
+  }
+  c0 = __shfl_sync(0xFFFFFFFFu, c0, 0);
+  c1 = __shfl_sync(0xFFFFFFFFu, c1, 0);
+  const long long i = row - ((long long)c0 + r);
+  if (c0 < 0 || c1 < c0 || c1 > P.N || i < 0 || i > c1 - c0) {
+    if (lane == 0) atomicOr(P.status, SPEC_STATUS_BAD_OFFSETS);
+    info.cls = -1;
+    info.c = 0.f;
+    info.x = -1;
+    return info;
+  }
+  int x = -1;
+  if (lane == 0) {
+    cls = row_class(P, r);
+    if (i < c1 - c0) x = __ldg(P.ids + c0 + i);
+  }
+  cls = __shfl_sync(0xFFFFFFFFu, cls, 0);
+  T = __shfl_sync(0xFFFFFFFFu, T, 0);
+  info.x = __shfl_sync(0xFFFFFFFFu, x, 0);
+  info.cls = (cls == kFiltered) ? -1 : cls;
+  info.c = (cls == kSoftmax) ? kLog2e / T : 0.f;
+  return info;
+}
+
+__global__ void __launch_bounds__(kTmaThreads, 2)
+k_rows_tma(Params P, long long R) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTmaStages * kTmaStageBytes);
+  uint64_t* empty = full + kTmaStages;
+  StageMeta* meta = reinterpret_cast<StageMeta*>(empty + kTmaStages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kTmaStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kTmaConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int esize = P.bf16 ? 2 : 4;
+  const long long row_bytes = (long long)P.V * esize;
+
+  if (warp == kTmaConsumerWarps) {
+    // ---------------- producer warp ----------------
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, issued_parity = 0;
+    bool ok = true;
+    const int nchunks = (int)((row_bytes + kTmaStageBytes - 1) / kTmaStageBytes);
+    long long row = blockIdx.x;
+    RowInfo cur;
+    cur.cls = -1;
+    while (row < R) {  // first row with work
+      cur = warp_row_info(P, row);
+      if (cur.cls >= 0) break;
+      row += gridDim.x;
+    }
+    while (row < R && ok) {
+      RowInfo next;
+      next.cls = -1;
+      long long nrow = row + gridDim.x;
+      bool next_done = false;
+      const char* src = (const char*)P.logits + row * row_bytes;
+      for (int ch = 0; ch < nchunks; ++ch) {
+        int waited = 1;
+        if (lane == 0) waited = mbar_wait(&empty[stage], phase ^ 1u) ? 1 : 0;
+        waited = __shfl_sync(0xFFFFFFFFu, waited, 0);
+        if (!waited) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          const long long off = (long long)ch * kTmaStageBytes;
+          const uint32_t bytes = (uint32_t)min((long long)kTmaStageBytes, row_bytes - off);
+          StageMeta& M = meta[stage];
+          M.row = row;
+          M.cls = cur.cls;
+          M.c = cur.c;
+          M.x = cur.x;
+          M.j0 = (int)(off / esize);
+          M.n = (int)(bytes / esize);
+          M.last = (ch == nchunks - 1) ? 1 : 0;
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          bulk_load(ring + (size_t)stage * kTmaStageBytes, src + off, bytes, &full[stage]);
+        }
+        issued |= 1u << stage;
+        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == kTmaStages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        if (ch == 0) {
+          // Look the next row up while this one streams.
+          while (nrow < R) {
+            next = warp_row_info(P, nrow);
+            if (next.cls >= 0) break;
+            nrow += gridDim.x;
+          }
+          next_done = true;
+        }
+      }
+      if (!next_done) break;
+      row = nrow;
+      cur = next;
+    }
+    if (lane == 0) {
+      // End-of-work marker, then make sure every issued copy has landed.
+      if (ok && mbar_wait(&empty[stage], phase ^ 1u)) {
+        meta[stage].row = -1;
+        mbar_arrive(&full[stage]);
+      } else {
+        atomicOr(P.status, SPEC_STATUS_TIMEOUT);
+      }
+      for (int s = 0; s < kTmaStages; ++s)
+        if (((issued >> s) & 1u) && !mbar_wait(&full[s], (issued_parity >> s) & 1u))
+          atomicOr(P.status, SPEC_STATUS_TIMEOUT);
+    }
+    return;
+  }
+
+  // ---------------- consumer warps ----------------
+  __shared__ float red_m[kTmaConsumerWarps], red_s[kTmaConsumerWarps];
+  __shared__ int red_i[kTmaConsumerWarps];
+  __shared__ float bc_m, s_lx;
+  __shared__ int bc_i;
+  const int tid = threadIdx.x;
+  const int epc = 16 / esize;
+  int stage = 0;
+  uint32_t phase = 0;
+  float vmax = -INFINITY, s = 0.f;
+  int imax = kNoIndex;
+  for (;;) {
+    int landed = 1;
+    if (lane == 0) landed = mbar_wait(&full[stage], phase) ? 1 : 0;
+    if (!__shfl_sync(0xFFFFFFFFu, landed, 0)) {
+      if (lane == 0) atomicOr(P.status, SPEC_STATUS_TIMEOUT);
+      break;
+    }
+    const StageMeta M = meta[stage];
+    if (M.row < 0) break;
+    const uint4* buf = reinterpret_cast<const uint4*>(ring + (size_t)stage * kTmaStageBytes);
+    const int nvec = M.n / epc;
+    const bool soft = (M.cls == kSoftmax);
+#pragma unroll 4
+    for (int v = tid; v < nvec; v += kTmaConsumers) {
+      float f[8];
+      const int n = unpack_chunk(buf[v], P.bf16, f);
+      const int jb = M.j0 + v * epc;
+      float m8 = f[0];
+#pragma unroll
+      for (int e = 1; e < 8; ++e)
+        if (e < n) m8 = fmaxf(m8, f[e]);
+      if (m8 > vmax || (imax == kNoIndex && m8 == m8)) {
+        if (soft && vmax > -INFINITY) s *= ex2((vmax - m8) * M.c);
+        int e = 0;
+        while (e < n - 1 && !(f[e] == m8)) ++e;
+        vmax = m8;
+        imax = jb + e;
+      }
+      if (soft && vmax > -INFINITY) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (e < n) s += ex2((f[e] - vmax) * M.c);
+      }
+      const int dx = M.x - jb;
+      if (dx >= 0 && dx < n) {
+        float lx = f[0];
+#pragma unroll
+        for (int e = 1; e < 8; ++e)
+          if (e == dx) lx = f[e];
+        s_lx = lx;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);
+    if (++stage == kTmaStages) {
+      stage = 0;
+      phase ^= 1u;
+    }
+    if (M.last) {
+      float m = vmax;
+      int a = imax;
+      warp_argmax(m, a);
+      if (lane == 0) {
+        red_m[warp] = m;
+        red_i[warp] = a;
+      }
+      named_sync(1, kTmaConsumers);
+      if (warp == 0) {
+        m = lane < kTmaConsumerWarps ? red_m[lane] : -INFINITY;
+        a = lane < kTmaConsumerWarps ? red_i[lane] : kNoIndex;
+        warp_argmax(m, a);
+        if (lane == 0) {
+          bc_m = m;
+          bc_i = a;
+        }
+      }
+      named_sync(1, kTmaConsumers);
+      m = bc_m;
+      a = bc_i;
+      float part = 0.f;
+      if (soft && vmax > -INFINITY && m > -INFINITY) part = s * ex2((vmax - m) * M.c);
+      part = warp_sum(part);
+      if (lane == 0) red_s[warp] = part;
+      named_sync(1, kTmaConsumers);
+      if (tid == 0) {
+        float z = 0.f;
+        if (soft)
+          for (int w = 0; w < kTmaConsumerWarps; ++w) z += red_s[w];
+        finish_row_x(P, M.row, M.cls, m, a == kNoIndex ? 0 : a, z, -INFINITY, M.c, M.x, s_lx);
+      }
+      named_sync(1, kTmaConsumers);
+      vmax = -INFINITY;
+      s = 0.f;
+      imax = kNoIndex;
+    }
+  }
+}
+
+}  // namespace sv

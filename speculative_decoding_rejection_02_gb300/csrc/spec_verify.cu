@@ -13,6 +13,7 @@
 #include "philox.cuh"
 #include "race.cuh"
 #include "rows.cuh"
+#include "rows_tma.cuh"
 
 struct spec_verify_handle {
   spec_verify_config cfg;
@@ -28,6 +29,7 @@ struct spec_verify_handle {
   int max_slices;
   cudaEvent_t phase[4];
   int n_phase;
+  int tma_blocks;  // resident CTAs of k_rows_tma on the device
 };
 
 namespace {
@@ -91,7 +93,15 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
     return SPEC_ERR_CAPACITY;
   const bool timed = h->n_phase >= 4;
   if (timed) cudaEventRecord(h->phase[0], stream);
-  sv::k_rows_stream<<<(unsigned)(R * P.slices_per_row), sv::kStreamThreads, 0, stream>>>(P);
+  const int esize = P.bf16 ? 2 : 4;
+  const bool rows_aligned = (((long long)b->V * esize) % 16 == 0) &&
+                            ((reinterpret_cast<uintptr_t>(b->target_logits) & 15) == 0);
+  if (rows_aligned && h->tma_blocks > 0) {
+    const long long grid = R < h->tma_blocks ? R : h->tma_blocks;
+    sv::k_rows_tma<<<(unsigned)grid, sv::kTmaThreads, sv::kTmaSmemBytes, stream>>>(P, R);
+  } else {
+    sv::k_rows_stream<<<(unsigned)(R * P.slices_per_row), sv::kStreamThreads, 0, stream>>>(P);
+  }
   if (!greedy && (P.top_k || P.top_p))
     sv::k_rows_filtered<<<(unsigned)R, sv::kFilterThreads, 0, stream>>>(P);
   if (timed) cudaEventRecord(h->phase[1], stream);
@@ -130,6 +140,15 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   if (!h) return SPEC_ERR_CUDA;
   h->cfg = *cfg;
   h->sm_count = prop.multiProcessorCount;
+  int per_sm = 0;
+  if (cudaFuncSetAttribute(sv::k_rows_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sv::kTmaSmemBytes) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv::k_rows_tma, sv::kTmaThreads,
+                                                    sv::kTmaSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    per_sm = 0;
+  }
+  h->tma_blocks = per_sm * prop.multiProcessorCount;
   h->max_slices = (cfg->max_vocab + sv::kSliceF32 - 1) / sv::kSliceF32;
 
   const size_t n_rows = (size_t)cfg->max_rows, n_b = (size_t)cfg->max_batch;
