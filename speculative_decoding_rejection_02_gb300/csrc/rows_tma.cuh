@@ -180,16 +180,21 @@ k_rows_tma(Params P, long long R) {
       cur = next;
     }
     if (lane == 0) {
-      // End-of-work marker, then make sure every issued copy has landed.
+      // Every issued copy has landed before the block may exit. This runs
+      // before the end marker: the marker advances a full barrier once more,
+      // after which the parity of that stage's last copy would name the
+      // (incomplete) current phase.
+      for (int s = 0; s < kTmaStages; ++s)
+        if (((issued >> s) & 1u) && !mbar_wait(&full[s], (issued_parity >> s) & 1u)) {
+          atomicOr(P.status, SPEC_STATUS_TIMEOUT);
+          ok = false;
+        }
       if (ok && mbar_wait(&empty[stage], phase ^ 1u)) {
         meta[stage].row = -1;
         mbar_arrive(&full[stage]);
       } else {
         atomicOr(P.status, SPEC_STATUS_TIMEOUT);
       }
-      for (int s = 0; s < kTmaStages; ++s)
-        if (((issued >> s) & 1u) && !mbar_wait(&full[s], (issued_parity >> s) & 1u))
-          atomicOr(P.status, SPEC_STATUS_TIMEOUT);
     }
     return;
   }
