@@ -56,6 +56,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="c5", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--B", type=int, default=None,
+                    help="resize the workload to B requests (profiling of small cases)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -286,7 +288,7 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    batch = synth.make(args.config)
+    batch = synth.make(args.config, B=args.B)
     B, V = batch["B"], batch["V"]
     batch["request_base"] = rank_request_base(rank, B)
     cu = batch["cu_num_draft"]

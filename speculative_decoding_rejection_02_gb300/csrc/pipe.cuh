@@ -1,13 +1,12 @@
 // Shared-memory pipeline primitives for sm_103a: mbarriers and 1-D bulk
 // asynchronous copies (cp.async.bulk, the TMA's untiled mode), in inline PTX.
-// Every wait is bounded: after kSpinLimit polls it gives up and reports it,
+// Every wait is bounded: after kTryLimit probes it gives up and reports it,
 // so a broken pipeline ends with a status bit instead of a hung GPU.
 #pragma once
 #include <cstdint>
 
 namespace sv {
 
-constexpr uint32_t kSpinLimit = 1u << 22;  // polls of ~64 ns: well under a second
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -45,13 +44,27 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Blocking probe: suspends the thread until the phase completes or about
+// `kSuspendHintNs` have passed.
+constexpr uint32_t kSuspendHintNs = 20000;
+constexpr uint32_t kTryLimit = 1u << 15;  // x 20 us: well under a second
+
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait until the phase with the given parity has completed; false on timeout.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_test(bar, parity)) return true;
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    __nanosleep(32);
-    if (mbar_test(bar, parity)) return true;
-  }
+  for (uint32_t i = 0; i < kTryLimit; ++i)
+    if (mbar_try(bar, parity)) return true;
   return false;
 }
 
