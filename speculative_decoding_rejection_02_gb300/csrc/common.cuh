@@ -2,6 +2,7 @@
 // workspace records, element decoding and block reductions.
 #pragma once
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/spec_verify.h"
@@ -87,6 +88,11 @@ struct Params {
 // ---------------------------------------------------------------------------
 // Element access
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ __nv_bfloat162 u32_as_bf162(uint32_t w) {
+  __nv_bfloat162 h;
+  memcpy(&h, &w, sizeof h);
+  return h;
+}
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

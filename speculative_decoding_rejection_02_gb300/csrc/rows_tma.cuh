@@ -4,13 +4,13 @@
 //
 // Each CTA owns rows blockIdx.x, blockIdx.x + gridDim.x, ... and streams
 // every row exactly once from HBM through a ring of shared-memory stages:
-//  * warp 8 (producer) looks up the next row's request and settings with
+//  * warp 16 (producer) looks up the next row's request and settings with
 //    warp-parallel loads while the current row streams, and lane 0 issues
-//    one 1-D bulk copy (TMA) per 16 KB stage, signalling an mbarrier;
-//  * warps 0..7 (consumers) wait on the stage, fold it into per-thread
+//    one 1-D bulk copy (TMA) per 32 KB stage, signalling an mbarrier;
+//  * warps 0..15 (consumers) wait on the stage, fold it into per-thread
 //    (max, lowest argmax, online sum of exp2((l - m) log2e / T)) in
 //    registers, capture the logit at the row's draft token, release the
-//    stage, and at the row's end reduce over the 256 consumers and write the
+//    stage, and at the row's end reduce over the 512 consumers and write the
 //    row statistics and p(x).
 // No slice partials and no atomics: a row never leaves its CTA.
 #pragma once
@@ -20,11 +20,12 @@
 
 namespace sv {
 
-constexpr int kTmaConsumerWarps = 8;
+constexpr int kTmaConsumerWarps = 16;
 constexpr int kTmaConsumers = kTmaConsumerWarps * 32;
 constexpr int kTmaThreads = kTmaConsumers + 32;
-constexpr int kTmaStageBytes = 16384;
-constexpr int kTmaStages = 6;
+constexpr int kTmaStageBytes = 32768;
+constexpr int kTmaStages = 3;
+constexpr int kTmaVecPerThread = kTmaStageBytes / 16 / kTmaConsumers;  // 4
 
 struct StageMeta {
   long long row;  // -1: end of work
@@ -222,34 +223,79 @@ k_rows_tma(Params P, long long R) {
     const uint4* buf = reinterpret_cast<const uint4*>(ring + (size_t)stage * kTmaStageBytes);
     const int nvec = M.n / epc;
     const bool soft = (M.cls == kSoftmax);
-#pragma unroll 4
-    for (int v = tid; v < nvec; v += kTmaConsumers) {
-      float f[8];
-      const int n = unpack_chunk(buf[v], P.bf16, f);
-      const int jb = M.j0 + v * epc;
-      float m8 = f[0];
+    // This thread's vectors of the stage, in increasing element order; the
+    // missing ones read as -inf (no max, no mass).
+    const uint32_t pad = P.bf16 ? 0xFF80FF80u : 0xFF800000u;
+    uint4 v[kTmaVecPerThread];
 #pragma unroll
-      for (int e = 1; e < 8; ++e)
-        if (e < n) m8 = fmaxf(m8, f[e]);
-      if (m8 > vmax || (imax == kNoIndex && m8 == m8)) {
-        if (soft && vmax > -INFINITY) s *= ex2((vmax - m8) * M.c);
-        int e = 0;
-        while (e < n - 1 && !(f[e] == m8)) ++e;
-        vmax = m8;
-        imax = jb + e;
+    for (int k = 0; k < kTmaVecPerThread; ++k) {
+      const int idx = tid + k * kTmaConsumers;
+      v[k] = idx < nvec ? buf[idx] : make_uint4(pad, pad, pad, pad);
+    }
+    float m32;
+    if (P.bf16) {
+      __nv_bfloat162 h = u32_as_bf162(v[0].x);
+#pragma unroll
+      for (int k = 0; k < kTmaVecPerThread; ++k) {
+        h = __hmax2(h, u32_as_bf162(v[k].x));
+        h = __hmax2(h, u32_as_bf162(v[k].y));
+        h = __hmax2(h, u32_as_bf162(v[k].z));
+        h = __hmax2(h, u32_as_bf162(v[k].w));
       }
-      if (soft && vmax > -INFINITY) {
+      m32 = fmaxf(__low2float(h), __high2float(h));
+    } else {
+      m32 = __uint_as_float(v[0].x);
+#pragma unroll
+      for (int k = 0; k < kTmaVecPerThread; ++k)
+        m32 = fmaxf(fmaxf(m32, fmaxf(__uint_as_float(v[k].x), __uint_as_float(v[k].y))),
+                    fmaxf(__uint_as_float(v[k].z), __uint_as_float(v[k].w)));
+    }
+    if (m32 > vmax || (imax == kNoIndex && m32 > -INFINITY)) {
+      // New running max (rare after the first stages): rescale, locate it.
+      if (soft && vmax > -INFINITY) s *= ex2((vmax - m32) * M.c);
+      int at = kNoIndex;
+#pragma unroll
+      for (int k = kTmaVecPerThread - 1; k >= 0; --k) {
+        float f[8];
+        const int n = unpack_chunk(v[k], P.bf16, f);
+#pragma unroll
+        for (int e = 7; e >= 0; --e)
+          if (e < n && f[e] == m32) at = M.j0 + (tid + k * kTmaConsumers) * epc + e;
+      }
+      vmax = m32;
+      imax = at;
+    }
+    if (soft && vmax > -INFINITY) {
+      float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < kTmaVecPerThread; ++k) {
+        float f[8];
+        const int n = unpack_chunk(v[k], P.bf16, f);
 #pragma unroll
         for (int e = 0; e < 8; ++e)
-          if (e < n) s += ex2((f[e] - vmax) * M.c);
+          if (e < n) a[e & 3] += ex2((f[e] - vmax) * M.c);
       }
-      const int dx = M.x - jb;
-      if (dx >= 0 && dx < n) {
-        float lx = f[0];
+      s += (a[0] + a[1]) + (a[2] + a[3]);
+    }
+    {
+      // The draft token's logit, captured by the thread that holds it.
+      const int dx = M.x - M.j0;
+      if (dx >= 0 && dx < M.n) {
+        const int vx = dx / epc;
+        if ((vx % kTmaConsumers) == tid) {
+          const int k = vx / kTmaConsumers;
+          uint4 vk = v[0];
 #pragma unroll
-        for (int e = 1; e < 8; ++e)
-          if (e == dx) lx = f[e];
-        s_lx = lx;
+          for (int t = 1; t < kTmaVecPerThread; ++t)
+            if (t == k) vk = v[t];
+          float f[8];
+          unpack_chunk(vk, P.bf16, f);
+          float lx = f[0];
+#pragma unroll
+          for (int e = 1; e < 8; ++e)
+            if (e == dx - vx * epc) lx = f[e];
+          s_lx = lx;
+        }
       }
     }
     __syncwarp();
