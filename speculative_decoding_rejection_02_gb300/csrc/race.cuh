@@ -44,7 +44,7 @@ __device__ __forceinline__ void race_weights(const Params& P, const RaceDesc& d,
   }
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const float p = (l[e] >= s.theta) ? exp2f((l[e] - s.m) * s.c) * s.inv_z : 0.f;
+    const float p = (l[e] >= s.theta) ? exp2f(fmaf(l[e], s.c, -(s.m * s.c))) * s.inv_z : 0.f;
     w[e] = (j0 + e < V) ? p : 0.f;
   }
   if (mode == kRaceResidual) {

@@ -60,7 +60,7 @@ __device__ void finish_row_x(const Params& P, long long row, int cls, float m, i
     if (cls == kArgmaxOnly) {
       p_x = (x == argmax) ? 1.f : 0.f;
     } else if (st == 0) {
-      p_x = (lx >= theta) ? exp2f((lx - m) * c) / z : 0.f;
+      p_x = (lx >= theta) ? exp2f(fmaf(lx, c, -(m * c))) / z : 0.f;
     }
   }
   RowStats s;
@@ -174,6 +174,7 @@ k_rows_stream(Params P) {
   block_argmax(m, am);
 
   float s = 0.f;
+  const float mc = m * c;
   if (cls == kSoftmax && m > -INFINITY) {
     if (aligned) {
 #pragma unroll
@@ -184,12 +185,12 @@ k_rows_stream(Params P) {
           const int n = unpack_chunk(v[k], P.bf16, f);
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            if (e < n) s += exp2f((f[e] - m) * c);
+            if (e < n) s += exp2f(fmaf(f[e], c, -mc));
         }
       }
     }
     for (int j = jt + threadIdx.x; j < j1; j += kStreamThreads)
-      s += exp2f((load_logit(P, row, j) - m) * c);
+      s += exp2f(fmaf(load_logit(P, row, j), c, -mc));
     s = block_sum(s);
   }
 
@@ -221,7 +222,7 @@ k_rows_stream(Params P) {
   if (cls == kSoftmax) {
     for (int t = lane; t < spr; t += 32) {
       const SlicePartial q = load_partial(P.partials + row * spr + t);
-      if (q.m > -INFINITY) z += q.s * exp2f((q.m - mm) * c);
+      if (q.m > -INFINITY) z += q.s * exp2f(q.m * c - mm * c);
     }
     z = warp_sum(z);
   }
@@ -310,6 +311,7 @@ k_rows_filtered(Params P) {
     return;
   }
 
+  const float mc = m * c;
   const long long key_space = bf16 ? (1ll << 16) : (1ll << 32);
   long long kk = 0;  // top-k key threshold (keep key >= kk)
   if (topk_on) {
@@ -325,7 +327,7 @@ k_rows_filtered(Params P) {
   }
   float zk = 0.f;
   row_for_each(P, row, [&](float v, int) {
-    if ((long long)elem_key(v, bf16) >= kk) zk += exp2f((v - m) * c);
+    if ((long long)elem_key(v, bf16) >= kk) zk += exp2f(fmaf(v, c, -mc));
   });
   zk = block_sum(zk);
 
@@ -338,7 +340,7 @@ k_rows_filtered(Params P) {
       float a = 0.f;
       row_for_each(P, row, [&](float v, int) {
         const long long k = elem_key(v, bf16);
-        if (k > mid && k >= kk) a += exp2f((v - m) * c);
+        if (k > mid && k >= kk) a += exp2f(fmaf(v, c, -mc));
       });
       a = block_sum(a);
       if (a < thr) hi = mid; else lo = mid;
@@ -347,7 +349,7 @@ k_rows_filtered(Params P) {
   }
   float z = 0.f;
   row_for_each(P, row, [&](float v, int) {
-    if ((long long)elem_key(v, bf16) >= kp) z += exp2f((v - m) * c);
+    if ((long long)elem_key(v, bf16) >= kp) z += exp2f(fmaf(v, c, -mc));
   });
   z = block_sum(z);
   if (threadIdx.x == 0) {

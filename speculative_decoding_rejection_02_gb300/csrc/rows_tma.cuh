@@ -96,6 +96,7 @@ __device__ RowInfo warp_row_info(const Params& P, long long row) {
   return info;
 }
 
+template <bool BF16>
 __global__ void __launch_bounds__(kTmaThreads, 2)
 k_rows_tma(Params P, long long R) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -114,7 +115,7 @@ k_rows_tma(Params P, long long R) {
   }
   __syncthreads();
 
-  const int esize = P.bf16 ? 2 : 4;
+  constexpr int esize = BF16 ? 2 : 4;
   const long long row_bytes = (long long)P.V * esize;
 
   if (warp == kTmaConsumerWarps) {
@@ -206,10 +207,12 @@ k_rows_tma(Params P, long long R) {
   __shared__ float bc_m, s_lx;
   __shared__ int bc_i;
   const int tid = threadIdx.x;
-  const int epc = 16 / esize;
+  constexpr int epc = 16 / esize;
   int stage = 0;
   uint32_t phase = 0;
-  float vmax = -INFINITY, s = 0.f;
+  // Running state of the current row: max, its lowest index, fl(max * c),
+  // and the sum of 2^(l c - fl(max c)) over this thread's elements.
+  float vmax = -INFINITY, vmc = 0.f, s = 0.f;
   int imax = kNoIndex;
   for (;;) {
     int landed = 1;
@@ -225,7 +228,7 @@ k_rows_tma(Params P, long long R) {
     const bool soft = (M.cls == kSoftmax);
     // This thread's vectors of the stage, in increasing element order; the
     // missing ones read as -inf (no max, no mass).
-    const uint32_t pad = P.bf16 ? 0xFF80FF80u : 0xFF800000u;
+    constexpr uint32_t pad = BF16 ? 0xFF80FF80u : 0xFF800000u;
     uint4 v[kTmaVecPerThread];
 #pragma unroll
     for (int k = 0; k < kTmaVecPerThread; ++k) {
@@ -233,7 +236,7 @@ k_rows_tma(Params P, long long R) {
       v[k] = idx < nvec ? buf[idx] : make_uint4(pad, pad, pad, pad);
     }
     float m32;
-    if (P.bf16) {
+    if (BF16) {
       __nv_bfloat162 h = u32_as_bf162(v[0].x);
 #pragma unroll
       for (int k = 0; k < kTmaVecPerThread; ++k) {
@@ -252,30 +255,53 @@ k_rows_tma(Params P, long long R) {
     }
     if (m32 > vmax || (imax == kNoIndex && m32 > -INFINITY)) {
       // New running max (rare after the first stages): rescale, locate it.
-      if (soft && vmax > -INFINITY) s *= ex2((vmax - m32) * M.c);
+      const float nmc = m32 * M.c;
+      if (soft && vmax > -INFINITY) s *= ex2(vmc - nmc);
       int at = kNoIndex;
 #pragma unroll
       for (int k = kTmaVecPerThread - 1; k >= 0; --k) {
         float f[8];
-        const int n = unpack_chunk(v[k], P.bf16, f);
+        unpack_chunk(v[k], BF16, f);
 #pragma unroll
-        for (int e = 7; e >= 0; --e)
-          if (e < n && f[e] == m32) at = M.j0 + (tid + k * kTmaConsumers) * epc + e;
+        for (int e = epc - 1; e >= 0; --e)
+          if (f[e] == m32) at = M.j0 + (tid + k * kTmaConsumers) * epc + e;
       }
       vmax = m32;
+      vmc = nmc;
       imax = at;
     }
     if (soft && vmax > -INFINITY) {
-      float a[4] = {0.f, 0.f, 0.f, 0.f};
+      const unsigned long long c2 = f2_pack(M.c, M.c);
+      const unsigned long long nmc2 = f2_pack(-vmc, -vmc);
+      unsigned long long acc0 = 0ull, acc1 = 0ull;  // (+0, +0) pairs
 #pragma unroll
       for (int k = 0; k < kTmaVecPerThread; ++k) {
-        float f[8];
-        const int n = unpack_chunk(v[k], P.bf16, f);
+        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+        if (BF16) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-          if (e < n) a[e & 3] += ex2((f[e] - vmax) * M.c);
+          for (int t = 0; t < 4; ++t) {
+            const unsigned long long x2 = f2_pack(bf16_lo(w[t]), bf16_hi(w[t]));
+            float z0, z1;
+            f2_unpack(f2_fma(x2, c2, nmc2), z0, z1);
+            const unsigned long long e2 = f2_pack(ex2(z0), ex2(z1));
+            if (t & 1) acc1 = f2_add(acc1, e2); else acc0 = f2_add(acc0, e2);
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < 4; t += 2) {
+            const unsigned long long x2 =
+                f2_pack(__uint_as_float(w[t]), __uint_as_float(w[t + 1]));
+            float z0, z1;
+            f2_unpack(f2_fma(x2, c2, nmc2), z0, z1);
+            const unsigned long long e2 = f2_pack(ex2(z0), ex2(z1));
+            if (t & 2) acc1 = f2_add(acc1, e2); else acc0 = f2_add(acc0, e2);
+          }
+        }
       }
-      s += (a[0] + a[1]) + (a[2] + a[3]);
+      float a0, a1, a2, a3;
+      f2_unpack(acc0, a0, a1);
+      f2_unpack(acc1, a2, a3);
+      s += (a0 + a1) + (a2 + a3);
     }
     {
       // The draft token's logit, captured by the thread that holds it.
@@ -289,10 +315,10 @@ k_rows_tma(Params P, long long R) {
           for (int t = 1; t < kTmaVecPerThread; ++t)
             if (t == k) vk = v[t];
           float f[8];
-          unpack_chunk(vk, P.bf16, f);
+          unpack_chunk(vk, BF16, f);
           float lx = f[0];
 #pragma unroll
-          for (int e = 1; e < 8; ++e)
+          for (int e = 1; e < epc; ++e)
             if (e == dx - vx * epc) lx = f[e];
           s_lx = lx;
         }
@@ -325,8 +351,9 @@ k_rows_tma(Params P, long long R) {
       named_sync(1, kTmaConsumers);
       m = bc_m;
       a = bc_i;
+      const float mc = m * M.c;
       float part = 0.f;
-      if (soft && vmax > -INFINITY && m > -INFINITY) part = s * ex2((vmax - m) * M.c);
+      if (soft && vmax > -INFINITY && m > -INFINITY) part = s * ex2(vmc - mc);
       part = warp_sum(part);
       if (lane == 0) red_s[warp] = part;
       named_sync(1, kTmaConsumers);
@@ -338,6 +365,7 @@ k_rows_tma(Params P, long long R) {
       }
       named_sync(1, kTmaConsumers);
       vmax = -INFINITY;
+      vmc = 0.f;
       s = 0.f;
       imax = kNoIndex;
     }

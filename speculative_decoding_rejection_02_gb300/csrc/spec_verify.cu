@@ -98,7 +98,10 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
                             ((reinterpret_cast<uintptr_t>(b->target_logits) & 15) == 0);
   if (rows_aligned && h->tma_blocks > 0) {
     const long long grid = R < h->tma_blocks ? R : h->tma_blocks;
-    sv::k_rows_tma<<<(unsigned)grid, sv::kTmaThreads, sv::kTmaSmemBytes, stream>>>(P, R);
+    if (P.bf16)
+      sv::k_rows_tma<true><<<(unsigned)grid, sv::kTmaThreads, sv::kTmaSmemBytes, stream>>>(P, R);
+    else
+      sv::k_rows_tma<false><<<(unsigned)grid, sv::kTmaThreads, sv::kTmaSmemBytes, stream>>>(P, R);
   } else {
     sv::k_rows_stream<<<(unsigned)(R * P.slices_per_row), sv::kStreamThreads, 0, stream>>>(P);
   }
@@ -141,9 +144,12 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   h->cfg = *cfg;
   h->sm_count = prop.multiProcessorCount;
   int per_sm = 0;
-  if (cudaFuncSetAttribute(sv::k_rows_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(sv::k_rows_tma<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)sv::kTmaSmemBytes) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv::k_rows_tma, sv::kTmaThreads,
+      cudaFuncSetAttribute(sv::k_rows_tma<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sv::kTmaSmemBytes) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv::k_rows_tma<true>,
+                                                    sv::kTmaThreads,
                                                     sv::kTmaSmemBytes) != cudaSuccess) {
     cudaGetLastError();
     per_sm = 0;
