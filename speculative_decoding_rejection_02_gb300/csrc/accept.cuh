@@ -1,104 +1,130 @@
-// Accept scan, one thread per request (velog "드래프트가 제안하고 타깃이
+// Accept scan, one warp per request (velog "드래프트가 제안하고 타깃이
 // 판정한다": positions are judged left to right with independent uniforms;
 // x_i is accepted iff u_i <= p_i(x_i) / q_i(x_i), and the first rejection
 // ends the round; "vLLM 커널은 이 규칙을 어떻게 옮겼나": the test is
 // q > 0 and p / q >= u with float64 u; "기본값 greedy 드래프트에서도 분포가
 // 지켜질까": no draft_probs means q(x) = 1, temperature 0 means argmax match).
 //
-// Writes the accepted prefix, num_accepted and -1 padding, emits the argmax
-// at k* for temperature-0 requests, and leaves a race descriptor for the
-// others (residual at the first rejection, or the bonus token from the last
-// row).
+// Lane i judges position i (chunks of 32 for longer rounds); the first
+// rejection is a ballot. The warp writes the accepted prefix, num_accepted,
+// -1 padding and, at temperature 0, the argmax at k*. For the other requests
+// it appends the request to the race list and seeds the race's running best
+// with the score of the row's argmax token (a valid candidate, so a lower
+// bound of the winner's score that lets the race skip most entries).
 #pragma once
 #include "common.cuh"
 #include "philox.cuh"
+#include "race.cuh"
 
 namespace sv {
 
-__global__ void k_accept(Params P) {
-  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+constexpr int kAcceptWarps = 8;  // requests per CTA
+
+__global__ void __launch_bounds__(kAcceptWarps * 32)
+k_accept(Params P) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kAcceptWarps + (threadIdx.x >> 5);
   if (r >= P.B) return;
   RaceDesc d;
   d.mode = kRaceNone;
   d.kstar = 0;
   d.x = -1;
   d.row = 0;
-  P.race_best[r] = 0ull;
-  P.race_counter[r] = 0u;
+  d.qrow = 0;
 
-  const int c0 = P.cu[r], c1 = P.cu[r + 1];
+  const int c0 = __ldg(P.cu + r), c1 = __ldg(P.cu + r + 1);
   bool bad = (c0 < 0 || c1 < c0 || c1 > P.N);
   if (r == 0 && c0 != 0) bad = true;
   if (r == P.B - 1 && c1 != P.N) bad = true;
   if (bad) {
-    atomicOr(P.status, SPEC_STATUS_BAD_OFFSETS);
-    P.num_accepted[r] = 0;
-    P.race[r] = d;
+    if (lane == 0) {
+      atomicOr(P.status, SPEC_STATUS_BAD_OFFSETS);
+      P.num_accepted[r] = 0;
+      P.race[r] = d;
+    }
     return;
   }
   const int gamma = c1 - c0;
   const long long row0 = (long long)c0 + r;
-  const bool greedy = P.greedy_call || !(P.temp[r] > 0.f);
+  const bool greedy = P.greedy_call || !(__ldg(P.temp + r) > 0.f);
 
   unsigned st = 0;
-  for (int i = 0; i <= gamma; ++i) st |= P.rows[row0 + i].status;
+  for (int i = lane; i <= gamma; i += 32) st |= P.rows[row0 + i].status;
+  st = __reduce_or_sync(0xFFFFFFFFu, st);
   if (!greedy && (st & (SPEC_STATUS_NONFINITE | SPEC_STATUS_NO_FINITE))) {
     // Unusable target row: nothing is emitted for this request.
-    for (int i = 0; i <= gamma; ++i) P.out_tokens[row0 + i] = -1;
+    for (int i = lane; i <= gamma; i += 32) P.out_tokens[row0 + i] = -1;
     if (P.p_at_draft)
-      for (int i = 0; i < gamma; ++i) P.p_at_draft[c0 + i] = 0.f;
-    P.num_accepted[r] = 0;
-    P.race[r] = d;
+      for (int i = lane; i < gamma; i += 32) P.p_at_draft[c0 + i] = 0.f;
+    if (lane == 0) {
+      P.num_accepted[r] = 0;
+      P.race[r] = d;
+    }
     return;
   }
 
   const long long greq = P.req_base + r;
   int k = gamma;
-  for (int i = 0; i < gamma; ++i) {
-    const int x = P.ids[c0 + i];
-    const bool valid = (x >= 0 && x < P.V);
-    if (!valid) st |= SPEC_STATUS_BAD_TOKEN;
-    const RowStats s = P.rows[row0 + i];
-    float pa;
-    bool ok;
-    if (greedy) {
-      ok = (x == s.argmax);
-      pa = ok ? 1.f : 0.f;
-    } else {
-      pa = s.p_x;
-      if (k == gamma) {
-        const float qx = P.q ? (valid ? __ldg(P.q + (long long)(c0 + i) * P.V + x) : 0.f) : 1.f;
-        const double u = accept_uniform(P.seed, greq, i);
-        ok = (qx > 0.f) && ((double)pa / (double)qx >= u);
+  unsigned bad_tok = 0;
+  for (int base = 0; base < gamma; base += 32) {
+    const int i = base + lane;
+    bool ok = true;
+    if (i < gamma) {
+      const int x = __ldg(P.ids + c0 + i);
+      const bool valid = (x >= 0 && x < P.V);
+      bad_tok |= valid ? 0u : 1u;
+      const RowStats s = P.rows[row0 + i];
+      float pa;
+      if (greedy) {
+        ok = (x == s.argmax);
+        pa = ok ? 1.f : 0.f;
       } else {
-        ok = false;
+        pa = s.p_x;
+        const float qx =
+            P.q ? (valid ? __ldg(P.q + (long long)(c0 + i) * P.V + x) : 0.f) : 1.f;
+        if (k == gamma) {
+          const double u = accept_uniform(P.seed, greq, i);
+          ok = (qx > 0.f) && ((double)pa / (double)qx >= u);
+        }
       }
+      if (P.p_at_draft) P.p_at_draft[c0 + i] = pa;
     }
-    if (P.p_at_draft) P.p_at_draft[c0 + i] = pa;
-    if (!ok && k == gamma) k = i;
+    const unsigned rej = __ballot_sync(0xFFFFFFFFu, !ok);
+    if (k == gamma && rej) k = base + __ffs(rej) - 1;
   }
+  if (__reduce_or_sync(0xFFFFFFFFu, bad_tok)) st |= SPEC_STATUS_BAD_TOKEN;
 
-  for (int i = 0; i < k; ++i) P.out_tokens[row0 + i] = P.ids[c0 + i];
-  for (int i = k + 1; i <= gamma; ++i) P.out_tokens[row0 + i] = -1;
-  if (greedy) {
-    P.out_tokens[row0 + k] = P.rows[row0 + k].argmax;
-  } else {
-    P.out_tokens[row0 + k] = -1;  // written by the race
-    d.kstar = k;
-    d.row = (int)(row0 + k);
-    if (k < gamma) {
-      const int x = P.ids[c0 + k];
-      d.x = x;
-      if (P.flags & SPEC_FLAG_NAIVE) d.mode = kRaceP;
-      else if (P.q) d.mode = kRaceResidual;
-      else d.mode = (x >= 0 && x < P.V) ? kRaceMasked : kRaceP;
-    } else {
-      d.mode = kRaceP;
-    }
+  for (int i = lane; i <= gamma; i += 32) {
+    int t = -1;
+    if (i < k) t = __ldg(P.ids + c0 + i);
+    else if (i == k && greedy) t = P.rows[row0 + k].argmax;
+    P.out_tokens[row0 + i] = t;
   }
-  P.num_accepted[r] = k;
-  P.race[r] = d;
-  if (st & (SPEC_STATUS_BAD_TOKEN)) atomicOr(P.status, SPEC_STATUS_BAD_TOKEN);
+  if (lane == 0) {
+    P.num_accepted[r] = k;
+    unsigned long long seed_best = 0ull;
+    if (!greedy) {
+      d.kstar = k;
+      d.row = (int)(row0 + k);
+      d.qrow = c0 + k;
+      if (k < gamma) {
+        const int x = __ldg(P.ids + c0 + k);
+        d.x = x;
+        if (P.flags & SPEC_FLAG_NAIVE) d.mode = kRaceP;
+        else if (P.q) d.mode = kRaceResidual;
+        else d.mode = (x >= 0 && x < P.V) ? kRaceMasked : kRaceP;
+      } else {
+        d.mode = kRaceP;
+      }
+      const RowStats s = P.rows[d.row];
+      seed_best = race_candidate(P, d, s, greq, s.argmax);
+      P.race_list[atomicAdd(P.race_count, 1u)] = r;
+    }
+    P.race[r] = d;
+    P.race_best[r] = seed_best;
+    P.race_counter[r] = 0u;
+    if (st & SPEC_STATUS_BAD_TOKEN) atomicOr(P.status, SPEC_STATUS_BAD_TOKEN);
+  }
 }
 
 }  // namespace sv

@@ -52,7 +52,8 @@ struct RaceDesc {
   int mode;    // RaceMode
   int kstar;   // position of the drawn token (0 .. gamma)
   int x;       // draft token at kstar (masked in kRaceMasked)
-  int row;     // target row of kstar
+  int row;     // target row of kstar (= output slot)
+  int qrow;    // draft_probs row of kstar (= cu[r] + kstar)
 };
 
 // Device view of one call.
@@ -80,6 +81,8 @@ struct Params {
   RaceDesc* race;
   unsigned long long* race_best;
   unsigned* race_counter;
+  int* race_list;        // requests with a token to draw (order not fixed)
+  unsigned* race_count;  // entries in race_list
   unsigned* status;
   int slices_per_row;
   int race_slices;

@@ -6,136 +6,200 @@
 // with the draft token masked; "드래프트가 제안하고 타깃이 판정한다": the bonus
 // token comes from p of the last row).
 //
-// The chosen row is cut into slices; one CTA scores one slice: 4 consecutive
-// entries share one Philox4x32-10 draw, E = -ln U, score = w / E, the lowest
-// index wins ties. Groups whose largest weight cannot beat the thread's best
-// even with the smallest possible E skip the draw (exact pruning). Slice
-// winners meet in one 64-bit atomicMax of (score bits, ~index); the last CTA
-// of the request writes the token.
+// Persistent kernel over tasks (request, 8192-entry slice), slice-major so
+// that later slices of a request start from the best score its earlier
+// slices published. Four consecutive entries share one Philox4x32-10 draw;
+// E = -ln U, score = w / E, the lowest index wins ties. A group whose largest
+// weight w satisfies w / E_floor <= best (E_floor below the smallest E a
+// race uniform can give) cannot produce a winner and skips the draw: exact
+// pruning. Slice winners meet in one 64-bit atomicMax of (score bits,
+// ~index); the last task of a request writes the token.
 #pragma once
 #include "common.cuh"
 #include "philox.cuh"
+#include "pipe.cuh"
 
 namespace sv {
 
 constexpr int kRaceThreads = 256;
-constexpr int kRaceSlice = 8192;  // entries per CTA (multiple of 4)
+constexpr int kRaceSlice = 8192;  // entries per task (multiple of 4 * kRaceThreads)
+constexpr int kRaceGroups = kRaceSlice / 4 / kRaceThreads;  // groups of 4 per thread
 // Below the smallest E = -ln(1 - 2^-24) ~ 5.96e-8 that a race uniform can give.
 constexpr float kEFloor = 5.0e-8f;
 
-// Weights of entries 4g .. 4g+3 of the race row (0 beyond V).
-__device__ __forceinline__ void race_weights(const Params& P, const RaceDesc& d,
-                                             const RowStats& s, long long qrow, int mode,
-                                             uint32_t g, float w[4]) {
-  const int V = P.V;
-  const int j0 = (int)(g * 4u);
-  float l[4];
-  const long long at = (long long)d.row * V + j0;
-  const uintptr_t addr = reinterpret_cast<uintptr_t>(P.logits) + (uintptr_t)(at * (P.bf16 ? 2 : 4));
-  if (j0 + 3 < V && P.bf16 && (addr & 7) == 0) {
-    const uint2 b = __ldg((const uint2*)((const unsigned short*)P.logits + at));
-    l[0] = bf16_lo(b.x); l[1] = bf16_hi(b.x); l[2] = bf16_lo(b.y); l[3] = bf16_hi(b.y);
-  } else if (j0 + 3 < V && !P.bf16 && (addr & 15) == 0) {
-    const float4 f = __ldg((const float4*)((const float*)P.logits + at));
-    l[0] = f.x; l[1] = f.y; l[2] = f.z; l[3] = f.w;
-  } else {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) l[e] = (j0 + e < V) ? load_logit(P, d.row, j0 + e) : -INFINITY;
-  }
+// p of one entry of a race row (0 if cut by top-k / top-p).
+__device__ __forceinline__ float race_p(float l, const RowStats& s, float mc) {
+  return (l >= s.theta) ? ex2(fmaf(l, s.c, -mc)) * s.inv_z : 0.f;
+}
+
+// The race weight of entry j given p and q.
+__device__ __forceinline__ float race_w(float p, float q, int j, int mode, int x) {
+  if (mode == kRaceResidual) return fmaxf(p - q, 0.f);
+  if (mode == kRaceMasked) return (j == x) ? 0.f : p;
+  return p;
+}
+
+__device__ __forceinline__ float race_score(float w, uint32_t word) {
+  const float E = -logf(race_uniform_from_word(word));
+  return w / E;
+}
+
+__device__ __forceinline__ unsigned long long race_pack(float score, int j) {
+  return ((unsigned long long)__float_as_uint(score) << 32) | (0xFFFFFFFFu - (uint32_t)j);
+}
+
+// One candidate entry j, scored exactly as the race scores it: the packed
+// (score, ~j), or 0 when w_j = 0.
+__device__ unsigned long long race_candidate(const Params& P, const RaceDesc& d,
+                                             const RowStats& s, long long greq, int j) {
+  if (j < 0 || j >= P.V || !(s.z > 0.f)) return 0ull;
+  const float l = load_logit(P, d.row, j);
+  const float q = (d.mode == kRaceResidual) ? __ldg(P.q + (long long)d.qrow * P.V + j) : 0.f;
+  const float w = race_w(race_p(l, s, s.m * s.c), q, j, d.mode, d.x);
+  if (!(w > 0.f)) return 0ull;
+  const uint4 r = race_words(P.seed, greq, d.kstar, (uint32_t)j >> 2);
+  const uint32_t words[4] = {r.x, r.y, r.z, r.w};
+  return race_pack(race_score(w, words[j & 3]), j);
+}
+
+// Score one group of 4 entries held in registers.
+__device__ __forceinline__ void race_group(const Params& P, const RaceDesc& d, const RowStats& s,
+                                           float mc, int mode, long long greq, uint32_t g,
+                                           const float l[4], const float q[4], float& best,
+                                           int& best_j) {
+  float w[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const float p = (l[e] >= s.theta) ? exp2f(fmaf(l[e], s.c, -(s.m * s.c))) * s.inv_z : 0.f;
-    w[e] = (j0 + e < V) ? p : 0.f;
+    const int j = (int)(g * 4u) + e;
+    w[e] = (j < P.V) ? race_w(race_p(l[e], s, mc), q[e], j, mode, d.x) : 0.f;
   }
-  if (mode == kRaceResidual) {
-    const float* qr = P.q + qrow * V;
+  const float wmax = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
+  if (!(wmax > 0.f) || wmax / kEFloor <= best) return;
+  const uint4 r = race_words(P.seed, greq, d.kstar, g);
+  const uint32_t words[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (j0 + e < V) w[e] = fmaxf(w[e] - __ldg(qr + j0 + e), 0.f);
-  } else if (mode == kRaceMasked) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (j0 + e == d.x) w[e] = 0.f;
+  for (int e = 0; e < 4; ++e) {
+    if (w[e] > 0.f) {
+      const float sc = race_score(w[e], words[e]);
+      const int j = (int)(g * 4u) + e;
+      if (sc > best || (sc == best && j < best_j)) {
+        best = sc;
+        best_j = j;
+      }
+    }
   }
 }
 
-// Score groups [g_begin, g_end) with this thread's stride; keeps the best.
-__device__ __forceinline__ void race_scan(const Params& P, const RaceDesc& d, const RowStats& s,
-                                          long long qrow, int mode, long long greq,
-                                          uint32_t g_begin, uint32_t g_end, float& best,
-                                          int& best_j) {
-  for (uint32_t g = g_begin + threadIdx.x; g < g_end; g += blockDim.x) {
-    float w[4];
-    race_weights(P, d, s, qrow, mode, g, w);
-    const float wmax = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
-    if (!(wmax > 0.f) || wmax / kEFloor <= best) continue;
-    const uint4 r = race_words(P.seed, greq, d.kstar, g);
-    const uint32_t words[4] = {r.x, r.y, r.z, r.w};
+// Groups [g0, g1) of the race row, this thread's share; loads for
+// kRaceGroups groups are issued before any of them is scored.
+__device__ void race_range(const Params& P, const RaceDesc& d, const RowStats& s, int mode,
+                           long long greq, uint32_t g0, uint32_t g1, float& best, int& best_j) {
+  const int V = P.V;
+  const float mc = s.m * s.c;
+  const long long lrow = (long long)d.row * V;
+  const long long qoff = (long long)d.qrow * V;
+  const uintptr_t la = reinterpret_cast<uintptr_t>(P.logits);
+  const uintptr_t qa = reinterpret_cast<uintptr_t>(P.q);
+  const bool vec = (V % 4 == 0) && ((la & 15) == 0) && (mode != kRaceResidual || (qa & 15) == 0);
+  const uint32_t stride = blockDim.x;
+  for (uint32_t gb = g0 + threadIdx.x; gb < g1; gb += stride * kRaceGroups) {
+    float l[kRaceGroups][4], q[kRaceGroups][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      if (w[e] > 0.f) {
-        const float E = -logf(race_uniform_from_word(words[e]));
-        const float sc = w[e] / E;
-        if (sc > best) {
-          best = sc;
-          best_j = (int)(g * 4u) + e;
+    for (int k = 0; k < kRaceGroups; ++k) {
+      const uint32_t g = gb + (uint32_t)k * stride;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        l[k][e] = -INFINITY;
+        q[k][e] = 0.f;
+      }
+      if (g < g1) {
+        const int j0 = (int)(g * 4u);
+        if (vec && j0 + 3 < V) {
+          if (P.bf16) {
+            const uint2 b = __ldg(reinterpret_cast<const uint2*>(
+                reinterpret_cast<const unsigned short*>(P.logits) + lrow + j0));
+            l[k][0] = bf16_lo(b.x);
+            l[k][1] = bf16_hi(b.x);
+            l[k][2] = bf16_lo(b.y);
+            l[k][3] = bf16_hi(b.y);
+          } else {
+            const float4 f = __ldg(reinterpret_cast<const float4*>(
+                reinterpret_cast<const float*>(P.logits) + lrow + j0));
+            l[k][0] = f.x; l[k][1] = f.y; l[k][2] = f.z; l[k][3] = f.w;
+          }
+          if (mode == kRaceResidual) {
+            const float4 f = __ldg(reinterpret_cast<const float4*>(P.q + qoff + j0));
+            q[k][0] = f.x; q[k][1] = f.y; q[k][2] = f.z; q[k][3] = f.w;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (j0 + e < V) {
+              l[k][e] = load_logit(P, d.row, j0 + e);
+              if (mode == kRaceResidual) q[k][e] = __ldg(P.q + qoff + j0 + e);
+            }
+          }
         }
       }
+    }
+#pragma unroll
+    for (int k = 0; k < kRaceGroups; ++k) {
+      const uint32_t g = gb + (uint32_t)k * stride;
+      if (g < g1) race_group(P, d, s, mc, mode, greq, g, l[k], q[k], best, best_j);
     }
   }
 }
 
 __global__ void __launch_bounds__(kRaceThreads)
 k_race(Params P) {
-  const int r = blockIdx.x / P.race_slices;
-  const int sl = blockIdx.x % P.race_slices;
-  const RaceDesc d = P.race[r];
-  if (d.mode == kRaceNone) return;
-  const RowStats s = P.rows[d.row];
-  const long long qrow = (long long)d.row - r;  // draft position index cu[r] + k*
-  const long long greq = P.req_base + r;
+  const unsigned n_race = *P.race_count;
+  const unsigned tasks = n_race * (unsigned)P.race_slices;
   const uint32_t groups = (uint32_t)((P.V + 3) / 4);
-  const uint32_t g0 = (uint32_t)sl * (kRaceSlice / 4);
-  const uint32_t g1 = min(groups, g0 + (uint32_t)(kRaceSlice / 4));
-
-  float best = 0.f;
-  int best_j = kNoIndex;
-  race_scan(P, d, s, qrow, d.mode, greq, g0, g1, best, best_j);
-  block_argmax(best, best_j);
-
   __shared__ int s_last;
-  if (threadIdx.x == 0) {
-    if (best_j != kNoIndex && best > 0.f) {
-      const unsigned long long packed =
-          ((unsigned long long)__float_as_uint(best) << 32) | (0xFFFFFFFFu - (uint32_t)best_j);
-      atomicMax(P.race_best + r, packed);
-    }
-    __threadfence();
-    const unsigned prev = atomicAdd(P.race_counter + r, 1u);
-    s_last = (prev == (unsigned)P.race_slices - 1u);
-  }
-  __syncthreads();
-  if (!s_last) return;
   __shared__ unsigned long long s_packed;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    s_packed = atomicAdd(P.race_best + r, 0ull);
+  for (unsigned t = blockIdx.x; t < tasks; t += gridDim.x) {
+    const int slice = (int)(t / n_race);
+    const int r = P.race_list[t % n_race];
+    const RaceDesc d = P.race[r];
+    const RowStats s = P.rows[d.row];
+    const long long greq = P.req_base + r;
+    const unsigned long long lb = __ldcg(P.race_best + r);
+    float best = lb ? __uint_as_float((uint32_t)(lb >> 32)) : 0.f;
+    int best_j = lb ? (int)(0xFFFFFFFFu - (uint32_t)lb) : kNoIndex;
+    const uint32_t g0 = (uint32_t)slice * (kRaceSlice / 4);
+    const uint32_t g1 = min(groups, g0 + (uint32_t)(kRaceSlice / 4));
+    if (s.z > 0.f) race_range(P, d, s, d.mode, greq, g0, g1, best, best_j);
+    block_argmax(best, best_j);
+    if (threadIdx.x == 0) {
+      if (best_j != kNoIndex && best > 0.f) atomicMax(P.race_best + r, race_pack(best, best_j));
+      __threadfence();
+      const unsigned prev = atomicAdd(P.race_counter + r, 1u);
+      s_last = (prev == (unsigned)P.race_slices - 1u);
+    }
+    __syncthreads();
+    if (s_last) {
+      if (threadIdx.x == 0) {
+        __threadfence();
+        s_packed = atomicAdd(P.race_best + r, 0ull);
+      }
+      __syncthreads();
+      const unsigned long long packed = s_packed;
+      int tok;
+      if (packed == 0ull) {
+        // Every weight was 0 (rounding only): draw from p over the whole row.
+        float b2 = 0.f;
+        int j2 = kNoIndex;
+        if (s.z > 0.f) race_range(P, d, s, kRaceP, greq, 0u, groups, b2, j2);
+        block_argmax(b2, j2);
+        tok = (j2 == kNoIndex) ? 0 : j2;
+        if (threadIdx.x == 0) atomicOr(P.status, SPEC_STATUS_EMPTY_RESIDUAL);
+      } else {
+        tok = (int)(0xFFFFFFFFu - (uint32_t)(packed & 0xFFFFFFFFull));
+      }
+      if (threadIdx.x == 0) P.out_tokens[d.row] = tok;
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  const unsigned long long packed = s_packed;
-  int tok;
-  if (packed == 0ull) {
-    // Every weight was 0 (rounding only): draw from p over the whole row.
-    float b2 = 0.f;
-    int j2 = kNoIndex;
-    race_scan(P, d, s, qrow, kRaceP, greq, 0u, groups, b2, j2);
-    block_argmax(b2, j2);
-    tok = (j2 == kNoIndex) ? 0 : j2;
-    if (threadIdx.x == 0) atomicOr(P.status, SPEC_STATUS_EMPTY_RESIDUAL);
-  } else {
-    tok = (int)(0xFFFFFFFFu - (uint32_t)(packed & 0xFFFFFFFFull));
-  }
-  if (threadIdx.x == 0) P.out_tokens[d.row] = tok;
 }
 
 }  // namespace sv

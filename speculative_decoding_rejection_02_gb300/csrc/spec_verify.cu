@@ -25,8 +25,11 @@ struct spec_verify_handle {
   sv::RaceDesc* race;
   unsigned long long* race_best;
   unsigned* race_counter;
+  int* race_list;
+  unsigned* race_count;
   unsigned* status;
   int max_slices;
+  int race_blocks;  // resident CTAs of k_race on the device
   cudaEvent_t phase[4];
   int n_phase;
   int tma_blocks;  // resident CTAs of k_rows_tma on the device
@@ -83,6 +86,8 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   P.race = h->race;
   P.race_best = h->race_best;
   P.race_counter = h->race_counter;
+  P.race_list = h->race_list;
+  P.race_count = h->race_count;
   P.status = h->status;
   const int slice = P.bf16 ? sv::kSliceBf16 : sv::kSliceF32;
   P.slices_per_row = (b->V + slice - 1) / slice;
@@ -93,6 +98,8 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
     return SPEC_ERR_CAPACITY;
   const bool timed = h->n_phase >= 4;
   if (timed) cudaEventRecord(h->phase[0], stream);
+  if (!greedy && cudaMemsetAsync(h->race_count, 0, sizeof(unsigned), stream) != cudaSuccess)
+    return SPEC_ERR_CUDA;
   const int esize = P.bf16 ? 2 : 4;
   const bool rows_aligned = (((long long)b->V * esize) % 16 == 0) &&
                             ((reinterpret_cast<uintptr_t>(b->target_logits) & 15) == 0);
@@ -108,10 +115,14 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   if (!greedy && (P.top_k || P.top_p))
     sv::k_rows_filtered<<<(unsigned)R, sv::kFilterThreads, 0, stream>>>(P);
   if (timed) cudaEventRecord(h->phase[1], stream);
-  sv::k_accept<<<(b->B + 127) / 128, 128, 0, stream>>>(P);
+  sv::k_accept<<<(b->B + sv::kAcceptWarps - 1) / sv::kAcceptWarps, sv::kAcceptWarps * 32, 0,
+                 stream>>>(P);
   if (timed) cudaEventRecord(h->phase[2], stream);
-  if (!greedy)
-    sv::k_race<<<(unsigned)((long long)b->B * P.race_slices), sv::kRaceThreads, 0, stream>>>(P);
+  if (!greedy) {
+    const long long want = (long long)b->B * P.race_slices;
+    const long long grid = want < h->race_blocks ? want : h->race_blocks;
+    sv::k_race<<<(unsigned)grid, sv::kRaceThreads, 0, stream>>>(P);
+  }
   if (timed) cudaEventRecord(h->phase[3], stream);
   if (cudaPeekAtLastError() != cudaSuccess) {
     cudaGetLastError();
@@ -155,6 +166,13 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
     per_sm = 0;
   }
   h->tma_blocks = per_sm * prop.multiProcessorCount;
+  int race_per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&race_per_sm, sv::k_race, sv::kRaceThreads,
+                                                    0) != cudaSuccess) {
+    cudaGetLastError();
+    race_per_sm = 1;
+  }
+  h->race_blocks = (race_per_sm > 0 ? race_per_sm : 1) * prop.multiProcessorCount;
   h->max_slices = (cfg->max_vocab + sv::kSliceF32 - 1) / sv::kSliceF32;
 
   const size_t n_rows = (size_t)cfg->max_rows, n_b = (size_t)cfg->max_batch;
@@ -164,8 +182,11 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   const size_t sz_race = align_up(n_b * sizeof(sv::RaceDesc));
   const size_t sz_best = align_up(n_b * sizeof(unsigned long long));
   const size_t sz_rccnt = align_up(n_b * sizeof(unsigned));
+  const size_t sz_list = align_up(n_b * sizeof(int));
+  const size_t sz_lcnt = align_up(sizeof(unsigned));
   const size_t sz_stat = align_up(sizeof(unsigned));
-  const size_t total = sz_rows + sz_part + sz_rcnt + sz_race + sz_best + sz_rccnt + sz_stat;
+  const size_t total = sz_rows + sz_part + sz_rcnt + sz_race + sz_best + sz_rccnt + sz_list +
+                       sz_lcnt + sz_stat;
   if (cudaMalloc(&h->ws, total) != cudaSuccess) {
     delete h;
     return SPEC_ERR_CUDA;
@@ -182,6 +203,8 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   h->race = (sv::RaceDesc*)p; p += sz_race;
   h->race_best = (unsigned long long*)p; p += sz_best;
   h->race_counter = (unsigned*)p; p += sz_rccnt;
+  h->race_list = (int*)p; p += sz_list;
+  h->race_count = (unsigned*)p; p += sz_lcnt;
   h->status = (unsigned*)p;
   *out = h;
   return SPEC_OK;
