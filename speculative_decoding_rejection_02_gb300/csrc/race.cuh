@@ -6,9 +6,9 @@
 // with the draft token masked; "드래프트가 제안하고 타깃이 판정한다": the bonus
 // token comes from p of the last row).
 //
-// Persistent kernel over tasks (request, 8192-entry slice), slice-major so
-// that later slices of a request start from the best score its earlier
-// slices published. Four consecutive entries share one Philox4x32-10 draw;
+// One CTA per task (request, 8192-entry slice), numbered slice-major so that
+// later slices of a request start from the best score its earlier slices
+// published (and from the argmax token's score seeded by the accept scan). Four consecutive entries share one Philox4x32-10 draw;
 // E = -ln U, score = w / E, the lowest index wins ties. A group whose largest
 // weight w satisfies w / E_floor <= best (E_floor below the smallest E a
 // race uniform can give) cannot produce a winner and skips the draw: exact
@@ -23,7 +23,7 @@ namespace sv {
 
 constexpr int kRaceThreads = 256;
 constexpr int kRaceSlice = 8192;  // entries per task (multiple of 4 * kRaceThreads)
-constexpr int kRaceGroups = kRaceSlice / 4 / kRaceThreads;  // groups of 4 per thread
+constexpr int kRaceGroups = 4;  // groups of 4 entries loaded together per thread
 // Below the smallest E = -ln(1 - 2^-24) ~ 5.96e-8 that a race uniform can give.
 constexpr float kEFloor = 5.0e-8f;
 
@@ -153,53 +153,50 @@ __device__ void race_range(const Params& P, const RaceDesc& d, const RowStats& s
 __global__ void __launch_bounds__(kRaceThreads)
 k_race(Params P) {
   const unsigned n_race = *P.race_count;
-  const unsigned tasks = n_race * (unsigned)P.race_slices;
+  const unsigned t = blockIdx.x;
+  if (t >= n_race * (unsigned)P.race_slices) return;
   const uint32_t groups = (uint32_t)((P.V + 3) / 4);
   __shared__ int s_last;
   __shared__ unsigned long long s_packed;
-  for (unsigned t = blockIdx.x; t < tasks; t += gridDim.x) {
-    const int slice = (int)(t / n_race);
-    const int r = P.race_list[t % n_race];
-    const RaceDesc d = P.race[r];
-    const RowStats s = P.rows[d.row];
-    const long long greq = P.req_base + r;
-    const unsigned long long lb = __ldcg(P.race_best + r);
-    float best = lb ? __uint_as_float((uint32_t)(lb >> 32)) : 0.f;
-    int best_j = lb ? (int)(0xFFFFFFFFu - (uint32_t)lb) : kNoIndex;
-    const uint32_t g0 = (uint32_t)slice * (kRaceSlice / 4);
-    const uint32_t g1 = min(groups, g0 + (uint32_t)(kRaceSlice / 4));
-    if (s.z > 0.f) race_range(P, d, s, d.mode, greq, g0, g1, best, best_j);
-    block_argmax(best, best_j);
-    if (threadIdx.x == 0) {
-      if (best_j != kNoIndex && best > 0.f) atomicMax(P.race_best + r, race_pack(best, best_j));
-      __threadfence();
-      const unsigned prev = atomicAdd(P.race_counter + r, 1u);
-      s_last = (prev == (unsigned)P.race_slices - 1u);
-    }
-    __syncthreads();
-    if (s_last) {
-      if (threadIdx.x == 0) {
-        __threadfence();
-        s_packed = atomicAdd(P.race_best + r, 0ull);
-      }
-      __syncthreads();
-      const unsigned long long packed = s_packed;
-      int tok;
-      if (packed == 0ull) {
-        // Every weight was 0 (rounding only): draw from p over the whole row.
-        float b2 = 0.f;
-        int j2 = kNoIndex;
-        if (s.z > 0.f) race_range(P, d, s, kRaceP, greq, 0u, groups, b2, j2);
-        block_argmax(b2, j2);
-        tok = (j2 == kNoIndex) ? 0 : j2;
-        if (threadIdx.x == 0) atomicOr(P.status, SPEC_STATUS_EMPTY_RESIDUAL);
-      } else {
-        tok = (int)(0xFFFFFFFFu - (uint32_t)(packed & 0xFFFFFFFFull));
-      }
-      if (threadIdx.x == 0) P.out_tokens[d.row] = tok;
-    }
-    __syncthreads();
+  const int slice = (int)(t / n_race);
+  const int r = P.race_list[t % n_race];
+  const RaceDesc d = P.race[r];
+  const RowStats s = P.rows[d.row];
+  const long long greq = P.req_base + r;
+  const unsigned long long lb = __ldcg(P.race_best + r);
+  float best = lb ? __uint_as_float((uint32_t)(lb >> 32)) : 0.f;
+  int best_j = lb ? (int)(0xFFFFFFFFu - (uint32_t)lb) : kNoIndex;
+  const uint32_t g0 = (uint32_t)slice * (kRaceSlice / 4);
+  const uint32_t g1 = min(groups, g0 + (uint32_t)(kRaceSlice / 4));
+  if (s.z > 0.f) race_range(P, d, s, d.mode, greq, g0, g1, best, best_j);
+  block_argmax(best, best_j);
+  if (threadIdx.x == 0) {
+    if (best_j != kNoIndex && best > 0.f) atomicMax(P.race_best + r, race_pack(best, best_j));
+    __threadfence();
+    const unsigned prev = atomicAdd(P.race_counter + r, 1u);
+    s_last = (prev == (unsigned)P.race_slices - 1u);
   }
+  __syncthreads();
+  if (!s_last) return;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_packed = atomicAdd(P.race_best + r, 0ull);
+  }
+  __syncthreads();
+  const unsigned long long packed = s_packed;
+  int tok;
+  if (packed == 0ull) {
+    // Every weight was 0 (rounding only): draw from p over the whole row.
+    float b2 = 0.f;
+    int j2 = kNoIndex;
+    if (s.z > 0.f) race_range(P, d, s, kRaceP, greq, 0u, groups, b2, j2);
+    block_argmax(b2, j2);
+    tok = (j2 == kNoIndex) ? 0 : j2;
+    if (threadIdx.x == 0) atomicOr(P.status, SPEC_STATUS_EMPTY_RESIDUAL);
+  } else {
+    tok = (int)(0xFFFFFFFFu - (uint32_t)(packed & 0xFFFFFFFFull));
+  }
+  if (threadIdx.x == 0) P.out_tokens[d.row] = tok;
 }
 
 }  // namespace sv

@@ -119,9 +119,7 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
                  stream>>>(P);
   if (timed) cudaEventRecord(h->phase[2], stream);
   if (!greedy) {
-    const long long want = (long long)b->B * P.race_slices;
-    const long long grid = want < h->race_blocks ? want : h->race_blocks;
-    sv::k_race<<<(unsigned)grid, sv::kRaceThreads, 0, stream>>>(P);
+    sv::k_race<<<(unsigned)((long long)b->B * P.race_slices), sv::kRaceThreads, 0, stream>>>(P);
   }
   if (timed) cudaEventRecord(h->phase[3], stream);
   if (cudaPeekAtLastError() != cudaSuccess) {
