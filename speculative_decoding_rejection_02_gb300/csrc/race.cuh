@@ -10,9 +10,11 @@
 // later slices of a request start from the best score its earlier slices
 // published (and from the argmax token's score seeded by the accept scan). Four consecutive entries share one Philox4x32-10 draw;
 // E = -ln U, score = w / E, the lowest index wins ties. A group whose largest
-// weight w satisfies w / E_floor <= best (E_floor below the smallest E a
-// race uniform can give) cannot produce a winner and skips the draw: exact
-// pruning. Slice winners meet in one 64-bit atomicMax of (score bits,
+// weight w satisfies w * kInvEMin <= best (kInvEMin above 1 / the smallest E
+// a race uniform can give) cannot produce a winner and skips the draw: exact
+// pruning. Since w <= p and p grows with the logit, the same bound (with a
+// factor-2 margin for rounding) becomes a logit threshold, so most entries
+// cost one compare. Slice winners meet in one 64-bit atomicMax of (score bits,
 // ~index); the last task of a request writes the token.
 #pragma once
 #include "common.cuh"
@@ -24,8 +26,9 @@ namespace sv {
 constexpr int kRaceThreads = 256;
 constexpr int kRaceSlice = 8192;  // entries per task (multiple of 4 * kRaceThreads)
 constexpr int kRaceGroups = 4;  // groups of 4 entries loaded together per thread
-// Below the smallest E = -ln(1 - 2^-24) ~ 5.96e-8 that a race uniform can give.
-constexpr float kEFloor = 5.0e-8f;
+// Above 1 / E_min, E_min = -ln(1 - 2^-24) ~ 5.96e-8 the smallest E a race
+// uniform can give: no entry scores more than w * kInvEMin.
+constexpr float kInvEMin = 1.7e7f;
 
 // p of one entry of a race row (0 if cut by top-k / top-p).
 __device__ __forceinline__ float race_p(float l, const RowStats& s, float mc) {
@@ -62,6 +65,18 @@ __device__ unsigned long long race_candidate(const Params& P, const RaceDesc& d,
   return race_pack(race_score(w, words[j & 3]), j);
 }
 
+// A logit at or below the returned value has p * kInvEMin <= best / 2 (p
+// is ex2(l c - m c) / Z), so neither its p nor its weight can reach `best`:
+//   l <= (log2(best Z / (2 kInvEMin)) + m c) / c.
+// The factor 2 absorbs every rounding of this bound and of p itself.
+// -inf (nothing skipped) while there is no best yet, the theta cut aside.
+__device__ __forceinline__ float race_logit_floor(const RowStats& s, float mc, float best) {
+  float t = -INFINITY;
+  if (best > 0.f && s.c > 0.f) t = (log2f(best * s.z / (2.f * kInvEMin)) + mc) / s.c;
+  // entries below theta have p = 0
+  return fmaxf(t, nextafterf(s.theta, -INFINITY));
+}
+
 // Score one group of 4 entries held in registers.
 __device__ __forceinline__ void race_group(const Params& P, const RaceDesc& d, const RowStats& s,
                                            float mc, int mode, long long greq, uint32_t g,
@@ -74,7 +89,7 @@ __device__ __forceinline__ void race_group(const Params& P, const RaceDesc& d, c
     w[e] = (j < P.V) ? race_w(race_p(l[e], s, mc), q[e], j, mode, d.x) : 0.f;
   }
   const float wmax = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
-  if (!(wmax > 0.f) || wmax / kEFloor <= best) return;
+  if (!(wmax > 0.f) || wmax * kInvEMin <= best) return;
   const uint4 r = race_words(P.seed, greq, d.kstar, g);
   const uint32_t words[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
@@ -102,6 +117,8 @@ __device__ void race_range(const Params& P, const RaceDesc& d, const RowStats& s
   const uintptr_t qa = reinterpret_cast<uintptr_t>(P.q);
   const bool vec = (V % 4 == 0) && ((la & 15) == 0) && (mode != kRaceResidual || (qa & 15) == 0);
   const uint32_t stride = blockDim.x;
+  // Groups whose largest logit is <= lthr cannot hold a winner.
+  float lthr = race_logit_floor(s, mc, best);
   for (uint32_t gb = g0 + threadIdx.x; gb < g1; gb += stride * kRaceGroups) {
     float l[kRaceGroups][4], q[kRaceGroups][4];
 #pragma unroll
@@ -145,7 +162,12 @@ __device__ void race_range(const Params& P, const RaceDesc& d, const RowStats& s
 #pragma unroll
     for (int k = 0; k < kRaceGroups; ++k) {
       const uint32_t g = gb + (uint32_t)k * stride;
-      if (g < g1) race_group(P, d, s, mc, mode, greq, g, l[k], q[k], best, best_j);
+      const float lmax = fmaxf(fmaxf(l[k][0], l[k][1]), fmaxf(l[k][2], l[k][3]));
+      if (g < g1 && lmax > lthr) {
+        const float before = best;
+        race_group(P, d, s, mc, mode, greq, g, l[k], q[k], best, best_j);
+        if (best != before) lthr = race_logit_floor(s, mc, best);
+      }
     }
   }
 }
