@@ -77,34 +77,6 @@ __device__ __forceinline__ float race_logit_floor(const RowStats& s, float mc, f
   return fmaxf(t, nextafterf(s.theta, -INFINITY));
 }
 
-// Score one group of 4 entries held in registers.
-__device__ __forceinline__ void race_group(const Params& P, const RaceDesc& d, const RowStats& s,
-                                           float mc, int mode, long long greq, uint32_t g,
-                                           const float l[4], const float q[4], float& best,
-                                           int& best_j) {
-  float w[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int j = (int)(g * 4u) + e;
-    w[e] = (j < P.V) ? race_w(race_p(l[e], s, mc), q[e], j, mode, d.x) : 0.f;
-  }
-  const float wmax = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
-  if (!(wmax > 0.f) || wmax * kInvEMin <= best) return;
-  const uint4 r = race_words(P.seed, greq, d.kstar, g);
-  const uint32_t words[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    if (w[e] > 0.f) {
-      const float sc = race_score(w[e], words[e]);
-      const int j = (int)(g * 4u) + e;
-      if (sc > best || (sc == best && j < best_j)) {
-        best = sc;
-        best_j = j;
-      }
-    }
-  }
-}
-
 // Groups [g0, g1) of the race row, this thread's share; loads for
 // kRaceGroups groups are issued before any of them is scored.
 __device__ void race_range(const Params& P, const RaceDesc& d, const RowStats& s, int mode,
@@ -159,15 +131,55 @@ __device__ void race_range(const Params& P, const RaceDesc& d, const RowStats& s
         }
       }
     }
+    // Decide every group of the batch against one snapshot of the best
+    // (the best only grows, so an older snapshot prunes less but never
+    // wrongly), then draw the needed groups' Philox words as independent
+    // chains, then score.
+    const float cut = best;
+    float w[kRaceGroups][4];
+    bool need[kRaceGroups];
+    bool any = false;
 #pragma unroll
     for (int k = 0; k < kRaceGroups; ++k) {
       const uint32_t g = gb + (uint32_t)k * stride;
       const float lmax = fmaxf(fmaxf(l[k][0], l[k][1]), fmaxf(l[k][2], l[k][3]));
+      need[k] = false;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) w[k][e] = 0.f;
       if (g < g1 && lmax > lthr) {
-        const float before = best;
-        race_group(P, d, s, mc, mode, greq, g, l[k], q[k], best, best_j);
-        if (best != before) lthr = race_logit_floor(s, mc, best);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = (int)(g * 4u) + e;
+          w[k][e] = (j < V) ? race_w(race_p(l[k][e], s, mc), q[k][e], j, mode, d.x) : 0.f;
+        }
+        const float wmax = fmaxf(fmaxf(w[k][0], w[k][1]), fmaxf(w[k][2], w[k][3]));
+        need[k] = (wmax > 0.f) && (wmax * kInvEMin > cut);
       }
+      any |= need[k];
+    }
+    if (any) {
+      uint4 rw[kRaceGroups];
+#pragma unroll
+      for (int k = 0; k < kRaceGroups; ++k)
+        rw[k] = race_words(P.seed, greq, d.kstar, gb + (uint32_t)k * stride);
+#pragma unroll
+      for (int k = 0; k < kRaceGroups; ++k) {
+        if (!need[k]) continue;
+        const uint32_t g = gb + (uint32_t)k * stride;
+        const uint32_t words[4] = {rw[k].x, rw[k].y, rw[k].z, rw[k].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (w[k][e] > 0.f) {
+            const float sc = race_score(w[k][e], words[e]);
+            const int j = (int)(g * 4u) + e;
+            if (sc > best || (sc == best && j < best_j)) {
+              best = sc;
+              best_j = j;
+            }
+          }
+        }
+      }
+      if (best != cut) lthr = race_logit_floor(s, mc, best);
     }
   }
 }
