@@ -79,8 +79,15 @@ __device__ __forceinline__ float race_logit_floor(const RowStats& s, float mc, f
 
 // Groups [g0, g1) of the race row, this thread's share; loads for
 // kRaceGroups groups are issued before any of them is scored.
+struct RaceItem {
+  uint32_t g;  // group (entries 4g .. 4g+3)
+  float w[4];  // their weights
+};
+
+// `queue`: shared memory for 32 * kRaceGroups items per warp of the block.
 __device__ void race_range(const Params& P, const RaceDesc& d, const RowStats& s, int mode,
-                           long long greq, uint32_t g0, uint32_t g1, float& best, int& best_j) {
+                           long long greq, uint32_t g0, uint32_t g1, float& best, int& best_j,
+                           RaceItem* queue) {
   const int V = P.V;
   const float mc = s.m * s.c;
   const long long lrow = (long long)d.row * V;
@@ -91,7 +98,11 @@ __device__ void race_range(const Params& P, const RaceDesc& d, const RowStats& s
   const uint32_t stride = blockDim.x;
   // Groups whose largest logit is <= lthr cannot hold a winner.
   float lthr = race_logit_floor(s, mc, best);
-  for (uint32_t gb = g0 + threadIdx.x; gb < g1; gb += stride * kRaceGroups) {
+  // Every lane runs the same number of batches (warp-wide ballots inside).
+  const uint32_t span = stride * kRaceGroups;
+  const uint32_t first = g0 + (threadIdx.x & ~31u);
+  for (uint32_t gw = first; gw < g1; gw += span) {
+    const uint32_t gb = gw + (threadIdx.x & 31u);
     float l[kRaceGroups][4], q[kRaceGroups][4];
 #pragma unroll
     for (int k = 0; k < kRaceGroups; ++k) {
@@ -133,54 +144,58 @@ __device__ void race_range(const Params& P, const RaceDesc& d, const RowStats& s
     }
     // Decide every group of the batch against one snapshot of the best
     // (the best only grows, so an older snapshot prunes less but never
-    // wrongly), then draw the needed groups' Philox words as independent
-    // chains, then score.
+    // wrongly). Groups that still need their Philox words are packed into
+    // a per-warp queue, so that the draws run on dense lanes instead of
+    // following each lane's divergent decisions.
     const float cut = best;
-    float w[kRaceGroups][4];
-    bool need[kRaceGroups];
-    bool any = false;
+    const int lane = threadIdx.x & 31;
+    RaceItem* qw = queue + (threadIdx.x >> 5) * (32 * kRaceGroups);
+    int n_items = 0;
 #pragma unroll
     for (int k = 0; k < kRaceGroups; ++k) {
       const uint32_t g = gb + (uint32_t)k * stride;
       const float lmax = fmaxf(fmaxf(l[k][0], l[k][1]), fmaxf(l[k][2], l[k][3]));
-      need[k] = false;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) w[k][e] = 0.f;
+      bool need = false;
+      float w[4] = {0.f, 0.f, 0.f, 0.f};
       if (g < g1 && lmax > lthr) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = (int)(g * 4u) + e;
-          w[k][e] = (j < V) ? race_w(race_p(l[k][e], s, mc), q[k][e], j, mode, d.x) : 0.f;
+          w[e] = (j < V) ? race_w(race_p(l[k][e], s, mc), q[k][e], j, mode, d.x) : 0.f;
         }
-        const float wmax = fmaxf(fmaxf(w[k][0], w[k][1]), fmaxf(w[k][2], w[k][3]));
-        need[k] = (wmax > 0.f) && (wmax * kInvEMin > cut);
+        const float wmax = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
+        need = (wmax > 0.f) && (wmax * kInvEMin > cut);
       }
-      any |= need[k];
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, need);
+      if (need) {
+        RaceItem& it = qw[n_items + __popc(m & ((1u << lane) - 1u))];
+        it.g = g;
+        it.w[0] = w[0]; it.w[1] = w[1]; it.w[2] = w[2]; it.w[3] = w[3];
+      }
+      n_items += __popc(m);
     }
-    if (any) {
-      uint4 rw[kRaceGroups];
+    __syncwarp();
+    for (int t = lane; t < n_items; t += 32) {
+      const RaceItem it = qw[t];
+      const uint4 r = race_words(P.seed, greq, d.kstar, it.g);
+      const uint32_t words[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-      for (int k = 0; k < kRaceGroups; ++k)
-        rw[k] = race_words(P.seed, greq, d.kstar, gb + (uint32_t)k * stride);
-#pragma unroll
-      for (int k = 0; k < kRaceGroups; ++k) {
-        if (!need[k]) continue;
-        const uint32_t g = gb + (uint32_t)k * stride;
-        const uint32_t words[4] = {rw[k].x, rw[k].y, rw[k].z, rw[k].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (w[k][e] > 0.f) {
-            const float sc = race_score(w[k][e], words[e]);
-            const int j = (int)(g * 4u) + e;
-            if (sc > best || (sc == best && j < best_j)) {
-              best = sc;
-              best_j = j;
-            }
+      for (int e = 0; e < 4; ++e) {
+        if (it.w[e] * kInvEMin > cut) {
+          const float sc = race_score(it.w[e], words[e]);
+          const int j = (int)(it.g * 4u) + e;
+          if (sc > best || (sc == best && j < best_j)) {
+            best = sc;
+            best_j = j;
           }
         }
       }
-      if (best != cut) lthr = race_logit_floor(s, mc, best);
     }
+    __syncwarp();
+    // One best for the whole warp: the next batch prunes against it.
+    warp_argmax(best, best_j);
+    if (best_j == kNoIndex) best = 0.f;
+    if (best != cut) lthr = race_logit_floor(s, mc, best);
   }
 }
 
@@ -192,6 +207,7 @@ k_race(Params P) {
   const uint32_t groups = (uint32_t)((P.V + 3) / 4);
   __shared__ int s_last;
   __shared__ unsigned long long s_packed;
+  __shared__ RaceItem queue[kRaceThreads * kRaceGroups];
   const int slice = (int)(t / n_race);
   const int r = P.race_list[t % n_race];
   const RaceDesc d = P.race[r];
@@ -202,7 +218,7 @@ k_race(Params P) {
   int best_j = lb ? (int)(0xFFFFFFFFu - (uint32_t)lb) : kNoIndex;
   const uint32_t g0 = (uint32_t)slice * (kRaceSlice / 4);
   const uint32_t g1 = min(groups, g0 + (uint32_t)(kRaceSlice / 4));
-  if (s.z > 0.f) race_range(P, d, s, d.mode, greq, g0, g1, best, best_j);
+  if (s.z > 0.f) race_range(P, d, s, d.mode, greq, g0, g1, best, best_j, queue);
   block_argmax(best, best_j);
   if (threadIdx.x == 0) {
     if (best_j != kNoIndex && best > 0.f) atomicMax(P.race_best + r, race_pack(best, best_j));
@@ -223,7 +239,7 @@ k_race(Params P) {
     // Every weight was 0 (rounding only): draw from p over the whole row.
     float b2 = 0.f;
     int j2 = kNoIndex;
-    if (s.z > 0.f) race_range(P, d, s, kRaceP, greq, 0u, groups, b2, j2);
+    if (s.z > 0.f) race_range(P, d, s, kRaceP, greq, 0u, groups, b2, j2, queue);
     block_argmax(b2, j2);
     tok = (j2 == kNoIndex) ? 0 : j2;
     if (threadIdx.x == 0) atomicOr(P.status, SPEC_STATUS_EMPTY_RESIDUAL);
