@@ -117,8 +117,23 @@ k_accept(Params P) {
         d.mode = kRaceP;
       }
       const RowStats s = P.rows[d.row];
-      seed_best = race_candidate(P, d, s, greq, s.argmax);
-      P.race_list[atomicAdd(P.race_count, 1u)] = r;
+      const RaceView v = race_view(P, r, d.row, d.qrow, d.kstar, d.mode, d.x, s.m, s.c,
+                                   s.inv_z, s.theta, s.z);
+      seed_best = race_candidate(P, v, s.argmax);
+      RaceTask task;
+      task.r = r;
+      task.row = d.row;
+      task.qrow = d.qrow;
+      task.kstar = d.kstar;
+      task.mode = d.mode;
+      task.x = d.x;
+      task.m = s.m;
+      task.c = s.c;
+      task.inv_z = s.inv_z;
+      task.theta = s.theta;
+      task.z = s.z;
+      task.pad = 0;
+      P.race_list[atomicAdd(P.race_count, 1u)] = task;
     }
     P.race[r] = d;
     P.race_best[r] = seed_best;

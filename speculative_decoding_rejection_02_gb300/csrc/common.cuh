@@ -56,6 +56,19 @@ struct RaceDesc {
   int qrow;    // draft_probs row of kstar (= cu[r] + kstar)
 };
 
+// Everything one race task needs, written by the accept scan so that a race
+// CTA starts its copies after a single dependent load.
+struct RaceTask {
+  int r;        // request
+  int row;      // target row of k* (= output slot)
+  int qrow;     // draft_probs row of k*
+  int kstar;    // position k*
+  int mode;     // RaceMode
+  int x;        // draft token at k*
+  float m, c, inv_z, theta, z;  // RowStats of the row
+  int pad;
+};
+
 // Device view of one call.
 struct Params {
   int B, V, N;
@@ -81,7 +94,7 @@ struct Params {
   RaceDesc* race;
   unsigned long long* race_best;
   unsigned* race_counter;
-  int* race_list;        // requests with a token to draw (order not fixed)
+  RaceTask* race_list;   // requests with a token to draw (order not fixed)
   unsigned* race_count;  // entries in race_list
   unsigned* status;
   int slices_per_row;

@@ -8,14 +8,18 @@
 //
 // One CTA per task (request, 8192-entry slice), numbered slice-major so that
 // later slices of a request start from the best score its earlier slices
-// published (and from the argmax token's score seeded by the accept scan). Four consecutive entries share one Philox4x32-10 draw;
-// E = -ln U, score = w / E, the lowest index wins ties. A group whose largest
-// weight w satisfies w * kInvEMin <= best (kInvEMin above 1 / the smallest E
-// a race uniform can give) cannot produce a winner and skips the draw: exact
-// pruning. Since w <= p and p grows with the logit, the same bound (with a
-// factor-2 margin for rounding) becomes a logit threshold, so most entries
-// cost one compare. Slice winners meet in one 64-bit atomicMax of (score bits,
-// ~index); the last task of a request writes the token.
+// published (and from the argmax token's score seeded by the accept scan).
+// The CTA pulls its slice of logits and draft probabilities into shared
+// memory with two bulk copies, then scores it. Four consecutive entries share
+// one Philox4x32-10 draw; E = -ln U, score = w / E, the lowest index wins
+// ties. A group whose largest weight w satisfies w * kInvEMin <= best
+// (kInvEMin above 1 / the smallest E a race uniform can give) cannot produce
+// a winner and skips the draw: exact pruning. Since w <= p and p grows with
+// the logit, the same bound (with a factor-2 margin for rounding) becomes a
+// logit threshold, so most entries cost one compare. Groups that still need
+// their draw are packed into a per-warp queue so the draws run on dense
+// lanes. Slice winners meet in one 64-bit atomicMax of (score bits, ~index);
+// the last task of a request writes the token.
 #pragma once
 #include "common.cuh"
 #include "philox.cuh"
@@ -24,15 +28,46 @@
 namespace sv {
 
 constexpr int kRaceThreads = 256;
-constexpr int kRaceSlice = 8192;  // entries per task (multiple of 4 * kRaceThreads)
-constexpr int kRaceGroups = 4;  // groups of 4 entries loaded together per thread
+constexpr int kRaceSlice = 8192;  // entries per task (multiple of 16 * kRaceThreads)
+constexpr int kRaceGroups = 4;    // groups of 4 entries per thread per batch
 // Above 1 / E_min, E_min = -ln(1 - 2^-24) ~ 5.96e-8 the smallest E a race
 // uniform can give: no entry scores more than w * kInvEMin.
 constexpr float kInvEMin = 1.7e7f;
+// Shared memory of the staged path: the slice's logits and its draft
+// probabilities (fp32).
+__host__ __device__ constexpr size_t race_smem_bytes(int logit_bytes) {
+  return (size_t)kRaceSlice * logit_bytes + (size_t)kRaceSlice * 4;
+}
+
+// What the scoring needs about the race row.
+struct RaceView {
+  int V, row, qrow, kstar, mode, x;
+  float c, mc, inv_z, theta, z;
+  long long greq;
+};
+
+__device__ __forceinline__ RaceView race_view(const Params& P, int r, int row, int qrow,
+                                              int kstar, int mode, int x, float m, float c,
+                                              float inv_z, float theta, float z) {
+  RaceView v;
+  v.V = P.V;
+  v.row = row;
+  v.qrow = qrow;
+  v.kstar = kstar;
+  v.mode = mode;
+  v.x = x;
+  v.c = c;
+  v.mc = m * c;
+  v.inv_z = inv_z;
+  v.theta = theta;
+  v.z = z;
+  v.greq = P.req_base + r;
+  return v;
+}
 
 // p of one entry of a race row (0 if cut by top-k / top-p).
-__device__ __forceinline__ float race_p(float l, const RowStats& s, float mc) {
-  return (l >= s.theta) ? ex2(fmaf(l, s.c, -mc)) * s.inv_z : 0.f;
+__device__ __forceinline__ float race_p(float l, const RaceView& v) {
+  return (l >= v.theta) ? ex2(fmaf(l, v.c, -v.mc)) * v.inv_z : 0.f;
 }
 
 // The race weight of entry j given p and q.
@@ -51,174 +86,238 @@ __device__ __forceinline__ unsigned long long race_pack(float score, int j) {
   return ((unsigned long long)__float_as_uint(score) << 32) | (0xFFFFFFFFu - (uint32_t)j);
 }
 
-// One candidate entry j, scored exactly as the race scores it: the packed
-// (score, ~j), or 0 when w_j = 0.
-__device__ unsigned long long race_candidate(const Params& P, const RaceDesc& d,
-                                             const RowStats& s, long long greq, int j) {
-  if (j < 0 || j >= P.V || !(s.z > 0.f)) return 0ull;
-  const float l = load_logit(P, d.row, j);
-  const float q = (d.mode == kRaceResidual) ? __ldg(P.q + (long long)d.qrow * P.V + j) : 0.f;
-  const float w = race_w(race_p(l, s, s.m * s.c), q, j, d.mode, d.x);
-  if (!(w > 0.f)) return 0ull;
-  const uint4 r = race_words(P.seed, greq, d.kstar, (uint32_t)j >> 2);
-  const uint32_t words[4] = {r.x, r.y, r.z, r.w};
-  return race_pack(race_score(w, words[j & 3]), j);
-}
-
 // A logit at or below the returned value has p * kInvEMin <= best / 2 (p
 // is ex2(l c - m c) / Z), so neither its p nor its weight can reach `best`:
 //   l <= (log2(best Z / (2 kInvEMin)) + m c) / c.
 // The factor 2 absorbs every rounding of this bound and of p itself.
-// -inf (nothing skipped) while there is no best yet, the theta cut aside.
-__device__ __forceinline__ float race_logit_floor(const RowStats& s, float mc, float best) {
+// Entries below theta have p = 0 and are always below the returned value.
+__device__ __forceinline__ float race_logit_floor(const RaceView& v, float best) {
   float t = -INFINITY;
-  if (best > 0.f && s.c > 0.f) t = (log2f(best * s.z / (2.f * kInvEMin)) + mc) / s.c;
-  // entries below theta have p = 0
-  return fmaxf(t, nextafterf(s.theta, -INFINITY));
+  if (best > 0.f && v.c > 0.f) t = (log2f(best * v.z / (2.f * kInvEMin)) + v.mc) / v.c;
+  return fmaxf(t, nextafterf(v.theta, -INFINITY));
 }
 
-// Groups [g0, g1) of the race row, this thread's share; loads for
-// kRaceGroups groups are issued before any of them is scored.
+// One candidate entry j, scored exactly as the race scores it: the packed
+// (score, ~j), or 0 when w_j = 0.
+__device__ unsigned long long race_candidate(const Params& P, const RaceView& v, int j) {
+  if (j < 0 || j >= P.V || !(v.z > 0.f)) return 0ull;
+  const float l = load_logit(P, v.row, j);
+  const float q = (v.mode == kRaceResidual) ? __ldg(P.q + (long long)v.qrow * P.V + j) : 0.f;
+  const float w = race_w(race_p(l, v), q, j, v.mode, v.x);
+  if (!(w > 0.f)) return 0ull;
+  const uint4 r = race_words(P.seed, v.greq, v.kstar, (uint32_t)j >> 2);
+  const uint32_t words[4] = {r.x, r.y, r.z, r.w};
+  return race_pack(race_score(w, words[j & 3]), j);
+}
+
 struct RaceItem {
   uint32_t g;  // group (entries 4g .. 4g+3)
   float w[4];  // their weights
 };
 
-// `queue`: shared memory for 32 * kRaceGroups items per warp of the block.
-__device__ void race_range(const Params& P, const RaceDesc& d, const RowStats& s, int mode,
-                           long long greq, uint32_t g0, uint32_t g1, float& best, int& best_j,
-                           RaceItem* queue) {
-  const int V = P.V;
-  const float mc = s.m * s.c;
-  const long long lrow = (long long)d.row * V;
-  const long long qoff = (long long)d.qrow * V;
-  const uintptr_t la = reinterpret_cast<uintptr_t>(P.logits);
-  const uintptr_t qa = reinterpret_cast<uintptr_t>(P.q);
-  const bool vec = (V % 4 == 0) && ((la & 15) == 0) && (mode != kRaceResidual || (qa & 15) == 0);
+// Score one batch: this thread's kRaceGroups groups (group ids gk[k], their
+// logits l[k][] and draft probabilities q[k][]; ids >= g1 are absent). All
+// 32 lanes of the warp call it together. `qw` is the warp's queue of
+// 32 * kRaceGroups items.
+__device__ __forceinline__ void race_batch(const Params& P, const RaceView& v, int mode,
+                                           const uint32_t gk[kRaceGroups], uint32_t g1,
+                                           float l[kRaceGroups][4], float q[kRaceGroups][4],
+                                           float& best, int& best_j, float& lthr,
+                                           RaceItem* qw) {
+  // Decide every group against one snapshot of the best (the best only
+  // grows, so an older snapshot prunes less but never wrongly).
+  const float cut = best;
+  const int lane = threadIdx.x & 31;
+  int n_items = 0;
+#pragma unroll
+  for (int k = 0; k < kRaceGroups; ++k) {
+    const uint32_t g = gk[k];
+    const float lmax = fmaxf(fmaxf(l[k][0], l[k][1]), fmaxf(l[k][2], l[k][3]));
+    bool need = false;
+    float w[4] = {0.f, 0.f, 0.f, 0.f};
+    if (g < g1 && lmax > lthr) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = (int)(g * 4u) + e;
+        w[e] = (j < v.V) ? race_w(race_p(l[k][e], v), q[k][e], j, mode, v.x) : 0.f;
+      }
+      const float wmax = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
+      need = (wmax > 0.f) && (wmax * kInvEMin > cut);
+    }
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, need);
+    if (need) {
+      RaceItem& it = qw[n_items + __popc(m & ((1u << lane) - 1u))];
+      it.g = g;
+      it.w[0] = w[0];
+      it.w[1] = w[1];
+      it.w[2] = w[2];
+      it.w[3] = w[3];
+    }
+    n_items += __popc(m);
+  }
+  __syncwarp();
+  for (int t = lane; t < n_items; t += 32) {
+    const RaceItem it = qw[t];
+    const uint4 r = race_words(P.seed, v.greq, v.kstar, it.g);
+    const uint32_t words[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (it.w[e] * kInvEMin > cut) {
+        const float sc = race_score(it.w[e], words[e]);
+        const int j = (int)(it.g * 4u) + e;
+        if (sc > best || (sc == best && j < best_j)) {
+          best = sc;
+          best_j = j;
+        }
+      }
+    }
+  }
+  __syncwarp();
+  // One best for the whole warp: the next batch prunes against it.
+  warp_argmax(best, best_j);
+  if (best_j == kNoIndex) best = 0.f;
+  if (best != cut) lthr = race_logit_floor(v, best);
+}
+
+// Groups [g0, g1) of the race row read straight from global memory (rows
+// that are not 16-byte aligned, and the rare whole-row fallback).
+__device__ void race_range_global(const Params& P, const RaceView& v, int mode, uint32_t g0,
+                                  uint32_t g1, float& best, int& best_j, RaceItem* queue) {
+  const int V = v.V;
   const uint32_t stride = blockDim.x;
-  // Groups whose largest logit is <= lthr cannot hold a winner.
-  float lthr = race_logit_floor(s, mc, best);
-  // Every lane runs the same number of batches (warp-wide ballots inside).
+  float lthr = race_logit_floor(v, best);
+  RaceItem* qw = queue + (threadIdx.x >> 5) * (32 * kRaceGroups);
   const uint32_t span = stride * kRaceGroups;
-  const uint32_t first = g0 + (threadIdx.x & ~31u);
-  for (uint32_t gw = first; gw < g1; gw += span) {
+  for (uint32_t gw = g0 + (threadIdx.x & ~31u); gw < g1; gw += span) {
     const uint32_t gb = gw + (threadIdx.x & 31u);
     float l[kRaceGroups][4], q[kRaceGroups][4];
+    uint32_t gk[kRaceGroups];
 #pragma unroll
     for (int k = 0; k < kRaceGroups; ++k) {
-      const uint32_t g = gb + (uint32_t)k * stride;
+      gk[k] = gb + (uint32_t)k * stride;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        l[k][e] = -INFINITY;
-        q[k][e] = 0.f;
-      }
-      if (g < g1) {
-        const int j0 = (int)(g * 4u);
-        if (vec && j0 + 3 < V) {
-          if (P.bf16) {
-            const uint2 b = __ldg(reinterpret_cast<const uint2*>(
-                reinterpret_cast<const unsigned short*>(P.logits) + lrow + j0));
-            l[k][0] = bf16_lo(b.x);
-            l[k][1] = bf16_hi(b.x);
-            l[k][2] = bf16_lo(b.y);
-            l[k][3] = bf16_hi(b.y);
-          } else {
-            const float4 f = __ldg(reinterpret_cast<const float4*>(
-                reinterpret_cast<const float*>(P.logits) + lrow + j0));
-            l[k][0] = f.x; l[k][1] = f.y; l[k][2] = f.z; l[k][3] = f.w;
-          }
-          if (mode == kRaceResidual) {
-            const float4 f = __ldg(reinterpret_cast<const float4*>(P.q + qoff + j0));
-            q[k][0] = f.x; q[k][1] = f.y; q[k][2] = f.z; q[k][3] = f.w;
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (j0 + e < V) {
-              l[k][e] = load_logit(P, d.row, j0 + e);
-              if (mode == kRaceResidual) q[k][e] = __ldg(P.q + qoff + j0 + e);
-            }
-          }
-        }
+        const int j = (int)(gk[k] * 4u) + e;
+        const bool in = gk[k] < g1 && j < V;
+        l[k][e] = in ? load_logit(P, v.row, j) : -INFINITY;
+        q[k][e] = (in && mode == kRaceResidual) ? __ldg(P.q + (long long)v.qrow * V + j) : 0.f;
       }
     }
-    // Decide every group of the batch against one snapshot of the best
-    // (the best only grows, so an older snapshot prunes less but never
-    // wrongly). Groups that still need their Philox words are packed into
-    // a per-warp queue, so that the draws run on dense lanes instead of
-    // following each lane's divergent decisions.
-    const float cut = best;
-    const int lane = threadIdx.x & 31;
-    RaceItem* qw = queue + (threadIdx.x >> 5) * (32 * kRaceGroups);
-    int n_items = 0;
-#pragma unroll
-    for (int k = 0; k < kRaceGroups; ++k) {
-      const uint32_t g = gb + (uint32_t)k * stride;
-      const float lmax = fmaxf(fmaxf(l[k][0], l[k][1]), fmaxf(l[k][2], l[k][3]));
-      bool need = false;
-      float w[4] = {0.f, 0.f, 0.f, 0.f};
-      if (g < g1 && lmax > lthr) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = (int)(g * 4u) + e;
-          w[e] = (j < V) ? race_w(race_p(l[k][e], s, mc), q[k][e], j, mode, d.x) : 0.f;
-        }
-        const float wmax = fmaxf(fmaxf(w[0], w[1]), fmaxf(w[2], w[3]));
-        need = (wmax > 0.f) && (wmax * kInvEMin > cut);
-      }
-      const unsigned m = __ballot_sync(0xFFFFFFFFu, need);
-      if (need) {
-        RaceItem& it = qw[n_items + __popc(m & ((1u << lane) - 1u))];
-        it.g = g;
-        it.w[0] = w[0]; it.w[1] = w[1]; it.w[2] = w[2]; it.w[3] = w[3];
-      }
-      n_items += __popc(m);
-    }
-    __syncwarp();
-    for (int t = lane; t < n_items; t += 32) {
-      const RaceItem it = qw[t];
-      const uint4 r = race_words(P.seed, greq, d.kstar, it.g);
-      const uint32_t words[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (it.w[e] * kInvEMin > cut) {
-          const float sc = race_score(it.w[e], words[e]);
-          const int j = (int)(it.g * 4u) + e;
-          if (sc > best || (sc == best && j < best_j)) {
-            best = sc;
-            best_j = j;
-          }
-        }
-      }
-    }
-    __syncwarp();
-    // One best for the whole warp: the next batch prunes against it.
-    warp_argmax(best, best_j);
-    if (best_j == kNoIndex) best = 0.f;
-    if (best != cut) lthr = race_logit_floor(s, mc, best);
+    race_batch(P, v, mode, gk, g1, l, q, best, best_j, lthr, qw);
   }
 }
 
 __global__ void __launch_bounds__(kRaceThreads)
 k_race(Params P) {
-  const unsigned n_race = *P.race_count;
-  const unsigned t = blockIdx.x;
-  if (t >= n_race * (unsigned)P.race_slices) return;
-  const uint32_t groups = (uint32_t)((P.V + 3) / 4);
+  extern __shared__ __align__(128) unsigned char race_smem[];
   __shared__ int s_last;
   __shared__ unsigned long long s_packed;
   __shared__ RaceItem queue[kRaceThreads * kRaceGroups];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_staged;
+
+  const unsigned n_race = *P.race_count;
+  const unsigned t = blockIdx.x;
+  if (t >= n_race * (unsigned)P.race_slices) return;
   const int slice = (int)(t / n_race);
-  const int r = P.race_list[t % n_race];
-  const RaceDesc d = P.race[r];
-  const RowStats s = P.rows[d.row];
-  const long long greq = P.req_base + r;
+  const RaceTask task = P.race_list[t % n_race];
+  const int r = task.r;
+  const RaceView v = race_view(P, r, task.row, task.qrow, task.kstar, task.mode, task.x, task.m,
+                               task.c, task.inv_z, task.theta, task.z);
+  const int V = P.V;
+  const uint32_t groups = (uint32_t)((V + 3) / 4);
+  const uint32_t g0 = (uint32_t)slice * (kRaceSlice / 4);
+  const uint32_t g1 = min(groups, g0 + (uint32_t)(kRaceSlice / 4));
+  const int j0 = (int)(g0 * 4u);
+  const int n = min(kRaceSlice, V - j0);
+  const int esize = P.bf16 ? 2 : 4;
+  const bool resid = (v.mode == kRaceResidual);
+  const char* lsrc = (const char*)P.logits + ((long long)v.row * V + j0) * esize;
+  const char* qsrc = resid ? (const char*)(P.q + (long long)v.qrow * V + j0) : nullptr;
+  unsigned char* lbuf = race_smem;
+  float* qbuf = reinterpret_cast<float*>(race_smem + (size_t)kRaceSlice * esize);
+
+  // Stage the slice with bulk copies when every address and size allows it.
+  if (threadIdx.x == 0) {
+    const uint32_t lbytes = (uint32_t)n * esize, qbytes = resid ? (uint32_t)n * 4u : 0u;
+    const bool ok = ((reinterpret_cast<uintptr_t>(lsrc) & 15) == 0) && (lbytes % 16 == 0) &&
+                    (!resid || (((reinterpret_cast<uintptr_t>(qsrc) & 15) == 0) &&
+                                (qbytes % 16 == 0)));
+    s_staged = ok ? 1 : 0;
+    if (ok) {
+      mbar_init(&bar, 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&bar, lbytes + qbytes);
+      bulk_load(lbuf, lsrc, lbytes, &bar);
+      if (resid) bulk_load(qbuf, qsrc, qbytes, &bar);
+    }
+  }
+  __syncthreads();
+  const bool staged = s_staged != 0;
+  if (staged) {
+    // Every thread waits for the copies (bounded); all agree on the outcome.
+    if (!__syncthreads_and(mbar_wait(&bar, 0) ? 1 : 0)) {
+      if (threadIdx.x == 0) atomicOr(P.status, SPEC_STATUS_TIMEOUT);
+      // one more bounded wait for the copies in flight, then give up
+      __syncthreads_and(mbar_wait(&bar, 0) ? 1 : 0);
+      return;
+    }
+  }
+
+  // The best so far (seeded by the accept scan, raised by earlier slices).
   const unsigned long long lb = __ldcg(P.race_best + r);
   float best = lb ? __uint_as_float((uint32_t)(lb >> 32)) : 0.f;
   int best_j = lb ? (int)(0xFFFFFFFFu - (uint32_t)lb) : kNoIndex;
-  const uint32_t g0 = (uint32_t)slice * (kRaceSlice / 4);
-  const uint32_t g1 = min(groups, g0 + (uint32_t)(kRaceSlice / 4));
-  if (s.z > 0.f) race_range(P, d, s, d.mode, greq, g0, g1, best, best_j, queue);
+  if (v.z > 0.f) {
+    if (staged) {
+      float lthr = race_logit_floor(v, best);
+      RaceItem* qw = queue + (threadIdx.x >> 5) * (32 * kRaceGroups);
+      const uint32_t stride = blockDim.x;
+      const uint32_t span = stride * kRaceGroups;
+      for (uint32_t gw = g0 + (threadIdx.x & ~31u); gw < g1; gw += span) {
+        const uint32_t gb = gw + (threadIdx.x & 31u);
+        float l[kRaceGroups][4], q[kRaceGroups][4];
+        uint32_t gk[kRaceGroups];
+#pragma unroll
+        for (int k = 0; k < kRaceGroups; ++k) {
+          gk[k] = gb + (uint32_t)k * stride;
+          const int le = (int)((gk[k] - g0) * 4u);  // entry within the slice
+          const bool in = gk[k] < g1 && le + 3 < n;
+          if (in) {
+            if (P.bf16) {
+              const uint2 b = *reinterpret_cast<const uint2*>(lbuf + (size_t)le * 2);
+              l[k][0] = bf16_lo(b.x);
+              l[k][1] = bf16_hi(b.x);
+              l[k][2] = bf16_lo(b.y);
+              l[k][3] = bf16_hi(b.y);
+            } else {
+              const float4 f = *reinterpret_cast<const float4*>(lbuf + (size_t)le * 4);
+              l[k][0] = f.x; l[k][1] = f.y; l[k][2] = f.z; l[k][3] = f.w;
+            }
+            if (resid) {
+              const float4 f = *reinterpret_cast<const float4*>(qbuf + le);
+              q[k][0] = f.x; q[k][1] = f.y; q[k][2] = f.z; q[k][3] = f.w;
+            } else {
+              q[k][0] = q[k][1] = q[k][2] = q[k][3] = 0.f;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const bool ine = gk[k] < g1 && le + e < n;
+              l[k][e] = ine ? (P.bf16 ? bf16_lo((uint32_t)*reinterpret_cast<const unsigned short*>(
+                                            lbuf + (size_t)(le + e) * 2))
+                                      : *reinterpret_cast<const float*>(lbuf + (size_t)(le + e) * 4))
+                            : -INFINITY;
+              q[k][e] = (ine && resid) ? qbuf[le + e] : 0.f;
+            }
+          }
+        }
+        race_batch(P, v, v.mode, gk, g1, l, q, best, best_j, lthr, qw);
+      }
+    } else {
+      race_range_global(P, v, v.mode, g0, g1, best, best_j, queue);
+    }
+  }
   block_argmax(best, best_j);
   if (threadIdx.x == 0) {
     if (best_j != kNoIndex && best > 0.f) atomicMax(P.race_best + r, race_pack(best, best_j));
@@ -239,14 +338,14 @@ k_race(Params P) {
     // Every weight was 0 (rounding only): draw from p over the whole row.
     float b2 = 0.f;
     int j2 = kNoIndex;
-    if (s.z > 0.f) race_range(P, d, s, kRaceP, greq, 0u, groups, b2, j2, queue);
+    if (v.z > 0.f) race_range_global(P, v, kRaceP, 0u, groups, b2, j2, queue);
     block_argmax(b2, j2);
     tok = (j2 == kNoIndex) ? 0 : j2;
     if (threadIdx.x == 0) atomicOr(P.status, SPEC_STATUS_EMPTY_RESIDUAL);
   } else {
     tok = (int)(0xFFFFFFFFu - (uint32_t)(packed & 0xFFFFFFFFull));
   }
-  if (threadIdx.x == 0) P.out_tokens[d.row] = tok;
+  if (threadIdx.x == 0) P.out_tokens[v.row] = tok;
 }
 
 }  // namespace sv

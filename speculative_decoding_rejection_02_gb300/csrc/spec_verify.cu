@@ -25,11 +25,10 @@ struct spec_verify_handle {
   sv::RaceDesc* race;
   unsigned long long* race_best;
   unsigned* race_counter;
-  int* race_list;
+  sv::RaceTask* race_list;
   unsigned* race_count;
   unsigned* status;
   int max_slices;
-  int race_blocks;  // resident CTAs of k_race on the device
   cudaEvent_t phase[4];
   int n_phase;
   int tma_blocks;  // resident CTAs of k_rows_tma on the device
@@ -119,7 +118,8 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
                  stream>>>(P);
   if (timed) cudaEventRecord(h->phase[2], stream);
   if (!greedy) {
-    sv::k_race<<<(unsigned)((long long)b->B * P.race_slices), sv::kRaceThreads, 0, stream>>>(P);
+    sv::k_race<<<(unsigned)((long long)b->B * P.race_slices), sv::kRaceThreads,
+                 sv::race_smem_bytes(P.bf16 ? 2 : 4), stream>>>(P);
   }
   if (timed) cudaEventRecord(h->phase[3], stream);
   if (cudaPeekAtLastError() != cudaSuccess) {
@@ -164,13 +164,11 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
     per_sm = 0;
   }
   h->tma_blocks = per_sm * prop.multiProcessorCount;
-  int race_per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&race_per_sm, sv::k_race, sv::kRaceThreads,
-                                                    0) != cudaSuccess) {
-    cudaGetLastError();
-    race_per_sm = 1;
+  if (cudaFuncSetAttribute(sv::k_race, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sv::race_smem_bytes(4)) != cudaSuccess) {
+    delete h;
+    return SPEC_ERR_CUDA;
   }
-  h->race_blocks = (race_per_sm > 0 ? race_per_sm : 1) * prop.multiProcessorCount;
   h->max_slices = (cfg->max_vocab + sv::kSliceF32 - 1) / sv::kSliceF32;
 
   const size_t n_rows = (size_t)cfg->max_rows, n_b = (size_t)cfg->max_batch;
@@ -180,7 +178,7 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   const size_t sz_race = align_up(n_b * sizeof(sv::RaceDesc));
   const size_t sz_best = align_up(n_b * sizeof(unsigned long long));
   const size_t sz_rccnt = align_up(n_b * sizeof(unsigned));
-  const size_t sz_list = align_up(n_b * sizeof(int));
+  const size_t sz_list = align_up(n_b * sizeof(sv::RaceTask));
   const size_t sz_lcnt = align_up(sizeof(unsigned));
   const size_t sz_stat = align_up(sizeof(unsigned));
   const size_t total = sz_rows + sz_part + sz_rcnt + sz_race + sz_best + sz_rccnt + sz_list +
@@ -201,7 +199,7 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   h->race = (sv::RaceDesc*)p; p += sz_race;
   h->race_best = (unsigned long long*)p; p += sz_best;
   h->race_counter = (unsigned*)p; p += sz_rccnt;
-  h->race_list = (int*)p; p += sz_list;
+  h->race_list = (sv::RaceTask*)p; p += sz_list;
   h->race_count = (unsigned*)p; p += sz_lcnt;
   h->status = (unsigned*)p;
   *out = h;
