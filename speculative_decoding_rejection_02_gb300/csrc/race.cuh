@@ -18,7 +18,9 @@
 // the logit, the same bound (with a factor-2 margin for rounding) becomes a
 // logit threshold, so most entries cost one compare. Groups that still need
 // their draw are packed into a per-warp queue so the draws run on dense
-// lanes. Slice winners meet in one 64-bit atomicMax of (score bits, ~index);
+// lanes; after the draw, -ln U >= 1 - U bounds every score by w / (1 - U),
+// so the logarithm and the division run only for entries that can still
+// win. Slice winners meet in one 64-bit atomicMax of (score bits, ~index);
 // the last task of a request writes the token.
 #pragma once
 #include "common.cuh"
@@ -162,7 +164,11 @@ __device__ __forceinline__ void race_batch(const Params& P, const RaceView& v, i
     const uint32_t words[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      if (it.w[e] * kInvEMin > cut) {
+      // -ln U >= 1 - U, so w / (1 - U) bounds the score from above; 1 - U
+      // is exact and the factor (1 + 2e-6) covers the roundings of the
+      // score and of this test. Entries that fail cannot reach `cut`.
+      const float v1 = 1.f - race_uniform_from_word(words[e]);
+      if (it.w[e] > 0.f && it.w[e] * 1.000002f > cut * v1) {
         const float sc = race_score(it.w[e], words[e]);
         const int j = (int)(it.g * 4u) + e;
         if (sc > best || (sc == best && j < best_j)) {
