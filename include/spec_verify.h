@@ -184,6 +184,40 @@ int spec_verify_check_batch(const spec_verify_config* cfg,
  */
 int spec_verify_set_phase_events(spec_verify_handle* h, void* const* events, int n);
 
+/*
+ * spec_verify_run_noalloc — spec_verify_run for callers that cannot allocate
+ * device memory: code that runs inside a CUDA graph that is being captured
+ * or replayed, inside a custom memory pool or allocator callback, or in a
+ * process whose allocator is owned by another framework. It needs no handle
+ * and calls no cudaMalloc, cudaFree or allocating library routine: its
+ * scratch (row statistics, slice partials, race state) lives in one
+ * file-scope device array of the library, SPEC_NOALLOC_SCRATCH_BYTES bytes
+ * on every GPU that loads the library, held until the process exits.
+ * The sources of the method have no counterpart of this entry point; it
+ * computes exactly what spec_verify_run computes.
+ *   b      [in]  host pointer to the batch (device arrays inside), on the
+ *                current CUDA device;
+ *   stream [in]  a cudaStream_t (NULL = legacy default stream);
+ *   device_status [in/out] device pointer to one unsigned that receives the
+ *                SPEC_STATUS_* bits of the call (OR-ed in: clear it first),
+ *                or NULL to drop them.
+ * Limits: B <= SPEC_NOALLOC_MAX_BATCH, N + B <= SPEC_NOALLOC_MAX_ROWS,
+ * V <= SPEC_NOALLOC_MAX_VOCAB; larger batches return SPEC_ERR_CAPACITY and
+ * enqueue nothing. The first call on a device resolves the array's device
+ * address (cudaGetSymbolAddress) and sets kernel attributes; make that first
+ * call outside any stream capture. Every call shares the one array, so calls
+ * whose kernels overlap on the GPU (other streams, other threads) race and
+ * give wrong results: serialise them. The counters it relies on are cleared
+ * by every call. Returns SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_CAPACITY,
+ * SPEC_ERR_UNSUPPORTED or SPEC_ERR_CUDA. Asynchronous.
+ */
+#define SPEC_NOALLOC_MAX_BATCH 2048
+#define SPEC_NOALLOC_MAX_ROWS 8192
+#define SPEC_NOALLOC_MAX_VOCAB 262144
+#define SPEC_NOALLOC_SCRATCH_BYTES (5u << 20)
+int spec_verify_run_noalloc(const spec_verify_batch* b, void* stream,
+                            unsigned* device_status);
+
 /* spec_verify_destroy — free the workspace and the handle (NULL is a no-op).
  * Synchronises the handle's device first. */
 void spec_verify_destroy(spec_verify_handle* h);

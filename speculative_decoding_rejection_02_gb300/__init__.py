@@ -33,8 +33,8 @@ FLAG_NAIVE = 0x1
 # The entry points declared in include/spec_verify.h.
 ENTRY_POINTS = (
     "spec_verify_init", "spec_verify_run", "spec_verify_greedy", "spec_verify_status",
-    "spec_verify_check_batch", "spec_verify_set_phase_events", "spec_verify_destroy",
-    "spec_verify_strerror",
+    "spec_verify_check_batch", "spec_verify_set_phase_events", "spec_verify_run_noalloc",
+    "spec_verify_destroy", "spec_verify_strerror",
 )
 
 
@@ -85,6 +85,7 @@ def lib():
             L.spec_verify_status.argtypes = [C.c_void_p, C.POINTER(C.c_uint)]
             L.spec_verify_check_batch.argtypes = [C.POINTER(Config), C.POINTER(Batch)]
             L.spec_verify_set_phase_events.argtypes = [C.c_void_p, C.c_void_p, C.c_int]
+            L.spec_verify_run_noalloc.argtypes = [C.POINTER(Batch), C.c_void_p, C.c_void_p]
             L.spec_verify_destroy.argtypes = [C.c_void_p]
             L.spec_verify_destroy.restype = None
             L.spec_verify_strerror.argtypes = [C.c_int]

@@ -5,6 +5,7 @@
 
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "../../include/spec_verify.h"
@@ -264,3 +265,120 @@ const char* spec_verify_strerror(int code) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// spec_verify_run_noalloc: the same launch sequence on a workspace carved out
+// of one file-scope device array instead of cudaMalloc'ed memory.
+// ---------------------------------------------------------------------------
+namespace {
+
+// Sizes of the workspace pieces at the no-allocation limits.
+constexpr size_t kNaRows = SPEC_NOALLOC_MAX_ROWS;
+constexpr size_t kNaBatch = SPEC_NOALLOC_MAX_BATCH;
+constexpr size_t kNaSlices = (SPEC_NOALLOC_MAX_VOCAB + sv::kSliceF32 - 1) / sv::kSliceF32;
+constexpr size_t na_align(size_t x) { return (x + 255) & ~size_t(255); }
+constexpr size_t kNaOffRows = 0;
+constexpr size_t kNaOffPart = kNaOffRows + na_align(kNaRows * sizeof(sv::RowStats));
+constexpr size_t kNaOffRcnt = kNaOffPart + na_align(kNaRows * kNaSlices * sizeof(sv::SlicePartial));
+constexpr size_t kNaOffRace = kNaOffRcnt + na_align(kNaRows * sizeof(unsigned));
+constexpr size_t kNaOffBest = kNaOffRace + na_align(kNaBatch * sizeof(sv::RaceDesc));
+constexpr size_t kNaOffRccnt = kNaOffBest + na_align(kNaBatch * sizeof(unsigned long long));
+constexpr size_t kNaOffList = kNaOffRccnt + na_align(kNaBatch * sizeof(unsigned));
+constexpr size_t kNaOffLcnt = kNaOffList + na_align(kNaBatch * sizeof(sv::RaceTask));
+constexpr size_t kNaOffStat = kNaOffLcnt + na_align(sizeof(unsigned));
+constexpr size_t kNaBytes = kNaOffStat + na_align(sizeof(unsigned));
+static_assert(kNaBytes <= SPEC_NOALLOC_SCRATCH_BYTES, "no-allocation scratch too small");
+
+constexpr int kNaMaxDevices = 64;
+struct NoallocDevice {
+  bool ready;
+  char* base;  // device address of g_noalloc_scratch on this device
+  int sm_count;
+  int tma_blocks;
+};
+NoallocDevice g_na_dev[kNaMaxDevices];
+std::mutex g_na_mutex;
+
+}  // namespace
+
+// The scratch of spec_verify_run_noalloc (one copy per device).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[SPEC_NOALLOC_SCRATCH_BYTES];
+
+extern "C" int spec_verify_run_noalloc(const spec_verify_batch* b, void* stream,
+                                       unsigned* device_status) {
+  if (!b) return SPEC_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+  if (dev < 0 || dev >= kNaMaxDevices) return SPEC_ERR_UNSUPPORTED;
+  spec_verify_config cfg;
+  cfg.device = dev;
+  cfg.max_batch = SPEC_NOALLOC_MAX_BATCH;
+  cfg.max_rows = SPEC_NOALLOC_MAX_ROWS;
+  cfg.max_vocab = SPEC_NOALLOC_MAX_VOCAB;
+  cfg.flags = 0;
+  int rc = check_batch(&cfg, b, false);
+  if (rc != SPEC_OK) return rc;
+
+  NoallocDevice nd;
+  {
+    std::lock_guard<std::mutex> lock(g_na_mutex);
+    NoallocDevice& slot = g_na_dev[dev];
+    if (!slot.ready) {
+      // Once per device, with that device current: resolve the array's
+      // device address and set the kernels' shared-memory attributes.
+      cudaDeviceProp prop;
+      if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return SPEC_ERR_CUDA;
+      if (!(prop.major == 10 && prop.minor == 3)) return SPEC_ERR_UNSUPPORTED;
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+        cudaGetLastError();
+        return SPEC_ERR_CUDA;
+      }
+      int per_sm = 0;
+      if (cudaFuncSetAttribute(sv::k_rows_tma<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sv::kTmaSmemBytes) != cudaSuccess ||
+          cudaFuncSetAttribute(sv::k_rows_tma<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sv::kTmaSmemBytes) != cudaSuccess ||
+          cudaFuncSetAttribute(sv::k_race, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sv::race_smem_bytes(4)) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv::k_rows_tma<true>,
+                                                        sv::kTmaThreads,
+                                                        sv::kTmaSmemBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return SPEC_ERR_CUDA;
+      }
+      slot.base = (char*)ptr;
+      slot.sm_count = prop.multiProcessorCount;
+      slot.tma_blocks = per_sm * prop.multiProcessorCount;
+      slot.ready = true;
+    }
+    nd = slot;
+  }
+  if (b->B == 0) return SPEC_OK;
+
+  // A handle on the stack whose workspace points into the array.
+  spec_verify_handle h;
+  std::memset(&h, 0, sizeof h);
+  h.cfg = cfg;
+  h.sm_count = nd.sm_count;
+  h.ws = nd.base;
+  h.rows = (sv::RowStats*)(nd.base + kNaOffRows);
+  h.partials = (sv::SlicePartial*)(nd.base + kNaOffPart);
+  h.row_counter = (unsigned*)(nd.base + kNaOffRcnt);
+  h.race = (sv::RaceDesc*)(nd.base + kNaOffRace);
+  h.race_best = (unsigned long long*)(nd.base + kNaOffBest);
+  h.race_counter = (unsigned*)(nd.base + kNaOffRccnt);
+  h.race_list = (sv::RaceTask*)(nd.base + kNaOffList);
+  h.race_count = (unsigned*)(nd.base + kNaOffLcnt);
+  h.status = device_status ? device_status : (unsigned*)(nd.base + kNaOffStat);
+  h.max_slices = (int)kNaSlices;
+  h.n_phase = 0;
+  h.tma_blocks = nd.tma_blocks;
+  // The slice counters must start at zero: clear them (the array keeps the
+  // previous call's contents).
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t rows = (size_t)b->N + (size_t)b->B;
+  if (cudaMemsetAsync(h.row_counter, 0, rows * sizeof(unsigned), s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  return launch(&h, b, s, false);
+}
