@@ -84,6 +84,7 @@ struct Params {
   long long req_base;
   unsigned flags;
   int greedy_call;  // 1 when called through spec_verify_greedy
+  int fast_filtered;  // 1 when the streaming pass handled top-k / top-p rows
   int* out_tokens;
   int* num_accepted;
   float* p_at_draft;

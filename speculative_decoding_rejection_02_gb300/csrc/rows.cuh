@@ -284,6 +284,7 @@ k_rows_filtered(Params P) {
   }
   __syncthreads();
   if (!s_ok || s_cls != kFiltered) return;
+  if (P.fast_filtered && !(P.rows[row].status & 0x80000000u)) return;  // done by the fast path
   const int r = s_req;
   const int bf16 = P.bf16;
   const float c = kLog2e / __ldg(P.temp + r);

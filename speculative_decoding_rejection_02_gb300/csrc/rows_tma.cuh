@@ -17,6 +17,7 @@
 #include "common.cuh"
 #include "pipe.cuh"
 #include "rows.cuh"
+#include "hist.cuh"
 
 namespace sv {
 
@@ -35,6 +36,8 @@ struct StageMeta {
   int j0;    // first element of the stage within the row
   int n;     // elements in the stage
   int last;  // 1 on the row's last stage
+  int tk;    // top-k of the row's request (filtered rows)
+  float tp;  // top-p of the row's request (filtered rows)
 };
 
 constexpr size_t kTmaSmemBytes =
@@ -46,12 +49,14 @@ struct RowInfo {
   int cls;  // -1: skip this row
   float c;
   int x;
+  int tk;
+  float tp;
 };
 
 // Warp-parallel lookup of the request owning `row` and its settings (all 32
 // lanes call it; every lane gets the result). Two or three dependent rounds
 // of loads instead of a serial binary search.
-__device__ RowInfo warp_row_info(const Params& P, long long row) {
+__device__ RowInfo warp_row_info(const Params& P, long long row, bool take_filtered) {
   const int lane = threadIdx.x & 31;
   int lo = 0, hi = P.B;  // answer in [lo, hi)
   while (hi - lo > 1) {
@@ -81,18 +86,27 @@ __device__ RowInfo warp_row_info(const Params& P, long long row) {
     info.cls = -1;
     info.c = 0.f;
     info.x = -1;
+    info.tk = 0;
+    info.tp = 1.f;
     return info;
   }
-  int x = -1;
+  int x = -1, tk = 0;
+  float tp = 1.f;
   if (lane == 0) {
     cls = row_class(P, r);
     if (i < c1 - c0) x = __ldg(P.ids + c0 + i);
+    if (cls == kFiltered) {
+      tk = P.top_k ? __ldg(P.top_k + r) : 0;
+      tp = P.top_p ? __ldg(P.top_p + r) : 1.f;
+    }
   }
   cls = __shfl_sync(0xFFFFFFFFu, cls, 0);
   T = __shfl_sync(0xFFFFFFFFu, T, 0);
   info.x = __shfl_sync(0xFFFFFFFFu, x, 0);
-  info.cls = (cls == kFiltered) ? -1 : cls;
-  info.c = (cls == kSoftmax) ? kLog2e / T : 0.f;
+  info.tk = __shfl_sync(0xFFFFFFFFu, tk, 0);
+  info.tp = __shfl_sync(0xFFFFFFFFu, tp, 0);
+  info.cls = (cls == kFiltered && !take_filtered) ? -1 : cls;
+  info.c = (cls != kArgmaxOnly) ? kLog2e / T : 0.f;
   return info;
 }
 
@@ -129,7 +143,7 @@ k_rows_tma(Params P, long long R) {
     RowInfo cur;
     cur.cls = -1;
     while (row < R) {  // first row with work
-      cur = warp_row_info(P, row);
+      cur = warp_row_info(P, row, BF16);
       if (cur.cls >= 0) break;
       row += gridDim.x;
     }
@@ -158,6 +172,8 @@ k_rows_tma(Params P, long long R) {
           M.j0 = (int)(off / esize);
           M.n = (int)(bytes / esize);
           M.last = (ch == nchunks - 1) ? 1 : 0;
+          M.tk = cur.tk;
+          M.tp = cur.tp;
           mbar_arrive_expect_tx(&full[stage], bytes);
           bulk_load(ring + (size_t)stage * kTmaStageBytes, src + off, bytes, &full[stage]);
         }
@@ -170,7 +186,7 @@ k_rows_tma(Params P, long long R) {
         if (ch == 0) {
           // Look the next row up while this one streams.
           while (nrow < R) {
-            next = warp_row_info(P, nrow);
+            next = warp_row_info(P, nrow, BF16);
             if (next.cls >= 0) break;
             nrow += gridDim.x;
           }
@@ -206,8 +222,18 @@ k_rows_tma(Params P, long long R) {
   __shared__ int red_i[kTmaConsumerWarps];
   __shared__ float bc_m, s_lx;
   __shared__ int bc_i;
+  // Value histogram of the current filtered row (bf16 only).
+  __shared__ unsigned hist[BF16 ? kHistBins : 1];
+  __shared__ float hist_nz;
+  __shared__ float fscr[kTmaConsumerWarps];
+  __shared__ int iscr[kTmaConsumerWarps];
   const int tid = threadIdx.x;
   constexpr int epc = 16 / esize;
+  if (BF16) {
+    for (int b = tid; b < kHistBins; b += kTmaConsumers) hist[b] = 0u;
+    if (tid == 0) hist_nz = 0.f;
+    named_sync(1, kTmaConsumers);
+  }
   int stage = 0;
   uint32_t phase = 0;
   // Running state of the current row: max, its lowest index, fl(max * c),
@@ -303,6 +329,21 @@ k_rows_tma(Params P, long long R) {
       f2_unpack(acc1, a2, a3);
       s += (a0 + a1) + (a2 + a3);
     }
+    if (BF16 && M.cls == kFiltered) {
+      // Count every element in its value's bin (exact top-k / top-p later).
+#pragma unroll
+      for (int k = 0; k < kTmaVecPerThread; ++k) {
+        if (tid + k * kTmaConsumers >= nvec) continue;
+        const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          const uint32_t b = (t & 1) ? (w[t >> 1] >> 16) : (w[t >> 1] & 0xFFFFu);
+          const int idx = hist_bin(b);
+          atomicAdd(&hist[idx], 1u);
+          if (idx == kNearZero) atomicAdd(&hist_nz, ex2(__uint_as_float(b << 16) * M.c));
+        }
+      }
+    }
     {
       // The draft token's logit, captured by the thread that holds it.
       const int dx = M.x - M.j0;
@@ -351,6 +392,33 @@ k_rows_tma(Params P, long long R) {
       named_sync(1, kTmaConsumers);
       m = bc_m;
       a = bc_i;
+      if (BF16 && M.cls == kFiltered) {
+        const HistResult hr = hist_finish<kTmaConsumerWarps>(hist, &hist_nz, m, M.c, M.tk, M.tp,
+                                                             P.V, tid, fscr, iscr);
+        if (tid == 0) {
+          if (hr.pending || !(m > -INFINITY)) {
+            RowStats ps;
+            ps.m = m;
+            ps.c = M.c;
+            ps.inv_z = 0.f;
+            ps.theta = -INFINITY;
+            ps.argmax = 0;
+            ps.p_x = 0.f;
+            ps.status = kPendingSlow;
+            ps.z = 0.f;
+            P.rows[M.row] = ps;
+          } else {
+            finish_row_x(P, M.row, M.cls, m, a == kNoIndex ? 0 : a, hr.z, hr.theta, M.c, M.x,
+                         s_lx);
+          }
+        }
+        named_sync(1, kTmaConsumers);
+        vmax = -INFINITY;
+        vmc = 0.f;
+        s = 0.f;
+        imax = kNoIndex;
+        continue;
+      }
       const float mc = m * M.c;
       float part = 0.f;
       if (soft && vmax > -INFINITY && m > -INFINITY) part = s * ex2(vmc - mc);

@@ -77,6 +77,7 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   P.req_base = b->request_base;
   P.flags = greedy ? 0u : b->flags;
   P.greedy_call = greedy ? 1 : 0;
+  P.fast_filtered = 0;
   P.out_tokens = b->out_tokens;
   P.num_accepted = b->num_accepted;
   P.p_at_draft = b->p_at_draft;
@@ -103,6 +104,7 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   const int esize = P.bf16 ? 2 : 4;
   const bool rows_aligned = (((long long)b->V * esize) % 16 == 0) &&
                             ((reinterpret_cast<uintptr_t>(b->target_logits) & 15) == 0);
+  P.fast_filtered = (rows_aligned && h->tma_blocks > 0 && P.bf16) ? 1 : 0;
   if (rows_aligned && h->tma_blocks > 0) {
     const long long grid = R < h->tma_blocks ? R : h->tma_blocks;
     if (P.bf16)

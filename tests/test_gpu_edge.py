@@ -147,3 +147,28 @@ def test_temperature_zero_ignores_draft_probs():
     b["temperature"][:] = 0
     b["draft_probs"][:] = 0  # must never be read at temperature 0
     check(b)
+
+
+@pytest.mark.parametrize("scale", [0.01, 0.2, 2.0, 30.0, 400.0, "ties"])
+@pytest.mark.parametrize("V", [304, 4096])
+def test_filtered_rows_on_the_streaming_path(scale, V):
+    """Aligned bf16 rows with top-k / top-p take the histogram path of the
+    streaming pass; tiny logits (threshold near 0) and |l| >= 256 fall back
+    to the exact bisection kernel. Both must agree with the oracle."""
+    rng = np.random.default_rng(V + (7 if scale == "ties" else int(float(scale) * 100)))
+    B = 36
+    g = rng.integers(0, 5, size=B)
+    N = int(g.sum())
+    if scale == "ties":
+        logits = np.round(rng.normal(0, 2, size=(N + B, V)))
+    else:
+        logits = rng.normal(0, float(scale), size=(N + B, V))
+    q = rng.random((N, V)) ** 2
+    q /= q.sum(1, keepdims=True)
+    ids = np.array([rng.choice(V, p=q[n]) for n in range(N)], np.int32)
+    temps = rng.choice([0.0, 0.5, 1.0, 2.0], size=B)
+    tk = rng.choice([0, 1, 5, 50, V], size=B)
+    tp = rng.choice([1.0, 0.3, 0.9, 0.999], size=B)
+    b = make_batch(logits, g, ids, temps, q, tk, tp, dtype="bf16", seed=V)
+    gpu, _ = check(b)
+    assert gpu["status"] & ~np.uint32(0x8) == 0
