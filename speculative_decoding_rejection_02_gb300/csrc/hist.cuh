@@ -31,6 +31,34 @@ constexpr int kOutOfRange = 2 * kFine + 2;      // 3074
 constexpr int kHistBins = 2 * kFine + 3;        // 3075
 constexpr unsigned kPendingSlow = 0x80000000u;  // row left to the exact slow path
 
+// Table form of hist_bin, one 32-bit entry per (sign, exponent) = b >> 7:
+// bin = base + mul * mantissa with mul in {-1, 0, +1} (low 16 bits: base,
+// high 16 bits: mul as a signed value).
+__device__ __forceinline__ uint32_t hist_table_entry(uint32_t se) {
+  const int e = (int)((se & 0xFFu));
+  const bool neg = (se & 0x100u) != 0;
+  int base, mul;
+  if (e >= kFineExpLo && e < kFineExpLo + kFineBinades) {
+    const int f0 = (e - kFineExpLo) << 7;
+    if (neg) { base = kFine - f0; mul = -1; }
+    else { base = kNearZero + 1 + f0; mul = 1; }
+  } else if (e < kFineExpLo) {
+    base = kNearZero; mul = 0;
+  } else {
+    base = kOutOfRange; mul = 0;  // |v| >= 256, inf, NaN; -inf fixed below
+  }
+  return (uint32_t)(base & 0xFFFF) | ((uint32_t)(mul & 0xFFFF) << 16);
+}
+
+// Bin of a bf16 value through the table (exact for every value but -inf,
+// which the caller maps to bin 0).
+__device__ __forceinline__ int hist_bin_tab(const uint32_t* tab, uint32_t b) {
+  const uint32_t t = tab[b >> 7];
+  const int base = (int)(t & 0xFFFFu);
+  const int mul = (int)(short)(t >> 16);
+  return base + mul * (int)(b & 0x7Fu);
+}
+
 __device__ __forceinline__ int hist_bin(uint32_t b) {
   const int f = (int)(b & 0x7FFFu) - kFineBase;
   if ((unsigned)f < (unsigned)kFine) return (b & 0x8000u) ? (kFine - f) : (kNearZero + 1 + f);

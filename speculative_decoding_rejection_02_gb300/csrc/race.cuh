@@ -275,6 +275,36 @@ k_race(Params P) {
   float best = lb ? __uint_as_float((uint32_t)(lb >> 32)) : 0.f;
   int best_j = lb ? (int)(0xFFFFFFFFu - (uint32_t)lb) : kNoIndex;
   if (v.z > 0.f) {
+    if (staged && best_j == kNoIndex) {
+      // No bound yet (the argmax token had weight 0 and no earlier slice has
+      // finished): score this slice's heaviest entry first and start from it.
+      float wb = 0.f;
+      int jb = kNoIndex;
+      for (int le = (int)threadIdx.x * 4; le < n; le += (int)blockDim.x * 4) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          if (le + e < n) {
+            const float lv = P.bf16 ? bf16_lo((uint32_t)*reinterpret_cast<const unsigned short*>(
+                                          lbuf + (size_t)(le + e) * 2))
+                                    : *reinterpret_cast<const float*>(lbuf + (size_t)(le + e) * 4);
+            const float qv = resid ? qbuf[le + e] : 0.f;
+            const int j = j0 + le + e;
+            const float w = race_w(race_p(lv, v), qv, j, v.mode, v.x);
+            if (w > wb) {
+              wb = w;
+              jb = j;
+            }
+          }
+        }
+      }
+      block_argmax(wb, jb);
+      if (jb != kNoIndex && wb > 0.f) {
+        const uint4 rw = race_words(P.seed, v.greq, v.kstar, (uint32_t)jb >> 2);
+        const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
+        best = race_score(wb, words[jb & 3]);
+        best_j = jb;
+      }
+    }
     if (staged) {
       float lthr = race_logit_floor(v, best);
       RaceItem* qw = queue + (threadIdx.x >> 5) * (32 * kRaceGroups);

@@ -224,6 +224,7 @@ k_rows_tma(Params P, long long R) {
   __shared__ int bc_i;
   // Value histogram of the current filtered row (bf16 only).
   __shared__ unsigned hist[BF16 ? kHistBins : 1];
+  __shared__ uint32_t hist_tab[BF16 ? 512 : 1];
   __shared__ float hist_nz;
   __shared__ float fscr[kTmaConsumerWarps];
   __shared__ int iscr[kTmaConsumerWarps];
@@ -231,6 +232,7 @@ k_rows_tma(Params P, long long R) {
   constexpr int epc = 16 / esize;
   if (BF16) {
     for (int b = tid; b < kHistBins; b += kTmaConsumers) hist[b] = 0u;
+    for (int e = tid; e < 512; e += kTmaConsumers) hist_tab[e] = hist_table_entry((uint32_t)e);
     if (tid == 0) hist_nz = 0.f;
     named_sync(1, kTmaConsumers);
   }
@@ -338,7 +340,8 @@ k_rows_tma(Params P, long long R) {
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
           const uint32_t b = (t & 1) ? (w[t >> 1] >> 16) : (w[t >> 1] & 0xFFFFu);
-          const int idx = hist_bin(b);
+          int idx = hist_bin_tab(hist_tab, b);
+          if (b == 0xFF80u) idx = 0;  // -inf
           atomicAdd(&hist[idx], 1u);
           if (idx == kNearZero) atomicAdd(&hist_nz, ex2(__uint_as_float(b << 16) * M.c));
         }
