@@ -1,81 +1,37 @@
 // Exact top-k / top-p on bf16 rows from a count histogram over bf16 values.
 //
-// A bf16 logit takes one of at most 65536 values, so the tempered, filtered
+// A bf16 logit takes one of 65536 values, so the tempered, filtered
 // distribution of a row (velog "vLLM 커널은 이 규칙을 어떻게 옮겼나":
 // temperature, top-k and top-p applied before the judgement) is fixed by how
 // many tokens hold each value. While a row streams through the SM, every
-// element adds 1 to its value's bin (a shared-memory atomic); at the row's
-// end the consumers turn counts into masses n_b 2^(v_b c - m c), scan the
-// bins from the largest value down, and read off the top-k and top-p
-// thresholds, Z over the kept set, and the kept set itself: no sort, no
-// per-element exp, one read of the row.
-//
-// Bins, in increasing value: 0 = -inf; 1 .. kFine = negative values with
-// 2^-4 <= |v| < 256, one per bf16 value; kNearZero = every |v| < 2^-4 (its
-// mass is accumulated per element); kNearZero+1 .. 2 kFine + 1 = positive
-// values with 2^-4 <= v < 256; kOutOfRange = |v| >= 256, +inf, NaN. A row
-// whose thresholds fall on the near-zero bin, or that has out-of-range
-// values, is left to the exact bisection kernel.
+// element adds 1 to the 16-bit counter indexed by its raw bits (one
+// shared-memory atomic, two counters per 32-bit word: 128 KB for all values).
+// At the row's end the consumers merge -0 into +0, turn counts into masses
+// n 2^(v c - m c), scan the values from the largest down and read off the
+// top-k and top-p thresholds, Z over the kept set and the kept set itself:
+// no sort, no per-element exp, one read of the row, exact for every value.
+// A counter can wrap only if more than 65535 tokens of one row share a
+// value; the total count then differs from V and the row is left to the
+// exact bisection kernel, as are rows with NaN or +inf.
 #pragma once
 #include "common.cuh"
 #include "pipe.cuh"
 
 namespace sv {
 
-constexpr int kFineExpLo = 123;                 // 2^-4
-constexpr int kFineBinades = 12;                // up to 2^8
-constexpr int kFine = kFineBinades * 128;       // 1536 values per sign
-constexpr int kFineBase = kFineExpLo << 7;      // bits of 2^-4 without sign
-constexpr int kNearZero = kFine + 1;            // 1537
-constexpr int kOutOfRange = 2 * kFine + 2;      // 3074
-constexpr int kHistBins = 2 * kFine + 3;        // 3075
 constexpr unsigned kPendingSlow = 0x80000000u;  // row left to the exact slow path
+constexpr size_t kHist16Bytes = 65536 * 2;      // 16-bit counters for every bf16 value
 
-// Table form of hist_bin, one 32-bit entry per (sign, exponent) = b >> 7:
-// bin = base + mul * mantissa with mul in {-1, 0, +1} (low 16 bits: base,
-// high 16 bits: mul as a signed value).
-__device__ __forceinline__ uint32_t hist_table_entry(uint32_t se) {
-  const int e = (int)((se & 0xFFu));
-  const bool neg = (se & 0x100u) != 0;
-  int base, mul;
-  if (e >= kFineExpLo && e < kFineExpLo + kFineBinades) {
-    const int f0 = (e - kFineExpLo) << 7;
-    if (neg) { base = kFine - f0; mul = -1; }
-    else { base = kNearZero + 1 + f0; mul = 1; }
-  } else if (e < kFineExpLo) {
-    base = kNearZero; mul = 0;
-  } else {
-    base = kOutOfRange; mul = 0;  // |v| >= 256, inf, NaN; -inf fixed below
-  }
-  return (uint32_t)(base & 0xFFFF) | ((uint32_t)(mul & 0xFFFF) << 16);
+// Order-preserving 16-bit key of a bf16 value and back.
+__device__ __forceinline__ uint32_t bf16_key(uint32_t b) {
+  return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
 }
-
-// Bin of a bf16 value through the table (exact for every value but -inf,
-// which the caller maps to bin 0).
-__device__ __forceinline__ int hist_bin_tab(const uint32_t* tab, uint32_t b) {
-  const uint32_t t = tab[b >> 7];
-  const int base = (int)(t & 0xFFFFu);
-  const int mul = (int)(short)(t >> 16);
-  return base + mul * (int)(b & 0x7Fu);
+__device__ __forceinline__ uint32_t key_bf16(uint32_t k) {
+  return (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
 }
-
-__device__ __forceinline__ int hist_bin(uint32_t b) {
-  const int f = (int)(b & 0x7FFFu) - kFineBase;
-  if ((unsigned)f < (unsigned)kFine) return (b & 0x8000u) ? (kFine - f) : (kNearZero + 1 + f);
-  if (f < 0) return kNearZero;
-  return (b == 0xFF80u) ? 0 : kOutOfRange;
+__device__ __forceinline__ unsigned hist16_count(const uint32_t* h, uint32_t bits) {
+  return (h[bits >> 1] >> ((bits & 1u) << 4)) & 0xFFFFu;
 }
-
-// The bf16 value of a fine bin (also -inf for bin 0).
-__device__ __forceinline__ float hist_value(int idx) {
-  if (idx <= 0) return -INFINITY;
-  uint32_t b;
-  if (idx <= kFine) b = 0x8000u | (uint32_t)(kFine - idx + kFineBase);
-  else b = (uint32_t)(idx - kNearZero - 1 + kFineBase);
-  return __uint_as_float(b << 16);
-}
-
-constexpr int kHistPer = 7;  // bins per consumer thread (7 * 512 >= kHistBins)
 
 // Sum of v over consumer threads with a larger index (exclusive suffix sum).
 // `scratch` holds one slot per consumer warp.
@@ -116,93 +72,109 @@ struct HistResult {
   int pending;  // 1: leave the row to the exact slow path
 };
 
-// Row-end processing of the histogram by the kWarps consumer warps (all of
-// them call it). Clears the histogram for the next row.
+// Row-end processing of the 16-bit value histogram by the kWarps consumer
+// warps (all call it; 128 values per thread, thread t holding the keys
+// [128 t, 128 t + 128)). Clears the histogram for the next row.
 template <int kWarps>
-__device__ HistResult hist_finish(unsigned* hist, float* nz, float m, float c, int tk, float tp,
-                                  int V, int tid, float* fscr, int* iscr) {
-  const float mc = m * c;
-  const int b0 = tid * kHistPer;
-  unsigned cnt[kHistPer];
-  float mass[kHistPer];
-  const float nz_mass = *nz * ex2(-mc);
-#pragma unroll
-  for (int i = 0; i < kHistPer; ++i) {
-    const int b = b0 + i;
-    const unsigned n = (b < kHistBins) ? hist[b] : 0u;
-    cnt[i] = n;
-    float w = 0.f;
-    if (n && b > 0 && b != kOutOfRange)
-      w = (b == kNearZero) ? nz_mass : (float)n * ex2(fmaf(hist_value(b), c, -mc));
-    mass[i] = w;
+__device__ HistResult hist16_finish(uint32_t* h, float m, float c, int tk, float tp, int V,
+                                    int tid, float* fscr, int* iscr) {
+  static_assert(kWarps * 32 * 128 == 65536, "128 keys per consumer thread");
+  if (tid == 0) {
+    // -0 and +0 are one value: move the count of -0 (bits 0x8000) to +0.
+    const unsigned neg0 = h[0x4000] & 0xFFFFu;
+    h[0x4000] &= 0xFFFF0000u;
+    h[0] += neg0;  // a carry out of +0 breaks the total below: detected
   }
-  const int oor = consumer_reduce<int, kWarps>(
-      (b0 <= kOutOfRange && kOutOfRange < b0 + kHistPer) ? (int)cnt[kOutOfRange - b0] : 0,
-      iscr, tid, [](int a, int b) { return a + b; });
+  named_sync(1, kWarps * 32);
+  const float mc = m * c;
+  const uint32_t k0 = (uint32_t)tid * 128u;
+  // mass of one value (0 for -inf); nonfinite values flagged separately
+  auto mass_of = [&](uint32_t bits, unsigned n) -> float {
+    if (!n || bits == 0xFF80u) return 0.f;
+    return (float)n * ex2(fmaf(__uint_as_float(bits << 16), c, -mc));
+  };
+  unsigned cnt_t = 0, bad_t = 0;
+  float mass_t = 0.f;
+  for (uint32_t k = k0; k < k0 + 128u; ++k) {
+    const uint32_t bits = key_bf16(k);
+    const unsigned n = hist16_count(h, bits);
+    cnt_t += n;
+    const bool nonfinite = ((bits & 0x7F80u) == 0x7F80u) && bits != 0xFF80u;
+    if (nonfinite) bad_t += n;
+    else mass_t += mass_of(bits, n);
+  }
+  const int total = consumer_reduce<int, kWarps>((int)cnt_t, iscr, tid,
+                                                 [](int a, int b) { return a + b; });
+  const int bad = consumer_reduce<int, kWarps>((int)bad_t, iscr, tid,
+                                               [](int a, int b) { return a + b; });
   const bool topk_on = (tk > 0 && tk < V);
   const bool topp_on = (tp < 1.f);
 
-  // top-k: the bin holding the k-th largest value (counts from the top).
+  // top-k: the key holding the k-th largest value (counts from the top).
   int bk = 0;
   if (topk_on) {
-    unsigned tc = 0;
-#pragma unroll
-    for (int i = 0; i < kHistPer; ++i) tc += cnt[i];
-    unsigned run = suffix_exclusive<unsigned, kWarps>(tc, (unsigned*)iscr, tid);
+    unsigned run = suffix_exclusive<unsigned, kWarps>(cnt_t, (unsigned*)iscr, tid);
     int cand = -1;
-#pragma unroll
-    for (int i = kHistPer - 1; i >= 0; --i) {
-      if (run < (unsigned)tk && run + cnt[i] >= (unsigned)tk) cand = b0 + i;
-      run += cnt[i];
+    if (run < (unsigned)tk && run + cnt_t >= (unsigned)tk) {
+      for (int k = (int)k0 + 127; k >= (int)k0; --k) {
+        const unsigned n = hist16_count(h, key_bf16((uint32_t)k));
+        if (run < (unsigned)tk && run + n >= (unsigned)tk) cand = k;
+        run += n;
+      }
     }
     bk = consumer_reduce<int, kWarps>(cand, iscr, tid, [](int a, int b) { return a > b ? a : b; });
     if (bk < 0) bk = 0;
   }
-  float part = 0.f;
-#pragma unroll
-  for (int i = 0; i < kHistPer; ++i)
-    if (b0 + i >= bk) part += mass[i];
-  const float zk = consumer_reduce<float, kWarps>(part, fscr, tid,
+  // mass of this thread's keys >= key0 (walking only when the range is cut)
+  auto mass_from = [&](int key0) -> float {
+    if ((int)k0 >= key0) return mass_t;
+    if ((int)k0 + 127 < key0) return 0.f;
+    float w = 0.f;
+    for (int k = key0; k <= (int)k0 + 127; ++k) {
+      const uint32_t bits = key_bf16((uint32_t)k);
+      if ((bits & 0x7F80u) == 0x7F80u && bits != 0xFF80u) continue;
+      w += mass_of(bits, hist16_count(h, bits));
+    }
+    return w;
+  };
+  const float part_k = mass_from(bk);
+  const float zk = consumer_reduce<float, kWarps>(part_k, fscr, tid,
                                                   [](float a, float b) { return a + b; });
 
-  // top-p: keep bin b iff the mass strictly above it (within the top-k set)
-  // is < top_p * Z_k; the kept bins are the top ones down to bp.
+  // top-p: keep value v iff the mass strictly above it (within the top-k set)
+  // is < top_p * Z_k; the kept values are the top ones down to bp.
   int bp = bk;
   if (topp_on) {
     const float thr = tp * zk;
-    float tm = 0.f;
-#pragma unroll
-    for (int i = 0; i < kHistPer; ++i)
-      if (b0 + i >= bk) tm += mass[i];
-    float run = suffix_exclusive<float, kWarps>(tm, fscr, tid);
+    float run = suffix_exclusive<float, kWarps>(part_k, fscr, tid);
     int cand = 0x7FFFFFFF;
-#pragma unroll
-    for (int i = kHistPer - 1; i >= 0; --i) {
-      const int b = b0 + i;
-      if (b >= bk && cnt[i] && run < thr) cand = b;
-      if (b >= bk) run += mass[i];
+    if (part_k > 0.f && run < thr) {
+      for (int k = (int)k0 + 127; k >= (int)k0 && k >= bk; --k) {
+        const uint32_t bits = key_bf16((uint32_t)k);
+        const unsigned n = hist16_count(h, bits);
+        if (n && run < thr) cand = k;
+        if (!((bits & 0x7F80u) == 0x7F80u && bits != 0xFF80u)) run += mass_of(bits, n);
+      }
     }
     bp = consumer_reduce<int, kWarps>(cand, iscr, tid, [](int a, int b) { return a < b ? a : b; });
     if (bp == 0x7FFFFFFF) bp = bk;
   }
-  part = 0.f;
-#pragma unroll
-  for (int i = 0; i < kHistPer; ++i)
-    if (b0 + i >= bp) part += mass[i];
-  const float z = consumer_reduce<float, kWarps>(part, fscr, tid,
+  const float z = consumer_reduce<float, kWarps>(mass_from(bp), fscr, tid,
                                                  [](float a, float b) { return a + b; });
 
-  // clear for the next row
+  // clear for the next row (this thread's 64 words)
+  {
+    const uint32_t b_lo = key_bf16(k0), b_hi = key_bf16(k0 + 127u);
+    const uint32_t w0 = (b_lo < b_hi ? b_lo : b_hi) >> 1;
+    uint4* p = reinterpret_cast<uint4*>(h + w0);
 #pragma unroll
-  for (int i = 0; i < kHistPer; ++i)
-    if (b0 + i < kHistBins) hist[b0 + i] = 0u;
-  if (tid == 0) *nz = 0.f;
+    for (int i = 0; i < 16; ++i) p[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
   named_sync(1, kWarps * 32);
 
   HistResult res;
-  res.pending = (oor > 0) || (topk_on && bk == kNearZero) ||
-                ((topk_on || topp_on) && bp == kNearZero);
-  res.theta = (topk_on || topp_on) ? hist_value(bp) : -INFINITY;
+  res.pending = (total != V) || (bad > 0);
+  res.theta = (topk_on || topp_on) ? __uint_as_float(key_bf16((uint32_t)bp) << 16) : -INFINITY;
   res.z = z;
   return res;
 }

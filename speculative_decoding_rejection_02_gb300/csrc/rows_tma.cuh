@@ -43,6 +43,9 @@ struct StageMeta {
 constexpr size_t kTmaSmemBytes =
     (size_t)kTmaStages * kTmaStageBytes + 2 * kTmaStages * sizeof(uint64_t) +
     kTmaStages * sizeof(StageMeta);
+// The top-k / top-p variant adds the 128 KB value histogram (16-byte aligned).
+constexpr size_t kTmaHistOffset = (kTmaSmemBytes + 255) & ~size_t(255);
+constexpr size_t kTmaFiltSmemBytes = kTmaHistOffset + kHist16Bytes;
 
 struct RowInfo {
   long long row;
@@ -56,7 +59,8 @@ struct RowInfo {
 // Warp-parallel lookup of the request owning `row` and its settings (all 32
 // lanes call it; every lane gets the result). Two or three dependent rounds
 // of loads instead of a serial binary search.
-__device__ RowInfo warp_row_info(const Params& P, long long row, bool take_filtered) {
+// want_filtered: take only rows with top-k / top-p (true) or only the others.
+__device__ RowInfo warp_row_info(const Params& P, long long row, bool want_filtered) {
   const int lane = threadIdx.x & 31;
   int lo = 0, hi = P.B;  // answer in [lo, hi)
   while (hi - lo > 1) {
@@ -105,14 +109,18 @@ __device__ RowInfo warp_row_info(const Params& P, long long row, bool take_filte
   info.x = __shfl_sync(0xFFFFFFFFu, x, 0);
   info.tk = __shfl_sync(0xFFFFFFFFu, tk, 0);
   info.tp = __shfl_sync(0xFFFFFFFFu, tp, 0);
-  info.cls = (cls == kFiltered && !take_filtered) ? -1 : cls;
+  info.cls = ((cls == kFiltered) != want_filtered) ? -1 : cls;
   info.c = (cls != kArgmaxOnly) ? kLog2e / T : 0.f;
   return info;
 }
 
-template <bool BF16>
-__global__ void __launch_bounds__(kTmaThreads, 2)
+// FILT = false: argmax-only and plain-softmax rows (2 CTAs per SM).
+// FILT = true (bf16 only): rows with top-k / top-p, counted into a value
+// histogram (1 CTA per SM: the histogram takes 128 KB).
+template <bool BF16, bool FILT>
+__global__ void __launch_bounds__(kTmaThreads, FILT ? 1 : 2)
 k_rows_tma(Params P, long long R) {
+  static_assert(!FILT || BF16, "the histogram path is for bf16 rows");
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTmaStages * kTmaStageBytes);
@@ -143,7 +151,7 @@ k_rows_tma(Params P, long long R) {
     RowInfo cur;
     cur.cls = -1;
     while (row < R) {  // first row with work
-      cur = warp_row_info(P, row, BF16);
+      cur = warp_row_info(P, row, FILT);
       if (cur.cls >= 0) break;
       row += gridDim.x;
     }
@@ -186,7 +194,7 @@ k_rows_tma(Params P, long long R) {
         if (ch == 0) {
           // Look the next row up while this one streams.
           while (nrow < R) {
-            next = warp_row_info(P, nrow, BF16);
+            next = warp_row_info(P, nrow, FILT);
             if (next.cls >= 0) break;
             nrow += gridDim.x;
           }
@@ -222,18 +230,16 @@ k_rows_tma(Params P, long long R) {
   __shared__ int red_i[kTmaConsumerWarps];
   __shared__ float bc_m, s_lx;
   __shared__ int bc_i;
-  // Value histogram of the current filtered row (bf16 only).
-  __shared__ unsigned hist[BF16 ? kHistBins : 1];
-  __shared__ uint32_t hist_tab[BF16 ? 512 : 1];
-  __shared__ float hist_nz;
   __shared__ float fscr[kTmaConsumerWarps];
   __shared__ int iscr[kTmaConsumerWarps];
   const int tid = threadIdx.x;
   constexpr int epc = 16 / esize;
-  if (BF16) {
-    for (int b = tid; b < kHistBins; b += kTmaConsumers) hist[b] = 0u;
-    for (int e = tid; e < 512; e += kTmaConsumers) hist_tab[e] = hist_table_entry((uint32_t)e);
-    if (tid == 0) hist_nz = 0.f;
+  // Value histogram of the current filtered row (FILT only): 16-bit counters.
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kTmaHistOffset);
+  if (FILT) {
+    uint4* hz = reinterpret_cast<uint4*>(hist);
+    for (int i = tid; i < (int)(kHist16Bytes / 16); i += kTmaConsumers)
+      hz[i] = make_uint4(0u, 0u, 0u, 0u);
     named_sync(1, kTmaConsumers);
   }
   int stage = 0;
@@ -331,19 +337,17 @@ k_rows_tma(Params P, long long R) {
       f2_unpack(acc1, a2, a3);
       s += (a0 + a1) + (a2 + a3);
     }
-    if (BF16 && M.cls == kFiltered) {
-      // Count every element in its value's bin (exact top-k / top-p later).
+    if (FILT) {
+      // Count every element under its raw bits (two 16-bit counters a word).
 #pragma unroll
       for (int k = 0; k < kTmaVecPerThread; ++k) {
         if (tid + k * kTmaConsumers >= nvec) continue;
         const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          const uint32_t b = (t & 1) ? (w[t >> 1] >> 16) : (w[t >> 1] & 0xFFFFu);
-          int idx = hist_bin_tab(hist_tab, b);
-          if (b == 0xFF80u) idx = 0;  // -inf
-          atomicAdd(&hist[idx], 1u);
-          if (idx == kNearZero) atomicAdd(&hist_nz, ex2(__uint_as_float(b << 16) * M.c));
+        for (int t = 0; t < 4; ++t) {
+          const uint32_t lo = w[t] & 0xFFFFu, hi = w[t] >> 16;
+          atomicAdd(&hist[lo >> 1], (lo & 1u) ? 0x10000u : 1u);
+          atomicAdd(&hist[hi >> 1], (hi & 1u) ? 0x10000u : 1u);
         }
       }
     }
@@ -395,9 +399,9 @@ k_rows_tma(Params P, long long R) {
       named_sync(1, kTmaConsumers);
       m = bc_m;
       a = bc_i;
-      if (BF16 && M.cls == kFiltered) {
-        const HistResult hr = hist_finish<kTmaConsumerWarps>(hist, &hist_nz, m, M.c, M.tk, M.tp,
-                                                             P.V, tid, fscr, iscr);
+      if (FILT) {
+        const HistResult hr = hist16_finish<kTmaConsumerWarps>(hist, m, M.c, M.tk, M.tp, P.V,
+                                                               tid, fscr, iscr);
         if (tid == 0) {
           if (hr.pending || !(m > -INFINITY)) {
             RowStats ps;

@@ -32,7 +32,8 @@ struct spec_verify_handle {
   int max_slices;
   cudaEvent_t phase[4];
   int n_phase;
-  int tma_blocks;  // resident CTAs of k_rows_tma on the device
+  int tma_blocks;   // resident CTAs of k_rows_tma<.., false> on the device
+  int filt_blocks;  // resident CTAs of k_rows_tma<true, true>
 };
 
 namespace {
@@ -104,13 +105,22 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   const int esize = P.bf16 ? 2 : 4;
   const bool rows_aligned = (((long long)b->V * esize) % 16 == 0) &&
                             ((reinterpret_cast<uintptr_t>(b->target_logits) & 15) == 0);
-  P.fast_filtered = (rows_aligned && h->tma_blocks > 0 && P.bf16) ? 1 : 0;
+  const bool filters = !greedy && (P.top_k || P.top_p);
+  P.fast_filtered = (rows_aligned && h->tma_blocks > 0 && h->filt_blocks > 0 && P.bf16 &&
+                     filters) ? 1 : 0;
   if (rows_aligned && h->tma_blocks > 0) {
     const long long grid = R < h->tma_blocks ? R : h->tma_blocks;
     if (P.bf16)
-      sv::k_rows_tma<true><<<(unsigned)grid, sv::kTmaThreads, sv::kTmaSmemBytes, stream>>>(P, R);
+      sv::k_rows_tma<true, false><<<(unsigned)grid, sv::kTmaThreads, sv::kTmaSmemBytes, stream>>>(
+          P, R);
     else
-      sv::k_rows_tma<false><<<(unsigned)grid, sv::kTmaThreads, sv::kTmaSmemBytes, stream>>>(P, R);
+      sv::k_rows_tma<false, false><<<(unsigned)grid, sv::kTmaThreads, sv::kTmaSmemBytes,
+                                     stream>>>(P, R);
+    if (P.fast_filtered) {
+      const long long fgrid = R < h->filt_blocks ? R : h->filt_blocks;
+      sv::k_rows_tma<true, true><<<(unsigned)fgrid, sv::kTmaThreads, sv::kTmaFiltSmemBytes,
+                                   stream>>>(P, R);
+    }
   } else {
     sv::k_rows_stream<<<(unsigned)(R * P.slices_per_row), sv::kStreamThreads, 0, stream>>>(P);
   }
@@ -156,17 +166,30 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   h->cfg = *cfg;
   h->sm_count = prop.multiProcessorCount;
   int per_sm = 0;
-  if (cudaFuncSetAttribute(sv::k_rows_tma<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  int filt_per_sm = 0;
+  if (cudaFuncSetAttribute(sv::k_rows_tma<true, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)sv::kTmaSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(sv::k_rows_tma<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(sv::k_rows_tma<false, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)sv::kTmaSmemBytes) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv::k_rows_tma<true>,
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv::k_rows_tma<true, false>,
                                                     sv::kTmaThreads,
                                                     sv::kTmaSmemBytes) != cudaSuccess) {
     cudaGetLastError();
     per_sm = 0;
   }
+  if (cudaFuncSetAttribute(sv::k_rows_tma<true, true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)sv::kTmaFiltSmemBytes) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&filt_per_sm, sv::k_rows_tma<true, true>,
+                                                    sv::kTmaThreads,
+                                                    sv::kTmaFiltSmemBytes) != cudaSuccess) {
+    cudaGetLastError();
+    filt_per_sm = 0;
+  }
   h->tma_blocks = per_sm * prop.multiProcessorCount;
+  h->filt_blocks = filt_per_sm * prop.multiProcessorCount;
   if (cudaFuncSetAttribute(sv::k_race, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)sv::race_smem_bytes(4)) != cudaSuccess) {
     delete h;
@@ -297,6 +320,7 @@ struct NoallocDevice {
   char* base;  // device address of g_noalloc_scratch on this device
   int sm_count;
   int tma_blocks;
+  int filt_blocks;
 };
 NoallocDevice g_na_dev[kNaMaxDevices];
 std::mutex g_na_mutex;
@@ -336,22 +360,31 @@ extern "C" int spec_verify_run_noalloc(const spec_verify_batch* b, void* stream,
         cudaGetLastError();
         return SPEC_ERR_CUDA;
       }
-      int per_sm = 0;
-      if (cudaFuncSetAttribute(sv::k_rows_tma<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      int per_sm = 0, filt_per_sm = 0;
+      if (cudaFuncSetAttribute(sv::k_rows_tma<true, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)sv::kTmaSmemBytes) != cudaSuccess ||
-          cudaFuncSetAttribute(sv::k_rows_tma<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+          cudaFuncSetAttribute(sv::k_rows_tma<false, false>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)sv::kTmaSmemBytes) != cudaSuccess ||
+          cudaFuncSetAttribute(sv::k_rows_tma<true, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)sv::kTmaFiltSmemBytes) != cudaSuccess ||
           cudaFuncSetAttribute(sv::k_race, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)sv::race_smem_bytes(4)) != cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv::k_rows_tma<true>,
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv::k_rows_tma<true, false>,
                                                         sv::kTmaThreads,
-                                                        sv::kTmaSmemBytes) != cudaSuccess) {
+                                                        sv::kTmaSmemBytes) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&filt_per_sm, sv::k_rows_tma<true, true>,
+                                                        sv::kTmaThreads,
+                                                        sv::kTmaFiltSmemBytes) != cudaSuccess) {
         cudaGetLastError();
         return SPEC_ERR_CUDA;
       }
       slot.base = (char*)ptr;
       slot.sm_count = prop.multiProcessorCount;
       slot.tma_blocks = per_sm * prop.multiProcessorCount;
+      slot.filt_blocks = filt_per_sm * prop.multiProcessorCount;
       slot.ready = true;
     }
     nd = slot;
@@ -376,6 +409,7 @@ extern "C" int spec_verify_run_noalloc(const spec_verify_batch* b, void* stream,
   h.max_slices = (int)kNaSlices;
   h.n_phase = 0;
   h.tma_blocks = nd.tma_blocks;
+  h.filt_blocks = nd.filt_blocks;
   // The slice counters must start at zero: clear them (the array keeps the
   // previous call's contents).
   cudaStream_t s = (cudaStream_t)stream;
