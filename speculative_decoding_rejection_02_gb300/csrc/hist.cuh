@@ -72,6 +72,16 @@ struct HistResult {
   int pending;  // 1: leave the row to the exact slow path
 };
 
+// Count and mass of one value (mass 0 for -inf and for NaN / +inf, which
+// are reported separately).
+__device__ __forceinline__ bool bf16_nonfinite(uint32_t bits) {
+  return ((bits & 0x7F80u) == 0x7F80u) && bits != 0xFF80u;
+}
+__device__ __forceinline__ float value_mass(uint32_t bits, unsigned n, float c, float mc) {
+  if (!n || bits == 0xFF80u || bf16_nonfinite(bits)) return 0.f;
+  return (float)n * ex2(fmaf(__uint_as_float(bits << 16), c, -mc));
+}
+
 // Row-end processing of the 16-bit value histogram by the kWarps consumer
 // warps (all call it; 128 values per thread, thread t holding the keys
 // [128 t, 128 t + 128)). Clears the histogram for the next row.
@@ -79,6 +89,12 @@ template <int kWarps>
 __device__ HistResult hist16_finish(uint32_t* h, float m, float c, int tk, float tp, int V,
                                     int tid, float* fscr, int* iscr) {
   static_assert(kWarps * 32 * 128 == 65536, "128 keys per consumer thread");
+  __shared__ float s_w[128];
+  __shared__ unsigned s_n[128];
+  __shared__ int s_blk;
+  __shared__ float s_above_f;
+  __shared__ unsigned s_above_u;
+  __shared__ int s_key;
   if (tid == 0) {
     // -0 and +0 are one value: move the count of -0 (bits 0x8000) to +0.
     const unsigned neg0 = h[0x4000] & 0xFFFFu;
@@ -88,20 +104,29 @@ __device__ HistResult hist16_finish(uint32_t* h, float m, float c, int tk, float
   named_sync(1, kWarps * 32);
   const float mc = m * c;
   const uint32_t k0 = (uint32_t)tid * 128u;
-  // mass of one value (0 for -inf); nonfinite values flagged separately
-  auto mass_of = [&](uint32_t bits, unsigned n) -> float {
-    if (!n || bits == 0xFF80u) return 0.f;
-    return (float)n * ex2(fmaf(__uint_as_float(bits << 16), c, -mc));
-  };
+  // This thread's 128 values occupy 64 consecutive words.
+  const uint32_t blo = key_bf16(k0), bhi = key_bf16(k0 + 127u);
+  const uint32_t bmin = blo < bhi ? blo : bhi;
+  const uint4* hw = reinterpret_cast<const uint4*>(h + (bmin >> 1));
   unsigned cnt_t = 0, bad_t = 0;
   float mass_t = 0.f;
-  for (uint32_t k = k0; k < k0 + 128u; ++k) {
-    const uint32_t bits = key_bf16(k);
-    const unsigned n = hist16_count(h, bits);
-    cnt_t += n;
-    const bool nonfinite = ((bits & 0x7F80u) == 0x7F80u) && bits != 0xFF80u;
-    if (nonfinite) bad_t += n;
-    else mass_t += mass_of(bits, n);
+#pragma unroll 4
+  for (int i = 0; i < 16; ++i) {
+    const uint4 q = hw[i];
+    if ((q.x | q.y | q.z | q.w) == 0u) continue;
+    const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (!wd[j]) continue;
+#pragma unroll
+      for (int hl = 0; hl < 2; ++hl) {
+        const unsigned n = (wd[j] >> (16 * hl)) & 0xFFFFu;
+        const uint32_t bits = bmin + (uint32_t)(8 * i + 2 * j + hl);
+        cnt_t += n;
+        if (bf16_nonfinite(bits)) bad_t += n;
+        else mass_t += value_mass(bits, n, c, mc);
+      }
+    }
   }
   const int total = consumer_reduce<int, kWarps>((int)cnt_t, iscr, tid,
                                                  [](int a, int b) { return a + b; });
@@ -110,30 +135,46 @@ __device__ HistResult hist16_finish(uint32_t* h, float m, float c, int tk, float
   const bool topk_on = (tk > 0 && tk < V);
   const bool topp_on = (tp < 1.f);
 
+  // Weight (count or mass) of key k0 + i for the block being refined.
+  auto key_count = [&](int blk, int i) -> unsigned {
+    return hist16_count(h, key_bf16((uint32_t)(blk * 128 + i)));
+  };
+
   // top-k: the key holding the k-th largest value (counts from the top).
   int bk = 0;
   if (topk_on) {
-    unsigned run = suffix_exclusive<unsigned, kWarps>(cnt_t, (unsigned*)iscr, tid);
-    int cand = -1;
+    if (tid == 0) s_blk = 0;
+    const unsigned run = suffix_exclusive<unsigned, kWarps>(cnt_t, (unsigned*)iscr, tid);
     if (run < (unsigned)tk && run + cnt_t >= (unsigned)tk) {
-      for (int k = (int)k0 + 127; k >= (int)k0; --k) {
-        const unsigned n = hist16_count(h, key_bf16((uint32_t)k));
-        if (run < (unsigned)tk && run + n >= (unsigned)tk) cand = k;
-        run += n;
-      }
+      s_blk = tid;
+      s_above_u = run;
     }
-    bk = consumer_reduce<int, kWarps>(cand, iscr, tid, [](int a, int b) { return a > b ? a : b; });
-    if (bk < 0) bk = 0;
+    named_sync(1, kWarps * 32);
+    const int blk = s_blk;
+    // 128 threads refine the block: suffix counts from the top key down.
+    if (tid < 128) s_n[tid] = key_count(blk, tid);
+    named_sync(1, kWarps * 32);
+    if (tid == 0) {
+      unsigned r = s_above_u;
+      int key = blk * 128;
+      for (int i = 127; i >= 0; --i) {
+        const unsigned n = s_n[i];
+        if (r < (unsigned)tk && r + n >= (unsigned)tk) { key = blk * 128 + i; break; }
+        r += n;
+      }
+      s_key = key;
+    }
+    named_sync(1, kWarps * 32);
+    bk = s_key;
   }
-  // mass of this thread's keys >= key0 (walking only when the range is cut)
+  // This thread's mass over keys >= key0.
   auto mass_from = [&](int key0) -> float {
     if ((int)k0 >= key0) return mass_t;
     if ((int)k0 + 127 < key0) return 0.f;
     float w = 0.f;
     for (int k = key0; k <= (int)k0 + 127; ++k) {
       const uint32_t bits = key_bf16((uint32_t)k);
-      if ((bits & 0x7F80u) == 0x7F80u && bits != 0xFF80u) continue;
-      w += mass_of(bits, hist16_count(h, bits));
+      w += value_mass(bits, hist16_count(h, bits), c, mc);
     }
     return w;
   };
@@ -146,29 +187,44 @@ __device__ HistResult hist16_finish(uint32_t* h, float m, float c, int tk, float
   int bp = bk;
   if (topp_on) {
     const float thr = tp * zk;
-    float run = suffix_exclusive<float, kWarps>(part_k, fscr, tid);
-    int cand = 0x7FFFFFFF;
-    if (part_k > 0.f && run < thr) {
-      for (int k = (int)k0 + 127; k >= (int)k0 && k >= bk; --k) {
-        const uint32_t bits = key_bf16((uint32_t)k);
-        const unsigned n = hist16_count(h, bits);
-        if (n && run < thr) cand = k;
-        if (!((bits & 0x7F80u) == 0x7F80u && bits != 0xFF80u)) run += mass_of(bits, n);
-      }
+    const float run = suffix_exclusive<float, kWarps>(part_k, fscr, tid);
+    // The lowest block whose mass above is below thr holds the crossing
+    // (every lower block has mass above >= thr and is dropped whole).
+    if (tid == 0) s_blk = 0x7FFFFFFF;
+    named_sync(1, kWarps * 32);
+    if (part_k > 0.f && run < thr) atomicMin(&s_blk, tid);
+    named_sync(1, kWarps * 32);
+    const int blk = s_blk == 0x7FFFFFFF ? 0 : s_blk;
+    if (tid == blk) s_above_f = run;
+    named_sync(1, kWarps * 32);
+    if (tid < 128) {
+      const int key = blk * 128 + tid;
+      const uint32_t bits = key_bf16((uint32_t)key);
+      const unsigned n = hist16_count(h, bits);
+      s_n[tid] = (key >= bk) ? n : 0u;
+      s_w[tid] = (key >= bk) ? value_mass(bits, n, c, mc) : 0.f;
     }
-    bp = consumer_reduce<int, kWarps>(cand, iscr, tid, [](int a, int b) { return a < b ? a : b; });
-    if (bp == 0x7FFFFFFF) bp = bk;
+    named_sync(1, kWarps * 32);
+    if (tid == 0) {
+      float a = s_above_f;
+      int key = blk * 128 + 127;
+      for (int i = 127; i >= 0; --i) {
+        if (s_n[i] && a < thr) key = blk * 128 + i;
+        a += s_w[i];
+      }
+      s_key = key;
+    }
+    named_sync(1, kWarps * 32);
+    bp = s_key;
   }
   const float z = consumer_reduce<float, kWarps>(mass_from(bp), fscr, tid,
                                                  [](float a, float b) { return a + b; });
 
   // clear for the next row (this thread's 64 words)
   {
-    const uint32_t b_lo = key_bf16(k0), b_hi = key_bf16(k0 + 127u);
-    const uint32_t w0 = (b_lo < b_hi ? b_lo : b_hi) >> 1;
-    uint4* p = reinterpret_cast<uint4*>(h + w0);
+    uint4* pz = reinterpret_cast<uint4*>(h + (bmin >> 1));
 #pragma unroll
-    for (int i = 0; i < 16; ++i) p[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = 0; i < 16; ++i) pz[i] = make_uint4(0u, 0u, 0u, 0u);
   }
   named_sync(1, kWarps * 32);
 
