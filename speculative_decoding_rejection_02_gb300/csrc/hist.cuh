@@ -82,19 +82,70 @@ __device__ __forceinline__ float value_mass(uint32_t bits, unsigned n, float c, 
   return (float)n * ex2(fmaf(__uint_as_float(bits << 16), c, -mc));
 }
 
+// Warp-level refinement inside one 128-key block (keys 128 blk + 4 lane ..
+// + 3): returns, in every lane of the calling warp,
+//   mode 0: the largest key whose weight summed from the top of the block,
+//           plus `above`, reaches `target` (top-k: counts);
+//   mode 1: the smallest nonempty key >= `from` whose weight strictly above
+//           it, plus `above`, is < `target` (top-p: masses).
+// `wt(key)` gives the weight of a key (0 below `from`), `nz(key)` whether it
+// holds tokens.
+template <typename Wt, typename Nz>
+__device__ __forceinline__ int warp_refine(int blk, float above, float target, int mode, Wt wt,
+                                           Nz nz) {
+  const int lane = threadIdx.x & 31;
+  float w[4];
+  bool nzv[4];
+  float mine = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int key = blk * 128 + 4 * lane + e;
+    w[e] = wt(key);
+    nzv[e] = nz(key);
+    mine += w[e];
+  }
+  // weight of all lanes above this one (keys of higher lanes are larger)
+  float x = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_down_sync(0xFFFFFFFFu, x, o);
+    if (lane + o < 32) x += y;
+  }
+  float run = above + (x - mine);  // weight strictly above this lane's keys
+  int cand = mode == 0 ? -1 : 0x7FFFFFFF;
+#pragma unroll
+  for (int e = 3; e >= 0; --e) {
+    const int key = blk * 128 + 4 * lane + e;
+    if (mode == 0) {
+      if (cand < 0 && run < target && run + w[e] >= target) cand = key;
+    } else if (nzv[e] && run < target) {
+      cand = key;
+    }
+    run += w[e];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const int c2 = __shfl_xor_sync(0xFFFFFFFFu, cand, o);
+    cand = mode == 0 ? max(cand, c2) : min(cand, c2);
+  }
+  return cand;
+}
+
 // Row-end processing of the 16-bit value histogram by the kWarps consumer
-// warps (all call it; 128 values per thread, thread t holding the keys
-// [128 t, 128 t + 128)). Clears the histogram for the next row.
+// warps (all call it). Warp w sums the 128-key blocks w, w + kWarps, ...
+// (empty blocks cost one ballot), so dense and sparse key ranges spread
+// over all warps; the per-block totals then locate the top-k and top-p
+// blocks, which one warp refines to the exact value. Clears the histogram.
 template <int kWarps>
 __device__ HistResult hist16_finish(uint32_t* h, float m, float c, int tk, float tp, int V,
                                     int tid, float* fscr, int* iscr) {
-  static_assert(kWarps * 32 * 128 == 65536, "128 keys per consumer thread");
-  __shared__ float s_w[128];
-  __shared__ unsigned s_n[128];
-  __shared__ int s_blk;
-  __shared__ float s_above_f;
-  __shared__ unsigned s_above_u;
-  __shared__ int s_key;
+  constexpr int kBlocks = 512;  // 128 keys each
+  static_assert(kWarps * 32 == kBlocks, "one block total per consumer thread");
+  __shared__ unsigned blk_cnt[kBlocks];
+  __shared__ float blk_mass[kBlocks];
+  __shared__ int s_blk, s_key;
+  __shared__ float s_above;
+  const int lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     // -0 and +0 are one value: move the count of -0 (bits 0x8000) to +0.
     const unsigned neg0 = h[0x4000] & 0xFFFFu;
@@ -103,42 +154,56 @@ __device__ HistResult hist16_finish(uint32_t* h, float m, float c, int tk, float
   }
   named_sync(1, kWarps * 32);
   const float mc = m * c;
-  const uint32_t k0 = (uint32_t)tid * 128u;
-  // This thread's 128 values occupy 64 consecutive words.
-  const uint32_t blo = key_bf16(k0), bhi = key_bf16(k0 + 127u);
-  const uint32_t bmin = blo < bhi ? blo : bhi;
-  const uint4* hw = reinterpret_cast<const uint4*>(h + (bmin >> 1));
-  unsigned cnt_t = 0, bad_t = 0;
-  float mass_t = 0.f;
-#pragma unroll 4
-  for (int i = 0; i < 16; ++i) {
-    const uint4 q = hw[i];
-    if ((q.x | q.y | q.z | q.w) == 0u) continue;
-    const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+  auto cnt_of = [&](int key) -> unsigned { return hist16_count(h, key_bf16((uint32_t)key)); };
+  auto mass_of = [&](int key) -> float {
+    const uint32_t bits = key_bf16((uint32_t)key);
+    return value_mass(bits, hist16_count(h, bits), c, mc);
+  };
+
+  // Pass 1: per-block totals. A block's 128 values are 64 consecutive words;
+  // lane l reads words 2l, 2l+1 (keys 4l .. 4l+3 up to the block's order).
+  unsigned bad_w = 0;
+  for (int blk = warp; blk < kBlocks; blk += kWarps) {
+    const uint32_t b0 = key_bf16((uint32_t)blk * 128u), b1 = key_bf16((uint32_t)blk * 128u + 127u);
+    const uint32_t bmin = b0 < b1 ? b0 : b1;
+    const uint2 q = reinterpret_cast<const uint2*>(h + (bmin >> 1))[lane];
+    const bool any = __any_sync(0xFFFFFFFFu, (q.x | q.y) != 0u);
+    unsigned cn = 0;
+    float ms = 0.f;
+    if (any) {
+      const uint32_t wd[2] = {q.x, q.y};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (!wd[j]) continue;
+      for (int j = 0; j < 2; ++j) {
 #pragma unroll
-      for (int hl = 0; hl < 2; ++hl) {
-        const unsigned n = (wd[j] >> (16 * hl)) & 0xFFFFu;
-        const uint32_t bits = bmin + (uint32_t)(8 * i + 2 * j + hl);
-        cnt_t += n;
-        if (bf16_nonfinite(bits)) bad_t += n;
-        else mass_t += value_mass(bits, n, c, mc);
+        for (int hl = 0; hl < 2; ++hl) {
+          const unsigned n = (wd[j] >> (16 * hl)) & 0xFFFFu;
+          const uint32_t bits = bmin + (uint32_t)(4 * lane + 2 * j + hl);
+          cn += n;
+          if (bf16_nonfinite(bits)) bad_w += n;
+          else ms += value_mass(bits, n, c, mc);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        cn += __shfl_xor_sync(0xFFFFFFFFu, cn, o);
+        ms += __shfl_xor_sync(0xFFFFFFFFu, ms, o);
       }
     }
+    if (lane == 0) {
+      blk_cnt[blk] = cn;
+      blk_mass[blk] = ms;
+    }
   }
+  named_sync(1, kWarps * 32);
+  // From here thread t holds block t's totals.
+  const unsigned cnt_t = blk_cnt[tid];
+  const float mass_t = blk_mass[tid];
   const int total = consumer_reduce<int, kWarps>((int)cnt_t, iscr, tid,
                                                  [](int a, int b) { return a + b; });
-  const int bad = consumer_reduce<int, kWarps>((int)bad_t, iscr, tid,
+  const int bad = consumer_reduce<int, kWarps>((int)bad_w, iscr, tid,
                                                [](int a, int b) { return a + b; });
   const bool topk_on = (tk > 0 && tk < V);
   const bool topp_on = (tp < 1.f);
-
-  // Weight (count or mass) of key k0 + i for the block being refined.
-  auto key_count = [&](int blk, int i) -> unsigned {
-    return hist16_count(h, key_bf16((uint32_t)(blk * 128 + i)));
-  };
 
   // top-k: the key holding the k-th largest value (counts from the top).
   int bk = 0;
@@ -147,35 +212,27 @@ __device__ HistResult hist16_finish(uint32_t* h, float m, float c, int tk, float
     const unsigned run = suffix_exclusive<unsigned, kWarps>(cnt_t, (unsigned*)iscr, tid);
     if (run < (unsigned)tk && run + cnt_t >= (unsigned)tk) {
       s_blk = tid;
-      s_above_u = run;
+      s_above = (float)run;
     }
     named_sync(1, kWarps * 32);
-    const int blk = s_blk;
-    // 128 threads refine the block: suffix counts from the top key down.
-    if (tid < 128) s_n[tid] = key_count(blk, tid);
-    named_sync(1, kWarps * 32);
-    if (tid == 0) {
-      unsigned r = s_above_u;
-      int key = blk * 128;
-      for (int i = 127; i >= 0; --i) {
-        const unsigned n = s_n[i];
-        if (r < (unsigned)tk && r + n >= (unsigned)tk) { key = blk * 128 + i; break; }
-        r += n;
-      }
-      s_key = key;
+    if (warp == 0) {
+      const int blk = s_blk;
+      const int key = warp_refine(
+          blk, s_above, (float)tk, 0, [&](int k) { return (float)cnt_of(k); },
+          [&](int k) { return cnt_of(k) != 0u; });
+      if (lane == 0) s_key = key < 0 ? blk * 128 : key;
     }
     named_sync(1, kWarps * 32);
     bk = s_key;
   }
-  // This thread's mass over keys >= key0.
+  // This block's mass over keys >= key0 (the block holding key0 is summed
+  // by its owner thread alone: at most 128 values).
   auto mass_from = [&](int key0) -> float {
-    if ((int)k0 >= key0) return mass_t;
-    if ((int)k0 + 127 < key0) return 0.f;
+    const int k0 = tid * 128;
+    if (k0 >= key0) return mass_t;
+    if (k0 + 127 < key0) return 0.f;
     float w = 0.f;
-    for (int k = key0; k <= (int)k0 + 127; ++k) {
-      const uint32_t bits = key_bf16((uint32_t)k);
-      w += value_mass(bits, hist16_count(h, bits), c, mc);
-    }
+    for (int k = key0; k <= k0 + 127; ++k) w += mass_of(k);
     return w;
   };
   const float part_k = mass_from(bk);
@@ -195,24 +252,13 @@ __device__ HistResult hist16_finish(uint32_t* h, float m, float c, int tk, float
     if (part_k > 0.f && run < thr) atomicMin(&s_blk, tid);
     named_sync(1, kWarps * 32);
     const int blk = s_blk == 0x7FFFFFFF ? 0 : s_blk;
-    if (tid == blk) s_above_f = run;
+    if (tid == blk) s_above = run;
     named_sync(1, kWarps * 32);
-    if (tid < 128) {
-      const int key = blk * 128 + tid;
-      const uint32_t bits = key_bf16((uint32_t)key);
-      const unsigned n = hist16_count(h, bits);
-      s_n[tid] = (key >= bk) ? n : 0u;
-      s_w[tid] = (key >= bk) ? value_mass(bits, n, c, mc) : 0.f;
-    }
-    named_sync(1, kWarps * 32);
-    if (tid == 0) {
-      float a = s_above_f;
-      int key = blk * 128 + 127;
-      for (int i = 127; i >= 0; --i) {
-        if (s_n[i] && a < thr) key = blk * 128 + i;
-        a += s_w[i];
-      }
-      s_key = key;
+    if (warp == 0) {
+      const int key = warp_refine(
+          blk, s_above, thr, 1, [&](int k) { return k >= bk ? mass_of(k) : 0.f; },
+          [&](int k) { return k >= bk && cnt_of(k) != 0u; });
+      if (lane == 0) s_key = (key == 0x7FFFFFFF) ? blk * 128 + 127 : key;
     }
     named_sync(1, kWarps * 32);
     bp = s_key;
@@ -220,9 +266,10 @@ __device__ HistResult hist16_finish(uint32_t* h, float m, float c, int tk, float
   const float z = consumer_reduce<float, kWarps>(mass_from(bp), fscr, tid,
                                                  [](float a, float b) { return a + b; });
 
-  // clear for the next row (this thread's 64 words)
-  {
-    uint4* pz = reinterpret_cast<uint4*>(h + (bmin >> 1));
+  // Clear the blocks that held tokens (thread t: block t's 64 words).
+  if (cnt_t) {
+    const uint32_t b0 = key_bf16((uint32_t)tid * 128u), b1 = key_bf16((uint32_t)tid * 128u + 127u);
+    uint4* pz = reinterpret_cast<uint4*>(h + ((b0 < b1 ? b0 : b1) >> 1));
 #pragma unroll
     for (int i = 0; i < 16; ++i) pz[i] = make_uint4(0u, 0u, 0u, 0u);
   }

@@ -24,9 +24,13 @@ namespace sv {
 constexpr int kTmaConsumerWarps = 16;
 constexpr int kTmaConsumers = kTmaConsumerWarps * 32;
 constexpr int kTmaThreads = kTmaConsumers + 32;
-constexpr int kTmaStageBytes = 32768;
 constexpr int kTmaStages = 3;
-constexpr int kTmaVecPerThread = kTmaStageBytes / 16 / kTmaConsumers;  // 4
+// Stage size: 32 KB for the softmax / argmax rows; 24 KB next to the 128 KB
+// histogram of the top-k / top-p variant.
+__host__ __device__ constexpr int tma_stage_bytes(bool filt) { return filt ? 24576 : 32768; }
+__host__ __device__ constexpr int tma_vec_per_thread(bool filt) {
+  return tma_stage_bytes(filt) / 16 / kTmaConsumers;
+}
 
 struct StageMeta {
   long long row;  // -1: end of work
@@ -40,11 +44,13 @@ struct StageMeta {
   float tp;  // top-p of the row's request (filtered rows)
 };
 
-constexpr size_t kTmaSmemBytes =
-    (size_t)kTmaStages * kTmaStageBytes + 2 * kTmaStages * sizeof(uint64_t) +
-    kTmaStages * sizeof(StageMeta);
+__host__ __device__ constexpr size_t tma_ring_bytes(bool filt) {
+  return (size_t)kTmaStages * tma_stage_bytes(filt) + 2 * kTmaStages * sizeof(uint64_t) +
+         kTmaStages * sizeof(StageMeta);
+}
+constexpr size_t kTmaSmemBytes = tma_ring_bytes(false);
 // The top-k / top-p variant adds the 128 KB value histogram (16-byte aligned).
-constexpr size_t kTmaHistOffset = (kTmaSmemBytes + 255) & ~size_t(255);
+constexpr size_t kTmaHistOffset = (tma_ring_bytes(true) + 255) & ~size_t(255);
 constexpr size_t kTmaFiltSmemBytes = kTmaHistOffset + kHist16Bytes;
 
 struct RowInfo {
@@ -121,6 +127,8 @@ template <bool BF16, bool FILT>
 __global__ void __launch_bounds__(kTmaThreads, FILT ? 1 : 2)
 k_rows_tma(Params P, long long R) {
   static_assert(!FILT || BF16, "the histogram path is for bf16 rows");
+  constexpr int kTmaStageBytes = tma_stage_bytes(FILT);
+  constexpr int kTmaVecPerThread = tma_vec_per_thread(FILT);
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTmaStages * kTmaStageBytes);
