@@ -90,9 +90,11 @@ __device__ __forceinline__ float value_mass(uint32_t bits, unsigned n, float c, 
 //           it, plus `above`, is < `target` (top-p: masses).
 // `wt(key)` gives the weight of a key (0 below `from`), `nz(key)` whether it
 // holds tokens.
-template <typename Wt, typename Nz>
-__device__ __forceinline__ int warp_refine(int blk, float above, float target, int mode, Wt wt,
-                                           Nz nz) {
+// As warp_refine, and *below_sum receives the sum of sw(key) over the
+// block's keys >= the returned key.
+template <typename Wt, typename Nz, typename Sw>
+__device__ __forceinline__ int warp_refine_sum(int blk, float above, float target, int mode,
+                                               Wt wt, Nz nz, Sw sw, float* sum_from) {
   const int lane = threadIdx.x & 31;
   float w[4];
   bool nzv[4];
@@ -128,8 +130,25 @@ __device__ __forceinline__ int warp_refine(int blk, float above, float target, i
     const int c2 = __shfl_xor_sync(0xFFFFFFFFu, cand, o);
     cand = mode == 0 ? max(cand, c2) : min(cand, c2);
   }
+  float part = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int key = blk * 128 + 4 * lane + e;
+    if (key >= cand) part += sw(key);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
+  *sum_from = part;
   return cand;
 }
+
+template <typename Wt, typename Nz>
+__device__ __forceinline__ int warp_refine(int blk, float above, float target, int mode, Wt wt,
+                                           Nz nz) {
+  float unused;
+  return warp_refine_sum(blk, above, target, mode, wt, nz, wt, &unused);
+}
+
 
 // Row-end processing of the 16-bit value histogram by the kWarps consumer
 // warps (all call it). Warp w sums the 128-key blocks w, w + kWarps, ...
@@ -143,8 +162,8 @@ __device__ HistResult hist16_finish(uint32_t* h, float m, float c, int tk, float
   static_assert(kWarps * 32 == kBlocks, "one block total per consumer thread");
   __shared__ unsigned blk_cnt[kBlocks];
   __shared__ float blk_mass[kBlocks];
-  __shared__ int s_blk, s_key;
-  __shared__ float s_above;
+  __shared__ int s_blk, s_key, s_from_blk;
+  __shared__ float s_above, s_from;
   const int lane = tid & 31, warp = tid >> 5;
   if (tid == 0) {
     // -0 and +0 are one value: move the count of -0 (bits 0x8000) to +0.
@@ -217,25 +236,28 @@ __device__ HistResult hist16_finish(uint32_t* h, float m, float c, int tk, float
     named_sync(1, kWarps * 32);
     if (warp == 0) {
       const int blk = s_blk;
-      const int key = warp_refine(
+      float from = 0.f;
+      int key = warp_refine_sum(
           blk, s_above, (float)tk, 0, [&](int k) { return (float)cnt_of(k); },
-          [&](int k) { return cnt_of(k) != 0u; });
-      if (lane == 0) s_key = key < 0 ? blk * 128 : key;
+          [&](int k) { return cnt_of(k) != 0u; }, [&](int k) { return mass_of(k); }, &from);
+      if (lane == 0) {
+        s_key = key < 0 ? blk * 128 : key;
+        s_from = from;
+        s_from_blk = blk;
+      }
     }
     named_sync(1, kWarps * 32);
     bk = s_key;
   }
-  // This block's mass over keys >= key0 (the block holding key0 is summed
-  // by its owner thread alone: at most 128 values).
-  auto mass_from = [&](int key0) -> float {
+  // This block's mass over keys >= key0; the block holding key0 takes the
+  // partial sum its refinement produced.
+  auto mass_from = [&](int key0, float from) -> float {
     const int k0 = tid * 128;
     if (k0 >= key0) return mass_t;
     if (k0 + 127 < key0) return 0.f;
-    float w = 0.f;
-    for (int k = key0; k <= k0 + 127; ++k) w += mass_of(k);
-    return w;
+    return from;
   };
-  const float part_k = mass_from(bk);
+  const float part_k = topk_on ? mass_from(bk, s_from) : mass_t;
   const float zk = consumer_reduce<float, kWarps>(part_k, fscr, tid,
                                                   [](float a, float b) { return a + b; });
 
@@ -255,15 +277,23 @@ __device__ HistResult hist16_finish(uint32_t* h, float m, float c, int tk, float
     if (tid == blk) s_above = run;
     named_sync(1, kWarps * 32);
     if (warp == 0) {
-      const int key = warp_refine(
+      float from = 0.f;
+      const int key = warp_refine_sum(
           blk, s_above, thr, 1, [&](int k) { return k >= bk ? mass_of(k) : 0.f; },
-          [&](int k) { return k >= bk && cnt_of(k) != 0u; });
-      if (lane == 0) s_key = (key == 0x7FFFFFFF) ? blk * 128 + 127 : key;
+          [&](int k) { return k >= bk && cnt_of(k) != 0u; },
+          [&](int k) { return k >= bk ? mass_of(k) : 0.f; }, &from);
+      if (lane == 0) {
+        s_key = (key == 0x7FFFFFFF) ? blk * 128 + 127 : key;
+        s_from = from;
+      }
     }
     named_sync(1, kWarps * 32);
     bp = s_key;
   }
-  const float z = consumer_reduce<float, kWarps>(mass_from(bp), fscr, tid,
+  float zpart;
+  if (topp_on) zpart = mass_from(bp, s_from);
+  else zpart = part_k;
+  const float z = consumer_reduce<float, kWarps>(zpart, fscr, tid,
                                                  [](float a, float b) { return a + b; });
 
   // Clear the blocks that held tokens (thread t: block t's 64 words).
