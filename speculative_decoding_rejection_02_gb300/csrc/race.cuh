@@ -6,12 +6,11 @@
 // with the draft token masked; "드래프트가 제안하고 타깃이 판정한다": the bonus
 // token comes from p of the last row).
 //
-// Persistent CTAs walk the tasks (request, 7168-entry slice), numbered
-// slice-major so that later slices of a request start from the best score
-// its earlier slices published (and from the argmax token's score seeded by
-// the accept scan). Each task's slice of logits and draft probabilities is
-// pulled into shared memory by bulk copies issued one task ahead, so the
-// copies of the next task fly while the current one is scored. Four consecutive entries share
+// One CTA per task (request, 8192-entry slice), numbered slice-major so that
+// later slices of a request start from the best score its earlier slices
+// published (and from the argmax token's score seeded by the accept scan).
+// The CTA pulls its slice of logits and draft probabilities into shared
+// memory with two bulk copies, then scores it. Four consecutive entries share
 // one Philox4x32-10 draw; E = -ln U, score = w / E, the lowest index wins
 // ties. A group whose largest weight w satisfies w * kInvEMin <= best
 // (kInvEMin above 1 / the smallest E a race uniform can give) cannot produce
@@ -31,19 +30,15 @@
 namespace sv {
 
 constexpr int kRaceThreads = 256;
-constexpr int kRaceSlice = 7168;  // entries per task (multiple of 4 * kRaceThreads)
+constexpr int kRaceSlice = 8192;  // entries per task (multiple of 16 * kRaceThreads)
 constexpr int kRaceGroups = 4;    // groups of 4 entries per thread per batch
 // Above 1 / E_min, E_min = -ln(1 - 2^-24) ~ 5.96e-8 the smallest E a race
 // uniform can give: no entry scores more than w * kInvEMin.
 constexpr float kInvEMin = 1.7e7f;
-// Shared memory of the staged path: two buffers (the task being scored and
-// the next one in flight), each the slice's logits then its draft
+// Shared memory of the staged path: the slice's logits and its draft
 // probabilities (fp32).
-__host__ __device__ constexpr size_t race_buf_bytes(int logit_bytes) {
-  return (size_t)kRaceSlice * logit_bytes + (size_t)kRaceSlice * 4;
-}
 __host__ __device__ constexpr size_t race_smem_bytes(int logit_bytes) {
-  return 2 * race_buf_bytes(logit_bytes);
+  return (size_t)kRaceSlice * logit_bytes + (size_t)kRaceSlice * 4;
 }
 
 // What the scoring needs about the race row.
@@ -218,198 +213,175 @@ __device__ void race_range_global(const Params& P, const RaceView& v, int mode, 
   }
 }
 
-struct RaceSlot {
-  RaceTask task;
-  int slice;
-  int staged;  // 1: the slice is in this buffer; 0: read it from global memory
-};
-
 __global__ void __launch_bounds__(kRaceThreads)
 k_race(Params P) {
   extern __shared__ __align__(128) unsigned char race_smem[];
-  __shared__ RaceItem queue[kRaceThreads * kRaceGroups];
-  __shared__ __align__(8) uint64_t bar[2];
-  __shared__ RaceSlot slot[2];
   __shared__ int s_last;
   __shared__ unsigned long long s_packed;
+  __shared__ RaceItem queue[kRaceThreads * kRaceGroups];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int s_staged;
 
   const unsigned n_race = *P.race_count;
-  const unsigned tasks = n_race * (unsigned)P.race_slices;
-  if (blockIdx.x >= tasks) return;
+  const unsigned t = blockIdx.x;
+  if (t >= n_race * (unsigned)P.race_slices) return;
+  const int slice = (int)(t / n_race);
+  const RaceTask task = P.race_list[t % n_race];
+  const int r = task.r;
+  const RaceView v = race_view(P, r, task.row, task.qrow, task.kstar, task.mode, task.x, task.m,
+                               task.c, task.inv_z, task.theta, task.z);
   const int V = P.V;
-  const int esize = P.bf16 ? 2 : 4;
-  const size_t bufsz = race_buf_bytes(esize);
   const uint32_t groups = (uint32_t)((V + 3) / 4);
-  if (threadIdx.x == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
+  const uint32_t g0 = (uint32_t)slice * (kRaceSlice / 4);
+  const uint32_t g1 = min(groups, g0 + (uint32_t)(kRaceSlice / 4));
+  const int j0 = (int)(g0 * 4u);
+  const int n = min(kRaceSlice, V - j0);
+  const int esize = P.bf16 ? 2 : 4;
+  const bool resid = (v.mode == kRaceResidual);
+  const char* lsrc = (const char*)P.logits + ((long long)v.row * V + j0) * esize;
+  const char* qsrc = resid ? (const char*)(P.q + (long long)v.qrow * V + j0) : nullptr;
+  unsigned char* lbuf = race_smem;
+  float* qbuf = reinterpret_cast<float*>(race_smem + (size_t)kRaceSlice * esize);
 
-  // Thread 0: record task t in buffer b and start its copies (or, when its
-  // addresses do not allow bulk copies, complete the buffer's phase empty).
-  auto issue = [&](unsigned t, int b) {
-    RaceSlot& sl = slot[b];
-    sl.slice = (int)(t / n_race);
-    sl.task = P.race_list[t % n_race];
-    const int j0 = sl.slice * kRaceSlice;
-    const int n = min(kRaceSlice, V - j0);
-    const bool resid = (sl.task.mode == kRaceResidual);
-    const char* lsrc = (const char*)P.logits + ((long long)sl.task.row * V + j0) * esize;
-    const char* qsrc = resid ? (const char*)(P.q + (long long)sl.task.qrow * V + j0) : nullptr;
+  // Stage the slice with bulk copies when every address and size allows it.
+  if (threadIdx.x == 0) {
     const uint32_t lbytes = (uint32_t)n * esize, qbytes = resid ? (uint32_t)n * 4u : 0u;
     const bool ok = ((reinterpret_cast<uintptr_t>(lsrc) & 15) == 0) && (lbytes % 16 == 0) &&
                     (!resid || (((reinterpret_cast<uintptr_t>(qsrc) & 15) == 0) &&
                                 (qbytes % 16 == 0)));
-    sl.staged = ok ? 1 : 0;
+    s_staged = ok ? 1 : 0;
     if (ok) {
-      unsigned char* lbuf = race_smem + (size_t)b * bufsz;
-      // the buffer was last read through the generic proxy
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive_expect_tx(&bar[b], lbytes + qbytes);
-      bulk_load(lbuf, lsrc, lbytes, &bar[b]);
-      if (resid) bulk_load(lbuf + (size_t)kRaceSlice * esize, qsrc, qbytes, &bar[b]);
-    } else {
-      mbar_arrive(&bar[b]);
+      mbar_init(&bar, 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&bar, lbytes + qbytes);
+      bulk_load(lbuf, lsrc, lbytes, &bar);
+      if (resid) bulk_load(qbuf, qsrc, qbytes, &bar);
     }
-  };
-
-  if (threadIdx.x == 0) issue(blockIdx.x, 0);
-  uint32_t parity[2] = {0u, 0u};
-  int cur = 0;
-  for (unsigned t = blockIdx.x; t < tasks; t += gridDim.x, cur ^= 1) {
-    const unsigned tn = t + gridDim.x;
-    if (threadIdx.x == 0 && tn < tasks) issue(tn, cur ^ 1);
-    // Every thread waits for this task's copies (bounded); all agree.
-    if (!__syncthreads_and(mbar_wait(&bar[cur], parity[cur]) ? 1 : 0)) {
+  }
+  __syncthreads();
+  const bool staged = s_staged != 0;
+  if (staged) {
+    // Every thread waits for the copies (bounded); all agree on the outcome.
+    if (!__syncthreads_and(mbar_wait(&bar, 0) ? 1 : 0)) {
       if (threadIdx.x == 0) atomicOr(P.status, SPEC_STATUS_TIMEOUT);
-      // one more bounded wait for the copies in flight in both buffers
-      __syncthreads_and(mbar_wait(&bar[cur], parity[cur]) ? 1 : 0);
-      if (tn < tasks) __syncthreads_and(mbar_wait(&bar[cur ^ 1], parity[cur ^ 1]) ? 1 : 0);
+      // one more bounded wait for the copies in flight, then give up
+      __syncthreads_and(mbar_wait(&bar, 0) ? 1 : 0);
       return;
     }
-    parity[cur] ^= 1u;
-    const RaceSlot sl = slot[cur];
-    const RaceTask& task = sl.task;
-    const int r = task.r;
-    const RaceView v = race_view(P, r, task.row, task.qrow, task.kstar, task.mode, task.x,
-                                 task.m, task.c, task.inv_z, task.theta, task.z);
-    const uint32_t g0 = (uint32_t)sl.slice * (kRaceSlice / 4);
-    const uint32_t g1 = min(groups, g0 + (uint32_t)(kRaceSlice / 4));
-    const int j0 = (int)(g0 * 4u);
-    const int n = min(kRaceSlice, V - j0);
-    const bool resid = (v.mode == kRaceResidual);
-    const unsigned char* lbuf = race_smem + (size_t)cur * bufsz;
-    const float* qbuf = reinterpret_cast<const float*>(lbuf + (size_t)kRaceSlice * esize);
-    auto l_at = [&](int le) -> float {
-      return P.bf16 ? bf16_lo((uint32_t)*reinterpret_cast<const unsigned short*>(lbuf + (size_t)le * 2))
-                    : *reinterpret_cast<const float*>(lbuf + (size_t)le * 4);
-    };
+  }
 
-    // The best so far (seeded by the accept scan, raised by earlier slices).
-    const unsigned long long lb = __ldcg(P.race_best + r);
-    float best = lb ? __uint_as_float((uint32_t)(lb >> 32)) : 0.f;
-    int best_j = lb ? (int)(0xFFFFFFFFu - (uint32_t)lb) : kNoIndex;
-    const float start_best = best;
-    if (v.z > 0.f) {
-      if (sl.staged && best_j == kNoIndex) {
-        // No bound yet (the argmax token had weight 0 and no earlier slice
-        // has finished): score this slice's heaviest entry first.
-        float wb = 0.f;
-        int jb = kNoIndex;
-        for (int le = (int)threadIdx.x; le < n; le += (int)blockDim.x) {
-          const int j = j0 + le;
-          const float w = race_w(race_p(l_at(le), v), resid ? qbuf[le] : 0.f, j, v.mode, v.x);
-          if (w > wb) {
-            wb = w;
-            jb = j;
-          }
-        }
-        block_argmax(wb, jb);
-        if (jb != kNoIndex && wb > 0.f) {
-          const uint4 rw = race_words(P.seed, v.greq, v.kstar, (uint32_t)jb >> 2);
-          const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
-          best = race_score(wb, words[jb & 3]);
-          best_j = jb;
-        }
-      }
-      if (sl.staged) {
-        float lthr = race_logit_floor(v, best);
-        RaceItem* qw = queue + (threadIdx.x >> 5) * (32 * kRaceGroups);
-        const uint32_t stride = blockDim.x;
-        const uint32_t span = stride * kRaceGroups;
-        for (uint32_t gw = g0 + (threadIdx.x & ~31u); gw < g1; gw += span) {
-          const uint32_t gb = gw + (threadIdx.x & 31u);
-          float l[kRaceGroups][4], q[kRaceGroups][4];
-          uint32_t gk[kRaceGroups];
+  // The best so far (seeded by the accept scan, raised by earlier slices).
+  const unsigned long long lb = __ldcg(P.race_best + r);
+  float best = lb ? __uint_as_float((uint32_t)(lb >> 32)) : 0.f;
+  int best_j = lb ? (int)(0xFFFFFFFFu - (uint32_t)lb) : kNoIndex;
+  if (v.z > 0.f) {
+    if (staged && best_j == kNoIndex) {
+      // No bound yet (the argmax token had weight 0 and no earlier slice has
+      // finished): score this slice's heaviest entry first and start from it.
+      float wb = 0.f;
+      int jb = kNoIndex;
+      for (int le = (int)threadIdx.x * 4; le < n; le += (int)blockDim.x * 4) {
 #pragma unroll
-          for (int k = 0; k < kRaceGroups; ++k) {
-            gk[k] = gb + (uint32_t)k * stride;
-            const int le = (int)((gk[k] - g0) * 4u);  // entry within the slice
-            if (gk[k] < g1 && le + 3 < n) {
-              if (P.bf16) {
-                const uint2 bb = *reinterpret_cast<const uint2*>(lbuf + (size_t)le * 2);
-                l[k][0] = bf16_lo(bb.x);
-                l[k][1] = bf16_hi(bb.x);
-                l[k][2] = bf16_lo(bb.y);
-                l[k][3] = bf16_hi(bb.y);
-              } else {
-                const float4 f = *reinterpret_cast<const float4*>(lbuf + (size_t)le * 4);
-                l[k][0] = f.x; l[k][1] = f.y; l[k][2] = f.z; l[k][3] = f.w;
-              }
-              if (resid) {
-                const float4 f = *reinterpret_cast<const float4*>(qbuf + le);
-                q[k][0] = f.x; q[k][1] = f.y; q[k][2] = f.z; q[k][3] = f.w;
-              } else {
-                q[k][0] = q[k][1] = q[k][2] = q[k][3] = 0.f;
-              }
-            } else {
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const bool in = gk[k] < g1 && le + e < n;
-                l[k][e] = in ? l_at(le + e) : -INFINITY;
-                q[k][e] = (in && resid) ? qbuf[le + e] : 0.f;
-              }
+        for (int e = 0; e < 4; ++e) {
+          if (le + e < n) {
+            const float lv = P.bf16 ? bf16_lo((uint32_t)*reinterpret_cast<const unsigned short*>(
+                                          lbuf + (size_t)(le + e) * 2))
+                                    : *reinterpret_cast<const float*>(lbuf + (size_t)(le + e) * 4);
+            const float qv = resid ? qbuf[le + e] : 0.f;
+            const int j = j0 + le + e;
+            const float w = race_w(race_p(lv, v), qv, j, v.mode, v.x);
+            if (w > wb) {
+              wb = w;
+              jb = j;
             }
           }
-          race_batch(P, v, v.mode, gk, g1, l, q, best, best_j, lthr, qw);
         }
-      } else {
-        race_range_global(P, v, v.mode, g0, g1, best, best_j, queue);
+      }
+      block_argmax(wb, jb);
+      if (jb != kNoIndex && wb > 0.f) {
+        const uint4 rw = race_words(P.seed, v.greq, v.kstar, (uint32_t)jb >> 2);
+        const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
+        best = race_score(wb, words[jb & 3]);
+        best_j = jb;
       }
     }
-    block_argmax(best, best_j);
-    if (threadIdx.x == 0) {
-      if (best_j != kNoIndex && best > 0.f && best >= start_best)
-        atomicMax(P.race_best + r, race_pack(best, best_j));
-      __threadfence();
-      const unsigned prev = atomicAdd(P.race_counter + r, 1u);
-      s_last = (prev == (unsigned)P.race_slices - 1u);
-      if (s_last) {
-        __threadfence();
-        s_packed = atomicAdd(P.race_best + r, 0ull);
+    if (staged) {
+      float lthr = race_logit_floor(v, best);
+      RaceItem* qw = queue + (threadIdx.x >> 5) * (32 * kRaceGroups);
+      const uint32_t stride = blockDim.x;
+      const uint32_t span = stride * kRaceGroups;
+      for (uint32_t gw = g0 + (threadIdx.x & ~31u); gw < g1; gw += span) {
+        const uint32_t gb = gw + (threadIdx.x & 31u);
+        float l[kRaceGroups][4], q[kRaceGroups][4];
+        uint32_t gk[kRaceGroups];
+#pragma unroll
+        for (int k = 0; k < kRaceGroups; ++k) {
+          gk[k] = gb + (uint32_t)k * stride;
+          const int le = (int)((gk[k] - g0) * 4u);  // entry within the slice
+          const bool in = gk[k] < g1 && le + 3 < n;
+          if (in) {
+            if (P.bf16) {
+              const uint2 b = *reinterpret_cast<const uint2*>(lbuf + (size_t)le * 2);
+              l[k][0] = bf16_lo(b.x);
+              l[k][1] = bf16_hi(b.x);
+              l[k][2] = bf16_lo(b.y);
+              l[k][3] = bf16_hi(b.y);
+            } else {
+              const float4 f = *reinterpret_cast<const float4*>(lbuf + (size_t)le * 4);
+              l[k][0] = f.x; l[k][1] = f.y; l[k][2] = f.z; l[k][3] = f.w;
+            }
+            if (resid) {
+              const float4 f = *reinterpret_cast<const float4*>(qbuf + le);
+              q[k][0] = f.x; q[k][1] = f.y; q[k][2] = f.z; q[k][3] = f.w;
+            } else {
+              q[k][0] = q[k][1] = q[k][2] = q[k][3] = 0.f;
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const bool ine = gk[k] < g1 && le + e < n;
+              l[k][e] = ine ? (P.bf16 ? bf16_lo((uint32_t)*reinterpret_cast<const unsigned short*>(
+                                            lbuf + (size_t)(le + e) * 2))
+                                      : *reinterpret_cast<const float*>(lbuf + (size_t)(le + e) * 4))
+                            : -INFINITY;
+              q[k][e] = (ine && resid) ? qbuf[le + e] : 0.f;
+            }
+          }
+        }
+        race_batch(P, v, v.mode, gk, g1, l, q, best, best_j, lthr, qw);
       }
+    } else {
+      race_range_global(P, v, v.mode, g0, g1, best, best_j, queue);
     }
-    __syncthreads();
-    if (s_last) {
-      const unsigned long long packed = s_packed;
-      int tok;
-      if (packed == 0ull) {
-        // Every weight was 0 (rounding only): draw from p over the whole row.
-        float b2 = 0.f;
-        int j2 = kNoIndex;
-        if (v.z > 0.f) race_range_global(P, v, kRaceP, 0u, groups, b2, j2, queue);
-        block_argmax(b2, j2);
-        tok = (j2 == kNoIndex) ? 0 : j2;
-        if (threadIdx.x == 0) atomicOr(P.status, SPEC_STATUS_EMPTY_RESIDUAL);
-      } else {
-        tok = (int)(0xFFFFFFFFu - (uint32_t)(packed & 0xFFFFFFFFull));
-      }
-      if (threadIdx.x == 0) P.out_tokens[v.row] = tok;
-    }
-    __syncthreads();
   }
+  block_argmax(best, best_j);
+  if (threadIdx.x == 0) {
+    if (best_j != kNoIndex && best > 0.f) atomicMax(P.race_best + r, race_pack(best, best_j));
+    __threadfence();
+    const unsigned prev = atomicAdd(P.race_counter + r, 1u);
+    s_last = (prev == (unsigned)P.race_slices - 1u);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_packed = atomicAdd(P.race_best + r, 0ull);
+  }
+  __syncthreads();
+  const unsigned long long packed = s_packed;
+  int tok;
+  if (packed == 0ull) {
+    // Every weight was 0 (rounding only): draw from p over the whole row.
+    float b2 = 0.f;
+    int j2 = kNoIndex;
+    if (v.z > 0.f) race_range_global(P, v, kRaceP, 0u, groups, b2, j2, queue);
+    block_argmax(b2, j2);
+    tok = (j2 == kNoIndex) ? 0 : j2;
+    if (threadIdx.x == 0) atomicOr(P.status, SPEC_STATUS_EMPTY_RESIDUAL);
+  } else {
+    tok = (int)(0xFFFFFFFFu - (uint32_t)(packed & 0xFFFFFFFFull));
+  }
+  if (threadIdx.x == 0) P.out_tokens[v.row] = tok;
 }
 
 }  // namespace sv

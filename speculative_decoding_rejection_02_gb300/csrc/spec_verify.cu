@@ -34,7 +34,6 @@ struct spec_verify_handle {
   int n_phase;
   int tma_blocks;   // resident CTAs of k_rows_tma<.., false> on the device
   int filt_blocks;  // resident CTAs of k_rows_tma<true, true>
-  int race_blocks_bf16, race_blocks_f32;  // resident CTAs of k_race per dtype
 };
 
 namespace {
@@ -132,11 +131,8 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
                  stream>>>(P);
   if (timed) cudaEventRecord(h->phase[2], stream);
   if (!greedy) {
-    const long long want = (long long)b->B * P.race_slices;
-    const int cap = P.bf16 ? h->race_blocks_bf16 : h->race_blocks_f32;
-    const long long grid = want < cap ? want : cap;
-    sv::k_race<<<(unsigned)grid, sv::kRaceThreads, sv::race_smem_bytes(P.bf16 ? 2 : 4),
-                 stream>>>(P);
+    sv::k_race<<<(unsigned)((long long)b->B * P.race_slices), sv::kRaceThreads,
+                 sv::race_smem_bytes(P.bf16 ? 2 : 4), stream>>>(P);
   }
   if (timed) cudaEventRecord(h->phase[3], stream);
   if (cudaPeekAtLastError() != cudaSuccess) {
@@ -194,20 +190,11 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   }
   h->tma_blocks = per_sm * prop.multiProcessorCount;
   h->filt_blocks = filt_per_sm * prop.multiProcessorCount;
-  int rb16 = 0, rb32 = 0;
   if (cudaFuncSetAttribute(sv::k_race, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)sv::race_smem_bytes(4)) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&rb16, sv::k_race, sv::kRaceThreads,
-                                                    sv::race_smem_bytes(2)) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&rb32, sv::k_race, sv::kRaceThreads,
-                                                    sv::race_smem_bytes(4)) != cudaSuccess ||
-      rb16 < 1 || rb32 < 1) {
-    cudaGetLastError();
+                           (int)sv::race_smem_bytes(4)) != cudaSuccess) {
     delete h;
     return SPEC_ERR_CUDA;
   }
-  h->race_blocks_bf16 = rb16 * prop.multiProcessorCount;
-  h->race_blocks_f32 = rb32 * prop.multiProcessorCount;
   h->max_slices = (cfg->max_vocab + sv::kSliceF32 - 1) / sv::kSliceF32;
 
   const size_t n_rows = (size_t)cfg->max_rows, n_b = (size_t)cfg->max_batch;
@@ -334,7 +321,6 @@ struct NoallocDevice {
   int sm_count;
   int tma_blocks;
   int filt_blocks;
-  int race16, race32;  // resident k_race CTAs per SM (bf16 / fp32 logits)
 };
 NoallocDevice g_na_dev[kNaMaxDevices];
 std::mutex g_na_mutex;
@@ -391,13 +377,7 @@ extern "C" int spec_verify_run_noalloc(const spec_verify_batch* b, void* stream,
                                                         sv::kTmaSmemBytes) != cudaSuccess ||
           cudaOccupancyMaxActiveBlocksPerMultiprocessor(&filt_per_sm, sv::k_rows_tma<true, true>,
                                                         sv::kTmaThreads,
-                                                        sv::kTmaFiltSmemBytes) != cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&slot.race16, sv::k_race,
-                                                        sv::kRaceThreads,
-                                                        sv::race_smem_bytes(2)) != cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&slot.race32, sv::k_race,
-                                                        sv::kRaceThreads,
-                                                        sv::race_smem_bytes(4)) != cudaSuccess) {
+                                                        sv::kTmaFiltSmemBytes) != cudaSuccess) {
         cudaGetLastError();
         return SPEC_ERR_CUDA;
       }
@@ -430,8 +410,6 @@ extern "C" int spec_verify_run_noalloc(const spec_verify_batch* b, void* stream,
   h.n_phase = 0;
   h.tma_blocks = nd.tma_blocks;
   h.filt_blocks = nd.filt_blocks;
-  h.race_blocks_bf16 = (nd.race16 > 0 ? nd.race16 : 1) * nd.sm_count;
-  h.race_blocks_f32 = (nd.race32 > 0 ? nd.race32 : 1) * nd.sm_count;
   // The slice counters must start at zero: clear them (the array keeps the
   // previous call's contents).
   cudaStream_t s = (cudaStream_t)stream;
