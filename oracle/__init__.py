@@ -34,6 +34,7 @@ ST_BAD_TOKEN = 4
 ST_EMPTY_RESIDUAL = 8
 
 FLAG_NAIVE = 1
+FLAG_SAMPLER_MATCH = 2
 
 
 def build(force: bool = False) -> str:
@@ -67,7 +68,7 @@ class _Outputs(C.Structure):
         ("out_tokens", C.c_void_p), ("num_accepted", C.c_void_p),
         ("p_at_draft", C.c_void_p), ("accept_margin", C.c_void_p),
         ("topp_margin", C.c_void_p), ("race_margin", C.c_void_p),
-        ("req_status", C.c_void_p),
+        ("req_status", C.c_void_p), ("row_race_margin", C.c_void_p),
     ]
 
 
@@ -225,6 +226,7 @@ def verify(batch, requests=None):
         "topp_margin": np.full(R, np.nan),
         "race_margin": np.full(B, np.nan),
         "req_status": np.zeros(B, np.uint32),
+        "row_race_margin": np.full(R, np.nan),
     }
     o = _Outputs(**{k: _ptr(v) for k, v in out.items()})
     if requests is None:

@@ -19,7 +19,8 @@
 //              exponential race, sampling constraints before the judgement),
 //              "기본값 greedy 드래프트에서도 분포가 지켜질까" (one-hot draft,
 //              temperature 0 argmax match)
-//  [mlxcel]    "투기적 디코딩", section 기본 라운드 (1..K+1 tokens per round)
+//  [mlxcel]    "투기적 디코딩", section 기본 라운드 (1..K+1 tokens per round),
+//              section "mlxcel의 프롬프트 조회" (sampler-match acceptance)
 //
 // Readings where the pages leave a step open are stated at the function
 // that takes them.
@@ -330,6 +331,7 @@ typedef struct {
   uint64_t seed;
   int64_t request_base;         // global index of request 0 (RNG key)
   unsigned flags;               // bit 0: naive resample-from-p control
+                                // bit 1: sampler-match acceptance
 } or_batch;
 
 // Per-call outputs and the decision log used to excuse near-tie decisions.
@@ -342,6 +344,8 @@ typedef struct {
   double* race_margin;      // [B]
   unsigned* req_status;     // [B] bit 0 non-finite, bit 1 no finite logit,
                             //     bit 2 bad token id, bit 3 empty residual
+  double* row_race_margin;  // [N+B] margin of the race drawn on each target
+                            //       row (+inf where no race was drawn)
 } or_outputs;
 
 static void or_verify_one(const or_batch* b, int r, const or_outputs* o) {
@@ -361,6 +365,7 @@ static void or_verify_one(const or_batch* b, int r, const or_outputs* o) {
   for (int s = 0; s <= gamma; ++s) {
     o->out_tokens[row0 + s] = -1;
     o->topp_margin[row0 + s] = inf;
+    o->row_race_margin[row0 + s] = inf;
   }
   for (int i = 0; i < gamma; ++i) o->accept_margin[c0 + i] = inf;
   o->race_margin[r] = inf;
@@ -396,6 +401,35 @@ static void or_verify_one(const or_batch* b, int r, const or_outputs* o) {
     }
     o->topp_margin[row0 + i] = info.topp_margin;
     if (i < gamma) o->p_at_draft[c0 + i] = valid(draft(i)) ? p[draft(i)] : 0.0;
+  }
+
+  // Sampler-match acceptance ([mlxcel] "투기적 디코딩", section "mlxcel의
+  // 프롬프트 조회"): at every position the target's own sampler draws a fresh
+  // token y_i from p_i; the draft is accepted iff it equals y_i, and the first
+  // mismatch (or the end of the block) emits y_i. Readings: the draw is the
+  // same exponential race over w = p_i, keyed by position i (so y_gamma is
+  // exactly the bonus draw of the rejection rule); draft_probs is not read
+  // (the rule never looks at q); temperature-0 requests keep the argmax
+  // match, which is the same rule with the argmax as the sampler.
+  if ((b->flags & 2u) && T > 0.0) {
+    int k_match = gamma;
+    for (int i = 0; i <= gamma; ++i) {
+      load_row(i);
+      or_row_info info;
+      or_target_probs(l.data(), V, T, tk, tp, p.data(), &info);
+      double margin;
+      const int y = or_race(p.data(), V, b->seed, greq, i, &margin);
+      o->row_race_margin[row0 + i] = margin;
+      o->out_tokens[row0 + i] = y;
+      if (i == gamma || draft(i) != y) {
+        k_match = i;
+        o->race_margin[r] = margin;
+        break;
+      }
+    }
+    o->num_accepted[r] = k_match;
+    o->req_status[r] = status;
+    return;
   }
 
   // Step 2: left-to-right accept scan; stop at the first rejection.
@@ -455,6 +489,7 @@ static void or_verify_one(const or_batch* b, int r, const or_outputs* o) {
       out_token = or_race(p.data(), V, b->seed, greq, k_star, &margin);
     }
     o->race_margin[r] = margin;
+    o->row_race_margin[row0 + k_star] = margin;
   }
 
   for (int i = 0; i < k_star; ++i) o->out_tokens[row0 + i] = draft(i);
