@@ -56,6 +56,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--config", default="c5", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--accept", default="rejection", choices=["rejection", "sampler-match"],
+                    help="acceptance rule: the rejection rule, or sampler-match (the "
+                         "target's sampler draws every position; drafts must equal it)")
     ap.add_argument("--B", type=int, default=None,
                     help="resize the workload to B requests (profiling of small cases)")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -101,7 +104,7 @@ def algorithmic_bytes(batch, num_accepted) -> dict:
     rows = R * V * esize
     q_rows = 0
     judged_q = 0
-    if batch["draft_probs"] is not None:
+    if batch["draft_probs"] is not None and not (int(batch.get("flags", 0)) & 2):
         hot = (T > 0)
         rejected = hot & (num_accepted < gam)
         q_rows = int(rejected.sum()) * V * 4
@@ -291,6 +294,8 @@ def main():
     batch = synth.make(args.config, B=args.B)
     B, V = batch["B"], batch["V"]
     batch["request_base"] = rank_request_base(rank, B)
+    if args.accept == "sampler-match":
+        batch["flags"] = sv.FLAG_SAMPLER_MATCH
     cu = batch["cu_num_draft"]
     N = int(cu[-1])
     R = N + B
@@ -393,8 +398,13 @@ def main():
         cpu = {"value": rate, "unit": "draft_positions/s", "cores": 1, "kind": "oracle",
                "sample": desc, "seconds": round(secs, 2)}
 
-    launches_per_step = 3 + (1 if (batch.get("top_k") is not None or
-                                   batch.get("top_p") is not None) else 0)
+    # row pass, accept scan, race; with top-k / top-p the filtered-row kernel,
+    # and for bf16 rows that are 16-byte aligned the histogram row pass too
+    filters = batch.get("top_k") is not None or batch.get("top_p") is not None
+    aligned_bf16 = batch["logits_dtype"] == "bf16" and (V * 2) % 16 == 0
+    launches_per_step = 3 + ((2 if aligned_bf16 else 1) if filters else 0)
+    if args.accept == "sampler-match":
+        launches_per_step += 1  # k_match
     if rank == 0:
         line = {
             "metric": "verified draft positions/sec and achieved HBM GB/s (fraction of GB300 peak)",
@@ -406,6 +416,7 @@ def main():
                        "logits_dtype": batch["logits_dtype"], "input_bytes": int(in_bytes),
                        "l2": ("inputs larger than L2" if flush is None
                               else "L2 flushed between timed calls (512 MB write)"),
+                       "acceptance": args.accept,
                        "parallelism": f"replicas x{world}"},
             "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak,
             "algorithmic_bytes_per_step": bytes_,

@@ -80,6 +80,15 @@ extern "C" {
 #define SPEC_FLAG_NAIVE 0x1u /* negative control: resample rejected positions
                                 from p instead of the residual (biased; for
                                 tests of the statistics only) */
+/* Sampler-match acceptance (mlxcel, "투기적 디코딩", section "mlxcel의 프롬프트
+ * 조회"): for every temperature > 0 request the target's sampler draws a
+ * fresh token y_i from p_i at each position i = 0 .. gamma (the exponential
+ * race over w = p_i, keyed by position i); x_i is accepted iff x_i == y_i and
+ * the first mismatch, or the end of the block, emits y_i. draft_probs is not
+ * read. Lossless for any draft; for one-hot drafts it accepts x with
+ * probability p(x), as the rejection rule does. Temperature-0 requests keep
+ * the argmax match. Cannot be combined with SPEC_FLAG_NAIVE. */
+#define SPEC_FLAG_SAMPLER_MATCH 0x2u
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 
@@ -139,6 +148,8 @@ int spec_verify_init(spec_verify_handle** h, const spec_verify_config* cfg);
  * requests take the argmax-match path, the others the probabilistic one.
  *   h [in] handle; b [in] host pointer to the batch description (device
  *   arrays inside); stream [in] a cudaStream_t (NULL = legacy default stream).
+ * b->flags may hold SPEC_FLAG_NAIVE or SPEC_FLAG_SAMPLER_MATCH, not both;
+ * anything else is SPEC_ERR_INVALID_ARG.
  * Returns SPEC_OK, SPEC_ERR_NOT_INIT, SPEC_ERR_INVALID_ARG, SPEC_ERR_CAPACITY
  * or SPEC_ERR_CUDA (launch failure). Asynchronous.
  */

@@ -29,6 +29,7 @@ STATUS_BAD_OFFSETS = 0x10
 STATUS_TIMEOUT = 0x20
 
 FLAG_NAIVE = 0x1
+FLAG_SAMPLER_MATCH = 0x2
 
 # The entry points declared in include/spec_verify.h.
 ENTRY_POINTS = (

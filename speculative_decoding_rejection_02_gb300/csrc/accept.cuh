@@ -20,6 +20,65 @@ namespace sv {
 
 constexpr int kAcceptWarps = 8;  // requests per CTA
 
+// Sampler-match acceptance (mlxcel "투기적 디코딩", section "mlxcel의 프롬프트
+// 조회"): the target's sampler draws y_i from p_i at every position
+// i = 0 .. gamma and x_i is accepted iff it equals y_i. Each row of the
+// request becomes one race over w = p_i keyed by position i (so y_gamma is the
+// bonus draw of the rejection rule); the race writes y_i to the row's output
+// slot and k_match finds the first mismatch. draft_probs is not read. Called
+// by the whole warp for a usable temperature > 0 request.
+__device__ __forceinline__ void enqueue_match_races(const Params& P, int r, int c0, int gamma,
+                                                    long long row0, unsigned st) {
+  const int lane = threadIdx.x & 31;
+  unsigned bad_tok = 0;
+  for (int base = 0; base <= gamma; base += 32) {
+    const int i = base + lane;
+    const bool on = i <= gamma;
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, on);
+    unsigned at = 0;
+    if (lane == 0) at = atomicAdd(P.race_count, (unsigned)__popc(m));
+    at = __shfl_sync(0xFFFFFFFFu, at, 0);
+    if (on) {
+      const long long row = row0 + i;
+      const RowStats s = P.rows[row];
+      if (i < gamma) {
+        const int x = __ldg(P.ids + c0 + i);
+        bad_tok |= (x >= 0 && x < P.V) ? 0u : 1u;
+        if (P.p_at_draft) P.p_at_draft[c0 + i] = s.p_x;
+      }
+      RaceTask task;
+      task.r = r;
+      task.row = (int)row;
+      task.qrow = c0 + i;
+      task.kstar = i;
+      task.mode = kRaceP;
+      task.x = -1;
+      task.m = s.m;
+      task.c = s.c;
+      task.inv_z = s.inv_z;
+      task.theta = s.theta;
+      task.z = s.z;
+      task.slot = (int)row;
+      const RaceView v = race_view(P, r, task.row, task.qrow, i, kRaceP, -1, s.m, s.c,
+                                   s.inv_z, s.theta, s.z);
+      P.race_best[row] = race_candidate(P, v, s.argmax);
+      P.race_counter[row] = 0u;
+      P.race_list[at + (unsigned)__popc(m & ((1u << lane) - 1u))] = task;
+    }
+  }
+  if (__reduce_or_sync(0xFFFFFFFFu, bad_tok)) st |= SPEC_STATUS_BAD_TOKEN;
+  if (lane == 0) {
+    RaceDesc d;
+    d.mode = kRaceMatch;
+    d.kstar = 0;
+    d.x = -1;
+    d.row = (int)row0;
+    d.qrow = c0;
+    P.race[r] = d;
+    if (st & SPEC_STATUS_BAD_TOKEN) atomicOr(P.status, SPEC_STATUS_BAD_TOKEN);
+  }
+}
+
 __global__ void __launch_bounds__(kAcceptWarps * 32)
 k_accept(Params P) {
   const int lane = threadIdx.x & 31;
@@ -60,6 +119,11 @@ k_accept(Params P) {
       P.num_accepted[r] = 0;
       P.race[r] = d;
     }
+    return;
+  }
+
+  if (!greedy && (P.flags & SPEC_FLAG_SAMPLER_MATCH)) {
+    enqueue_match_races(P, r, c0, gamma, row0, st);
     return;
   }
 
@@ -132,14 +196,46 @@ k_accept(Params P) {
       task.inv_z = s.inv_z;
       task.theta = s.theta;
       task.z = s.z;
-      task.pad = 0;
+      task.slot = r;
       P.race_list[atomicAdd(P.race_count, 1u)] = task;
     }
     P.race[r] = d;
-    P.race_best[r] = seed_best;
-    P.race_counter[r] = 0u;
+    if (!greedy) {
+      // Only requests with a race own slot r (under sampler-match the slots
+      // are rows, and greedy requests must not touch them).
+      P.race_best[r] = seed_best;
+      P.race_counter[r] = 0u;
+    }
     if (st & SPEC_STATUS_BAD_TOKEN) atomicOr(P.status, SPEC_STATUS_BAD_TOKEN);
   }
+}
+
+// After the races of a sampler-match batch: one warp per request finds the
+// first position whose drawn token differs from the draft (the drawn tokens
+// already sit in the output slots), pads the slots after it with -1 and
+// writes num_accepted. Other requests were finished by k_accept.
+__global__ void __launch_bounds__(kAcceptWarps * 32)
+k_match(Params P) {
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * kAcceptWarps + (threadIdx.x >> 5);
+  if (r >= P.B) return;
+  const RaceDesc d = P.race[r];
+  if (d.mode != kRaceMatch) return;
+  const int c0 = d.qrow;
+  const int gamma = __ldg(P.cu + r + 1) - c0;
+  const long long row0 = d.row;
+  int k = gamma;
+  for (int base = 0; base < gamma; base += 32) {
+    const int i = base + lane;
+    const bool ok = (i >= gamma) || (P.out_tokens[row0 + i] == __ldg(P.ids + c0 + i));
+    const unsigned rej = __ballot_sync(0xFFFFFFFFu, !ok);
+    if (rej) {
+      k = base + __ffs(rej) - 1;
+      break;
+    }
+  }
+  for (int i = k + 1 + lane; i <= gamma; i += 32) P.out_tokens[row0 + i] = -1;
+  if (lane == 0) P.num_accepted[r] = k;
 }
 
 }  // namespace sv

@@ -25,6 +25,7 @@ enum RaceMode : int {
   kRaceResidual = 1,  // w = max(p - q, 0) with q the draft_probs row
   kRaceMasked = 2,    // one-hot draft: w = p with the draft token masked
   kRaceP = 3,         // bonus token or naive control: w = p
+  kRaceMatch = 4,     // sampler-match request: a race on every row, then k_match
 };
 
 // Per target row: what the accept scan and the race need.
@@ -62,11 +63,12 @@ struct RaceTask {
   int r;        // request
   int row;      // target row of k* (= output slot)
   int qrow;     // draft_probs row of k*
-  int kstar;    // position k*
+  int kstar;    // position k* (the race's Philox position)
   int mode;     // RaceMode
   int x;        // draft token at k*
   float m, c, inv_z, theta, z;  // RowStats of the row
-  int pad;
+  int slot;     // index into race_best / race_counter (request, or row for
+                // sampler-match)
 };
 
 // Device view of one call.
@@ -93,9 +95,9 @@ struct Params {
   SlicePartial* partials;
   unsigned* row_counter;
   RaceDesc* race;
-  unsigned long long* race_best;
-  unsigned* race_counter;
-  RaceTask* race_list;   // requests with a token to draw (order not fixed)
+  unsigned long long* race_best;  // per race slot: packed (score, ~index)
+  unsigned* race_counter;         // per race slot: finished slices
+  RaceTask* race_list;   // races to draw (order not fixed)
   unsigned* race_count;  // entries in race_list
   unsigned* status;
   int slices_per_row;

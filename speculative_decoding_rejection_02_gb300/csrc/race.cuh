@@ -6,9 +6,12 @@
 // with the draft token masked; "드래프트가 제안하고 타깃이 판정한다": the bonus
 // token comes from p of the last row).
 //
-// One CTA per task (request, 8192-entry slice), numbered slice-major so that
-// later slices of a request start from the best score its earlier slices
+// One CTA per task (race, 8192-entry slice), numbered slice-major so that
+// later slices of a race start from the best score its earlier slices
 // published (and from the argmax token's score seeded by the accept scan).
+// A race is one request's k* row, or, under sampler-match acceptance, every
+// row of a request (mlxcel "투기적 디코딩", section "mlxcel의 프롬프트 조회":
+// the target's sampler draws a token at each position).
 // The CTA pulls its slice of logits and draft probabilities into shared
 // memory with two bulk copies, then scores it. Four consecutive entries share
 // one Philox4x32-10 draw; E = -ln U, score = w / E, the lowest index wins
@@ -21,7 +24,7 @@
 // lanes; after the draw, -ln U >= 1 - U bounds every score by w / (1 - U),
 // so the logarithm and the division run only for entries that can still
 // win. Slice winners meet in one 64-bit atomicMax of (score bits, ~index);
-// the last task of a request writes the token.
+// the last task of a race writes the token to the race row's output slot.
 #pragma once
 #include "common.cuh"
 #include "philox.cuh"
@@ -228,6 +231,7 @@ k_race(Params P) {
   const int slice = (int)(t / n_race);
   const RaceTask task = P.race_list[t % n_race];
   const int r = task.r;
+  const int slot = task.slot;
   const RaceView v = race_view(P, r, task.row, task.qrow, task.kstar, task.mode, task.x, task.m,
                                task.c, task.inv_z, task.theta, task.z);
   const int V = P.V;
@@ -271,7 +275,7 @@ k_race(Params P) {
   }
 
   // The best so far (seeded by the accept scan, raised by earlier slices).
-  const unsigned long long lb = __ldcg(P.race_best + r);
+  const unsigned long long lb = __ldcg(P.race_best + slot);
   float best = lb ? __uint_as_float((uint32_t)(lb >> 32)) : 0.f;
   int best_j = lb ? (int)(0xFFFFFFFFu - (uint32_t)lb) : kNoIndex;
   if (v.z > 0.f) {
@@ -356,16 +360,16 @@ k_race(Params P) {
   }
   block_argmax(best, best_j);
   if (threadIdx.x == 0) {
-    if (best_j != kNoIndex && best > 0.f) atomicMax(P.race_best + r, race_pack(best, best_j));
+    if (best_j != kNoIndex && best > 0.f) atomicMax(P.race_best + slot, race_pack(best, best_j));
     __threadfence();
-    const unsigned prev = atomicAdd(P.race_counter + r, 1u);
+    const unsigned prev = atomicAdd(P.race_counter + slot, 1u);
     s_last = (prev == (unsigned)P.race_slices - 1u);
   }
   __syncthreads();
   if (!s_last) return;
   if (threadIdx.x == 0) {
     __threadfence();
-    s_packed = atomicAdd(P.race_best + r, 0ull);
+    s_packed = atomicAdd(P.race_best + slot, 0ull);
   }
   __syncthreads();
   const unsigned long long packed = s_packed;

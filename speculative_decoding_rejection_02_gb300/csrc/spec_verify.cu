@@ -49,6 +49,9 @@ int check_batch(const spec_verify_config* cfg, const spec_verify_batch* b, bool 
     return SPEC_ERR_INVALID_ARG;
   if (b->N > 0 && !b->draft_token_ids) return SPEC_ERR_INVALID_ARG;
   if (!greedy && !b->temperature) return SPEC_ERR_INVALID_ARG;
+  if (!greedy && ((b->flags & ~(SPEC_FLAG_NAIVE | SPEC_FLAG_SAMPLER_MATCH)) ||
+                  ((b->flags & SPEC_FLAG_NAIVE) && (b->flags & SPEC_FLAG_SAMPLER_MATCH))))
+    return SPEC_ERR_INVALID_ARG;
   if (b->B > cfg->max_batch || b->V > cfg->max_vocab ||
       (long long)b->N + b->B > cfg->max_rows)
     return SPEC_ERR_CAPACITY;
@@ -96,7 +99,10 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   P.race_slices = (b->V + sv::kRaceSlice - 1) / sv::kRaceSlice;
 
   const long long R = (long long)b->N + b->B;
-  if (R * P.slices_per_row > 0x7FFFFFFFll || (long long)b->B * P.race_slices > 0x7FFFFFFFll)
+  const bool match = !greedy && (P.flags & SPEC_FLAG_SAMPLER_MATCH);
+  // Races: one per request (its k* row), or one per row under sampler-match.
+  const long long races = match ? R : (long long)b->B;
+  if (R * P.slices_per_row > 0x7FFFFFFFll || races * P.race_slices > 0x7FFFFFFFll)
     return SPEC_ERR_CAPACITY;
   const bool timed = h->n_phase >= 4;
   if (timed) cudaEventRecord(h->phase[0], stream);
@@ -131,8 +137,11 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
                  stream>>>(P);
   if (timed) cudaEventRecord(h->phase[2], stream);
   if (!greedy) {
-    sv::k_race<<<(unsigned)((long long)b->B * P.race_slices), sv::kRaceThreads,
+    sv::k_race<<<(unsigned)(races * P.race_slices), sv::kRaceThreads,
                  sv::race_smem_bytes(P.bf16 ? 2 : 4), stream>>>(P);
+    if (match)
+      sv::k_match<<<(b->B + sv::kAcceptWarps - 1) / sv::kAcceptWarps, sv::kAcceptWarps * 32, 0,
+                    stream>>>(P);
   }
   if (timed) cudaEventRecord(h->phase[3], stream);
   if (cudaPeekAtLastError() != cudaSuccess) {
@@ -201,10 +210,11 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   const size_t sz_rows = align_up(n_rows * sizeof(sv::RowStats));
   const size_t sz_part = align_up(n_rows * h->max_slices * sizeof(sv::SlicePartial));
   const size_t sz_rcnt = align_up(n_rows * sizeof(unsigned));
+  // Race slots and tasks: one per row covers sampler-match batches.
   const size_t sz_race = align_up(n_b * sizeof(sv::RaceDesc));
-  const size_t sz_best = align_up(n_b * sizeof(unsigned long long));
-  const size_t sz_rccnt = align_up(n_b * sizeof(unsigned));
-  const size_t sz_list = align_up(n_b * sizeof(sv::RaceTask));
+  const size_t sz_best = align_up(n_rows * sizeof(unsigned long long));
+  const size_t sz_rccnt = align_up(n_rows * sizeof(unsigned));
+  const size_t sz_list = align_up(n_rows * sizeof(sv::RaceTask));
   const size_t sz_lcnt = align_up(sizeof(unsigned));
   const size_t sz_stat = align_up(sizeof(unsigned));
   const size_t total = sz_rows + sz_part + sz_rcnt + sz_race + sz_best + sz_rccnt + sz_list +
@@ -307,9 +317,9 @@ constexpr size_t kNaOffPart = kNaOffRows + na_align(kNaRows * sizeof(sv::RowStat
 constexpr size_t kNaOffRcnt = kNaOffPart + na_align(kNaRows * kNaSlices * sizeof(sv::SlicePartial));
 constexpr size_t kNaOffRace = kNaOffRcnt + na_align(kNaRows * sizeof(unsigned));
 constexpr size_t kNaOffBest = kNaOffRace + na_align(kNaBatch * sizeof(sv::RaceDesc));
-constexpr size_t kNaOffRccnt = kNaOffBest + na_align(kNaBatch * sizeof(unsigned long long));
-constexpr size_t kNaOffList = kNaOffRccnt + na_align(kNaBatch * sizeof(unsigned));
-constexpr size_t kNaOffLcnt = kNaOffList + na_align(kNaBatch * sizeof(sv::RaceTask));
+constexpr size_t kNaOffRccnt = kNaOffBest + na_align(kNaRows * sizeof(unsigned long long));
+constexpr size_t kNaOffList = kNaOffRccnt + na_align(kNaRows * sizeof(unsigned));
+constexpr size_t kNaOffLcnt = kNaOffList + na_align(kNaRows * sizeof(sv::RaceTask));
 constexpr size_t kNaOffStat = kNaOffLcnt + na_align(sizeof(unsigned));
 constexpr size_t kNaBytes = kNaOffStat + na_align(sizeof(unsigned));
 static_assert(kNaBytes <= SPEC_NOALLOC_SCRATCH_BYTES, "no-allocation scratch too small");

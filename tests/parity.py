@@ -4,7 +4,8 @@
 * accepted counts and tokens: identical, except where the oracle's first
   differing decision has a relative margin below 1e-5 (|p/q - u| / u for an
   accept test, (s1 - s2) / s1 for a race, |mass above - top_p| / top_p for a
-  top-p boundary); such excused decisions are counted.
+  top-p boundary); such excused decisions are counted. Under sampler-match
+  acceptance the decision at a position is the race drawn on its row.
 * p at the draft tokens: relative 1e-5 for fp32 logits, 2e-3 for bf16 (rows
   whose top-p boundary margin is below 1e-5 are skipped).
 """
@@ -38,6 +39,7 @@ def compare(batch, gpu, ref, requests=None, check_p=True):
     reqs = range(B) if requests is None else requests
     bf16 = batch["logits_dtype"] == "bf16"
     rtol = 2e-3 if bf16 else 1e-5
+    sampler_match = bool(int(batch.get("flags", 0)) & 2)
     rep = dict(requests=0, decisions=0, excused=0, unexcused=[], p_checked=0, p_bad=[],
                p_max_rel=0.0)
     for r in reqs:
@@ -58,10 +60,14 @@ def compare(batch, gpu, ref, requests=None, check_p=True):
             else:
                 d = int(np.nonzero(to != tg)[0][0])
             margins = [ref["topp_margin"][row0 + d]]
-            if d < g:
-                margins.append(ref["accept_margin"][c0 + d])
-            if d == ko:
-                margins.append(ref["race_margin"][r])
+            if sampler_match:
+                # the decision at position d is the race drawn on row d
+                margins.append(ref["row_race_margin"][row0 + d])
+            else:
+                if d < g:
+                    margins.append(ref["accept_margin"][c0 + d])
+                if d == ko:
+                    margins.append(ref["race_margin"][r])
             if temps[r] > 0 and np.nanmin(margins) < MARGIN:
                 rep["excused"] += 1
             else:

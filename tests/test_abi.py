@@ -67,6 +67,16 @@ def test_check_batch(L):
     assert sv.check_batch(cfg, _batch(N=0, draft_token_ids=None)) == 0
 
 
+def test_check_batch_flags(L):
+    cfg = _cfg()
+    assert sv.check_batch(cfg, _batch(flags=sv.FLAG_NAIVE)) == 0
+    assert sv.check_batch(cfg, _batch(flags=sv.FLAG_SAMPLER_MATCH)) == 0
+    # the two rules exclude each other; unknown bits are refused
+    assert sv.check_batch(cfg, _batch(flags=sv.FLAG_NAIVE | sv.FLAG_SAMPLER_MATCH)) == -1
+    assert sv.check_batch(cfg, _batch(flags=0x4)) == -1
+    assert sv.check_batch(cfg, _batch(flags=0x80000000)) == -1
+
+
 def test_strerror(L):
     for code in (0, -1, -2, -3, -4, -5, -6, 99):
         assert isinstance(sv.strerror(code), str) and sv.strerror(code)
