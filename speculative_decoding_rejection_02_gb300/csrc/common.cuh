@@ -100,6 +100,8 @@ struct Params {
   RaceTask* race_list;   // races to draw (order not fixed)
   unsigned* race_count;  // entries in race_list
   unsigned* status;
+  long long* pending_rows;  // filtered rows left to the exact slow kernel
+  unsigned* pending_count;  // entries in pending_rows (race_count + 1)
   int slices_per_row;
   int race_slices;
 };

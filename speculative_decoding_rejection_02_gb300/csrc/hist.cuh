@@ -1,18 +1,32 @@
-// Exact top-k / top-p on bf16 rows from a count histogram over bf16 values.
+// Exact top-k / top-p on bf16 rows from a window histogram of values.
 //
 // A bf16 logit takes one of 65536 values, so the tempered, filtered
 // distribution of a row (velog "vLLM 커널은 이 규칙을 어떻게 옮겼나":
 // temperature, top-k and top-p applied before the judgement) is fixed by how
-// many tokens hold each value. While a row streams through the SM, every
-// element adds 1 to the 16-bit counter indexed by its raw bits (one
-// shared-memory atomic, two counters per 32-bit word: 128 KB for all values).
-// At the row's end the consumers merge -0 into +0, turn counts into masses
-// n 2^(v c - m c), scan the values from the largest down and read off the
-// top-k and top-p thresholds, Z over the kept set and the kept set itself:
-// no sort, no per-element exp, one read of the row, exact for every value.
-// A counter can wrap only if more than 65535 tokens of one row share a
-// value; the total count then differs from V and the row is left to the
-// exact bisection kernel, as are rows with NaN or +inf.
+// many tokens hold each value. Only values near the row maximum m can decide
+// the thresholds. For top-p, the tokens below m - D with
+//   D = (log2(V / (1 - top_p)) + 1) / c,   c = log2(e) / T,
+// weigh less than (1 - top_p) / 2 in units of the maximum's weight, and
+// Z >= 1 in those units, so the mass at or above m - D exceeds top_p Z and
+// the top-p boundary lies inside the window [m - D, m]. For top-k the window
+// is 30 / c wide (weights down to 2^-30 of the maximum's).
+//
+// While the row streams, each thread drops an element unless it lies at or
+// above (its own running max) - D; every running max is at most m, so every
+// element at or above m - D is counted. A counted element adds 1 to the
+// counter of its value: one 32-bit counter per bf16 value of magnitude in
+// [2^-16, 2^8) (24 binades x 128 values per sign, 24 KB), plus one merged
+// counter per sign for the magnitudes below 2^-16, which also sums the
+// weights 2^(l c) of its members. A counted value of magnitude 2^8 or more
+// (or +inf) sends the row to the exact slow path.
+//
+// At the row's end the consumers turn counts into masses n 2^(v c - m c),
+// scan the values from the largest down and read off the top-k and top-p
+// thresholds, Z over the kept set and the kept set itself: exact for every
+// value, one read of the row, no sort, no per-element exp beyond the row
+// sum. The row goes to the slow path when a threshold falls on a merged
+// counter or outside the window (top-k with fewer than k tokens in it), or
+// when the row holds NaN or +inf.
 #pragma once
 #include "common.cuh"
 #include "pipe.cuh"
@@ -20,17 +34,97 @@
 namespace sv {
 
 constexpr unsigned kPendingSlow = 0x80000000u;  // row left to the exact slow path
-constexpr size_t kHist16Bytes = 65536 * 2;      // 16-bit counters for every bf16 value
 
-// Order-preserving 16-bit key of a bf16 value and back.
-__device__ __forceinline__ uint32_t bf16_key(uint32_t b) {
-  return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+constexpr int kWinELo = 111;                 // biased exponent of 2^-16
+constexpr int kWinBinades = 24;              // magnitudes 2^-16 .. 2^8
+constexpr int kWinHalf = kWinBinades * 128;  // single-value counters per sign
+constexpr int kWinFine = 2 * kWinHalf;       // 6144
+// Items in increasing value order: negative values (most negative first),
+// the merged negative and positive counters, positive values.
+constexpr int kWinItems = kWinFine + 2;
+constexpr int kWinTinyNeg = kWinHalf;
+constexpr int kWinTinyPos = kWinHalf + 1;
+constexpr float kWinTopKWidth = 30.f;  // top-k window, in units of 1 / c
+constexpr float kWinTinyNegLow = -1.52587890625e-05f;  // -2^-16
+
+struct WinHist {
+  unsigned cnt[kWinItems];  // counter of fine item i at cnt[i] (the two merged
+                            // items keep theirs below)
+  unsigned tiny_cnt[2];     // merged counters: [0] negative, [1] positive
+  float tiny_w[2];          // their sums of 2^(l c)
+  unsigned out_of_range;    // set when a counted value has magnitude >= 2^8
+  unsigned pad[1];
+};
+static_assert(sizeof(WinHist) % 16 == 0, "cleared with 16-byte stores");
+
+// Window half-width D (logit units) of a filtered row; c > 0.
+__device__ __forceinline__ float win_delta(float c, int tk, float tp, int V) {
+  float d = 0.f;
+  if (tp < 1.f) d = (log2f((float)V / (1.f - tp)) + 1.f) / c;
+  if (tk > 0 && tk < V) d = fmaxf(d, kWinTopKWidth / c);
+  return d;
 }
-__device__ __forceinline__ uint32_t key_bf16(uint32_t k) {
-  return (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+
+// Item (and counter) index of a bf16 value of magnitude in [2^-16, 2^8);
+// `fine` tells whether the magnitude is in that range.
+__device__ __forceinline__ int win_slot(uint32_t bits, bool& fine) {
+  const int idx = (int)(bits & 0x7FFFu) - kWinELo * 128;
+  fine = (unsigned)idx < (unsigned)kWinHalf;
+  return (bits & 0x8000u) ? (kWinHalf - 1 - idx) : (kWinHalf + 2 + idx);
 }
-__device__ __forceinline__ unsigned hist16_count(const uint32_t* h, uint32_t bits) {
-  return (h[bits >> 1] >> ((bits & 1u) << 4)) & 0xFFFFu;
+
+// Count an element outside the single-value range (merged counter, or the
+// out-of-range flag for magnitudes >= 2^8 and +inf).
+__device__ __forceinline__ void win_add_rare(WinHist* h, uint32_t bits, float l, float c) {
+  const int e = (int)((bits & 0x7FFFu) >> 7);
+  const uint32_t pos = ((bits >> 15) & 1u) ^ 1u;
+  if (e < kWinELo) {
+    atomicAdd(&h->tiny_cnt[pos], 1u);
+    atomicAdd(&h->tiny_w[pos], ex2(l * c));
+  } else {
+    h->out_of_range = 1u;
+  }
+}
+
+// Count the elements of 4 words of packed bf16 pairs that lie at or above
+// the floor `flo` (-inf never does). The common case is one predicated
+// shared-memory add per element; the rare out-of-range ones are redone by
+// the warp's lanes that hold any.
+__device__ __forceinline__ void win_count(WinHist* h, const uint32_t w[4], float flo, float c) {
+  bool rare = false;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t b0 = w[t] & 0xFFFFu, b1 = w[t] >> 16;
+    const float l0 = __uint_as_float(w[t] << 16), l1 = __uint_as_float(w[t] & 0xFFFF0000u);
+    bool f0, f1;
+    const int k0 = win_slot(b0, f0), k1 = win_slot(b1, f1);
+    const bool c0 = l0 >= flo, c1 = l1 >= flo;
+    if (c0 && f0) atomicAdd(&h->cnt[k0], 1u);
+    if (c1 && f1) atomicAdd(&h->cnt[k1], 1u);
+    rare |= (c0 && !f0) || (c1 && !f1);
+  }
+  if (__any_sync(0xFFFFFFFFu, rare) && rare) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t b0 = w[t] & 0xFFFFu, b1 = w[t] >> 16;
+      const float l0 = __uint_as_float(w[t] << 16), l1 = __uint_as_float(w[t] & 0xFFFF0000u);
+      bool f0, f1;
+      win_slot(b0, f0);
+      win_slot(b1, f1);
+      if (l0 >= flo && !f0) win_add_rare(h, b0, l0, c);
+      if (l1 >= flo && !f1) win_add_rare(h, b1, l1, c);
+    }
+  }
+}
+
+// Value of fine item i (not a merged one).
+__device__ __forceinline__ float win_value(int i) {
+  if (i < kWinHalf) {
+    const uint32_t a = (uint32_t)(kWinHalf - 1 - i) + kWinELo * 128u;
+    return __uint_as_float((0x8000u | a) << 16);
+  }
+  const uint32_t a = (uint32_t)(i - kWinHalf - 2) + kWinELo * 128u;
+  return __uint_as_float(a << 16);
 }
 
 // Sum of v over consumer threads with a larger index (exclusive suffix sum).
@@ -72,242 +166,144 @@ struct HistResult {
   int pending;  // 1: leave the row to the exact slow path
 };
 
-// Count and mass of one value (mass 0 for -inf and for NaN / +inf, which
-// are reported separately).
-__device__ __forceinline__ bool bf16_nonfinite(uint32_t bits) {
-  return ((bits & 0x7F80u) == 0x7F80u) && bits != 0xFF80u;
-}
-__device__ __forceinline__ float value_mass(uint32_t bits, unsigned n, float c, float mc) {
-  if (!n || bits == 0xFF80u || bf16_nonfinite(bits)) return 0.f;
-  return (float)n * ex2(fmaf(__uint_as_float(bits << 16), c, -mc));
-}
-
-// Warp-level refinement inside one 128-key block (keys 128 blk + 4 lane ..
-// + 3): returns, in every lane of the calling warp,
-//   mode 0: the largest key whose weight summed from the top of the block,
-//           plus `above`, reaches `target` (top-k: counts);
-//   mode 1: the smallest nonempty key >= `from` whose weight strictly above
-//           it, plus `above`, is < `target` (top-p: masses).
-// `wt(key)` gives the weight of a key (0 below `from`), `nz(key)` whether it
-// holds tokens.
-// As warp_refine, and *below_sum receives the sum of sw(key) over the
-// block's keys >= the returned key.
-template <typename Wt, typename Nz, typename Sw>
-__device__ __forceinline__ int warp_refine_sum(int blk, float above, float target, int mode,
-                                               Wt wt, Nz nz, Sw sw, float* sum_from) {
-  const int lane = threadIdx.x & 31;
-  float w[4];
-  bool nzv[4];
-  float mine = 0.f;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int key = blk * 128 + 4 * lane + e;
-    w[e] = wt(key);
-    nzv[e] = nz(key);
-    mine += w[e];
-  }
-  // weight of all lanes above this one (keys of higher lanes are larger)
-  float x = mine;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_down_sync(0xFFFFFFFFu, x, o);
-    if (lane + o < 32) x += y;
-  }
-  float run = above + (x - mine);  // weight strictly above this lane's keys
-  int cand = mode == 0 ? -1 : 0x7FFFFFFF;
-#pragma unroll
-  for (int e = 3; e >= 0; --e) {
-    const int key = blk * 128 + 4 * lane + e;
-    if (mode == 0) {
-      if (cand < 0 && run < target && run + w[e] >= target) cand = key;
-    } else if (nzv[e] && run < target) {
-      cand = key;
-    }
-    run += w[e];
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const int c2 = __shfl_xor_sync(0xFFFFFFFFu, cand, o);
-    cand = mode == 0 ? max(cand, c2) : min(cand, c2);
-  }
-  float part = 0.f;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const int key = blk * 128 + 4 * lane + e;
-    if (key >= cand) part += sw(key);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
-  *sum_from = part;
-  return cand;
-}
-
-template <typename Wt, typename Nz>
-__device__ __forceinline__ int warp_refine(int blk, float above, float target, int mode, Wt wt,
-                                           Nz nz) {
-  float unused;
-  return warp_refine_sum(blk, above, target, mode, wt, nz, wt, &unused);
-}
-
-
-// Row-end processing of the 16-bit value histogram by the kWarps consumer
-// warps (all call it). Warp w sums the 128-key blocks w, w + kWarps, ...
-// (empty blocks cost one ballot), so dense and sparse key ranges spread
-// over all warps; the per-block totals then locate the top-k and top-p
-// blocks, which one warp refines to the exact value. Clears the histogram.
+// Row-end processing of the window histogram by the kWarps consumer warps
+// (all call it): m the row max, c = log2(e) / T, zfull the sum of
+// 2^(l c - m c) over the whole row, lo = m - D the window floor. Thread t
+// owns a run of consecutive items (kWinFine / threads fine ones; the merged
+// two go to the threads on either side of the sign change), and higher
+// threads hold larger values. Each thread reads its items' counts once,
+// clears them, and works from registers; items not wholly inside the window
+// (values below lo, not all counted) read as empty, so a threshold never
+// lands on them. Clears the histogram.
 template <int kWarps>
-__device__ HistResult hist16_finish(uint32_t* h, float m, float c, int tk, float tp, int V,
-                                    int tid, float* fscr, int* iscr) {
-  constexpr int kBlocks = 512;  // 128 keys each
-  static_assert(kWarps * 32 == kBlocks, "one block total per consumer thread");
-  __shared__ unsigned blk_cnt[kBlocks];
-  __shared__ float blk_mass[kBlocks];
-  __shared__ int s_blk, s_key, s_from_blk;
-  __shared__ float s_above, s_from;
-  const int lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    // -0 and +0 are one value: move the count of -0 (bits 0x8000) to +0.
-    const unsigned neg0 = h[0x4000] & 0xFFFFu;
-    h[0x4000] &= 0xFFFF0000u;
-    h[0] += neg0;  // a carry out of +0 breaks the total below: detected
-  }
-  named_sync(1, kWarps * 32);
+__device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, float lo, int tk,
+                                 float tp, int V, int tid, float* fscr, int* iscr) {
+  constexpr int kThreads = kWarps * 32;
+  constexpr int kPer = kWinFine / kThreads;
+  constexpr int kHalfT = kThreads / 2;
+  constexpr int kMax = kPer + 1;  // items of the two threads at the sign change
+  static_assert(kPer * kThreads == kWinFine, "fine items split evenly over the threads");
+  static_assert(kPer * kHalfT == kWinHalf, "the sign change falls between two threads");
+  __shared__ int s_item;
+  const int i0 = tid < kHalfT ? tid * kPer : tid * kPer + 2 - (tid == kHalfT ? 1 : 0);
+  const int ni = (tid == kHalfT - 1 || tid == kHalfT) ? kMax : kPer;
   const float mc = m * c;
-  auto cnt_of = [&](int key) -> unsigned { return hist16_count(h, key_bf16((uint32_t)key)); };
-  auto mass_of = [&](int key) -> float {
-    const uint32_t bits = key_bf16((uint32_t)key);
-    return value_mass(bits, hist16_count(h, bits), c, mc);
-  };
-
-  // Pass 1: per-block totals. A block's 128 values are 64 consecutive words;
-  // lane l reads words 2l, 2l+1 (keys 4l .. 4l+3 up to the block's order).
-  unsigned bad_w = 0;
-  for (int blk = warp; blk < kBlocks; blk += kWarps) {
-    const uint32_t b0 = key_bf16((uint32_t)blk * 128u), b1 = key_bf16((uint32_t)blk * 128u + 127u);
-    const uint32_t bmin = b0 < b1 ? b0 : b1;
-    const uint2 q = reinterpret_cast<const uint2*>(h + (bmin >> 1))[lane];
-    const bool any = __any_sync(0xFFFFFFFFu, (q.x | q.y) != 0u);
-    unsigned cn = 0;
-    float ms = 0.f;
-    if (any) {
-      const uint32_t wd[2] = {q.x, q.y};
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-#pragma unroll
-        for (int hl = 0; hl < 2; ++hl) {
-          const unsigned n = (wd[j] >> (16 * hl)) & 0xFFFFu;
-          const uint32_t bits = bmin + (uint32_t)(4 * lane + 2 * j + hl);
-          cn += n;
-          if (bf16_nonfinite(bits)) bad_w += n;
-          else ms += value_mass(bits, n, c, mc);
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        cn += __shfl_xor_sync(0xFFFFFFFFu, cn, o);
-        ms += __shfl_xor_sync(0xFFFFFFFFu, ms, o);
-      }
-    }
-    if (lane == 0) {
-      blk_cnt[blk] = cn;
-      blk_mass[blk] = ms;
-    }
-  }
-  named_sync(1, kWarps * 32);
-  // From here thread t holds block t's totals.
-  const unsigned cnt_t = blk_cnt[tid];
-  const float mass_t = blk_mass[tid];
-  const int total = consumer_reduce<int, kWarps>((int)cnt_t, iscr, tid,
-                                                 [](int a, int b) { return a + b; });
-  const int bad = consumer_reduce<int, kWarps>((int)bad_w, iscr, tid,
-                                               [](int a, int b) { return a + b; });
   const bool topk_on = (tk > 0 && tk < V);
   const bool topp_on = (tp < 1.f);
+  const float emc = ex2(-mc);
 
-  // top-k: the key holding the k-th largest value (counts from the top).
-  int bk = 0;
-  if (topk_on) {
-    if (tid == 0) s_blk = 0;
-    const unsigned run = suffix_exclusive<unsigned, kWarps>(cnt_t, (unsigned*)iscr, tid);
-    if (run < (unsigned)tk && run + cnt_t >= (unsigned)tk) {
-      s_blk = tid;
-      s_above = (float)run;
-    }
-    named_sync(1, kWarps * 32);
-    if (warp == 0) {
-      const int blk = s_blk;
-      float from = 0.f;
-      int key = warp_refine_sum(
-          blk, s_above, (float)tk, 0, [&](int k) { return (float)cnt_of(k); },
-          [&](int k) { return cnt_of(k) != 0u; }, [&](int k) { return mass_of(k); }, &from);
-      if (lane == 0) {
-        s_key = key < 0 ? blk * 128 : key;
-        s_from = from;
-        s_from_blk = blk;
+  // Counts and masses of this thread's items, in increasing value order.
+  unsigned cn[kMax];
+  float ms[kMax];
+  unsigned my_cnt = 0;
+#pragma unroll
+  for (int k = 0; k < kMax; ++k) {
+    const int i = i0 + k;
+    cn[k] = 0u;
+    ms[k] = 0.f;
+    if (k < ni) {
+      unsigned n;
+      float w;
+      bool whole;
+      if (i == kWinTinyNeg || i == kWinTinyPos) {
+        const int s = i - kWinTinyNeg;
+        n = h->tiny_cnt[s];
+        w = h->tiny_w[s] * emc;
+        h->tiny_cnt[s] = 0u;
+        h->tiny_w[s] = 0.f;
+        whole = (s == 0) ? (lo <= kWinTinyNegLow) : (lo <= 0.f);
+      } else {
+        n = h->cnt[i];
+        h->cnt[i] = 0u;
+        const float v = win_value(i);
+        w = n ? (float)n * ex2(fmaf(v, c, -mc)) : 0.f;
+        whole = v >= lo;
+      }
+      if (whole) {
+        cn[k] = n;
+        ms[k] = w;
+        my_cnt += n;
       }
     }
-    named_sync(1, kWarps * 32);
-    bk = s_key;
   }
-  // This block's mass over keys >= key0; the block holding key0 takes the
-  // partial sum its refinement produced.
-  auto mass_from = [&](int key0, float from) -> float {
-    const int k0 = tid * 128;
-    if (k0 >= key0) return mass_t;
-    if (k0 + 127 < key0) return 0.f;
-    return from;
-  };
-  const float part_k = topk_on ? mass_from(bk, s_from) : mass_t;
-  const float zk = consumer_reduce<float, kWarps>(part_k, fscr, tid,
-                                                  [](float a, float b) { return a + b; });
+  auto merged = [](int i) { return i == kWinTinyNeg || i == kWinTinyPos; };
+  int pending = (zfull == zfull && m < INFINITY) ? 0 : 1;  // NaN or +inf in the row
 
-  // top-p: keep value v iff the mass strictly above it (within the top-k set)
-  // is < top_p * Z_k; the kept values are the top ones down to bp.
-  int bp = bk;
+  // top-k: the item holding the k-th largest value (counts from the top).
+  int ik = -1;  // lowest item kept by top-k (-1: all)
+  if (topk_on) {
+    if (tid == 0) s_item = -1;
+    const unsigned above = suffix_exclusive<unsigned, kWarps>(my_cnt, (unsigned*)iscr, tid);
+    if (above < (unsigned)tk && above + my_cnt >= (unsigned)tk) {
+      unsigned run = above;
+      int found = -1;
+#pragma unroll
+      for (int k = kMax - 1; k >= 0; --k) {
+        if (k < ni && found < 0) {
+          run += cn[k];
+          if (run >= (unsigned)tk) found = i0 + k;
+        }
+      }
+      s_item = found;
+    }
+    named_sync(1, kThreads);
+    ik = s_item;
+    if (ik < 0 || merged(ik)) pending = 1;  // outside the window, or on a merged item
+  }
+
+  // Mass of this thread's items in the top-k set.
+  float my_mass = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMax; ++k)
+    if (i0 + k >= ik) my_mass += ms[k];
+  float zk = zfull;
+  if (topk_on)
+    zk = consumer_reduce<float, kWarps>(my_mass, fscr, tid, [](float a, float b) { return a + b; });
+
+  // top-p: keep value v iff the mass strictly above it (in the top-k set) is
+  // < top_p Z_k: the kept values run from the top down to item ip, the
+  // lowest nonempty item whose mass above is below the bar.
+  int ikeep = ik;
+  float z = zk;
   if (topp_on) {
     const float thr = tp * zk;
-    const float run = suffix_exclusive<float, kWarps>(part_k, fscr, tid);
-    // The lowest block whose mass above is below thr holds the crossing
-    // (every lower block has mass above >= thr and is dropped whole).
-    if (tid == 0) s_blk = 0x7FFFFFFF;
-    named_sync(1, kWarps * 32);
-    if (part_k > 0.f && run < thr) atomicMin(&s_blk, tid);
-    named_sync(1, kWarps * 32);
-    const int blk = s_blk == 0x7FFFFFFF ? 0 : s_blk;
-    if (tid == blk) s_above = run;
-    named_sync(1, kWarps * 32);
-    if (warp == 0) {
-      float from = 0.f;
-      const int key = warp_refine_sum(
-          blk, s_above, thr, 1, [&](int k) { return k >= bk ? mass_of(k) : 0.f; },
-          [&](int k) { return k >= bk && cnt_of(k) != 0u; },
-          [&](int k) { return k >= bk ? mass_of(k) : 0.f; }, &from);
-      if (lane == 0) {
-        s_key = (key == 0x7FFFFFFF) ? blk * 128 + 127 : key;
-        s_from = from;
+    const float above = suffix_exclusive<float, kWarps>(my_mass, fscr, tid);
+    int cand = 0x7FFFFFFF;
+    float run = above;
+#pragma unroll
+    for (int k = kMax - 1; k >= 0; --k) {
+      const int i = i0 + k;
+      if (k < ni && i >= ik) {
+        if (cn[k] && run < thr) cand = i;
+        run += ms[k];
       }
     }
-    named_sync(1, kWarps * 32);
-    bp = s_key;
-  }
-  float zpart;
-  if (topp_on) zpart = mass_from(bp, s_from);
-  else zpart = part_k;
-  const float z = consumer_reduce<float, kWarps>(zpart, fscr, tid,
-                                                 [](float a, float b) { return a + b; });
-
-  // Clear the blocks that held tokens (thread t: block t's 64 words).
-  if (cnt_t) {
-    const uint32_t b0 = key_bf16((uint32_t)tid * 128u), b1 = key_bf16((uint32_t)tid * 128u + 127u);
-    uint4* pz = reinterpret_cast<uint4*>(h + ((b0 < b1 ? b0 : b1) >> 1));
+    if (tid == 0) s_item = 0x7FFFFFFF;
+    named_sync(1, kThreads);
+    if (cand != 0x7FFFFFFF) atomicMin(&s_item, cand);
+    named_sync(1, kThreads);
+    const int ip = s_item;
+    if (ip == 0x7FFFFFFF || merged(ip)) pending = 1;
+    ikeep = ip;
+    float zpart = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) pz[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int k = 0; k < kMax; ++k)
+      if (i0 + k >= ip) zpart += ms[k];
+    z = consumer_reduce<float, kWarps>(zpart, fscr, tid, [](float a, float b) { return a + b; });
+    // The next value below ip has the kept mass z above it; it is dropped
+    // (wherever it lies, inside the window or not) iff z >= thr. Unless
+    // top-k ends the set at ip, a kept mass below the bar means the kept set
+    // might continue below the window.
+    if (!pending && !(topk_on && ip == ik) && !(z >= thr)) pending = 1;
   }
-  named_sync(1, kWarps * 32);
+
+  const unsigned oor = h->out_of_range;
+  named_sync(1, kThreads);
+  if (tid == 0) h->out_of_range = 0u;
 
   HistResult res;
-  res.pending = (total != V) || (bad > 0);
-  res.theta = (topk_on || topp_on) ? __uint_as_float(key_bf16((uint32_t)bp) << 16) : -INFINITY;
+  res.pending = (pending || oor != 0u) ? 1 : 0;
+  res.theta = (!res.pending && ikeep >= 0) ? win_value(ikeep) : -INFINITY;
   res.z = z;
   return res;
 }

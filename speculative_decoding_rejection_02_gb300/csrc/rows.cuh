@@ -272,9 +272,8 @@ __device__ __forceinline__ float key_threshold(uint32_t k, int bf16) {
   return key_float(k);
 }
 
-__global__ void __launch_bounds__(kFilterThreads)
-k_rows_filtered(Params P) {
-  const long long row = blockIdx.x;
+// One filtered row, exactly, by the whole block (all threads call it).
+__device__ void filtered_row(const Params& P, long long row) {
   __shared__ int s_req, s_cls, s_ok;
   if (threadIdx.x == 0) {
     int r = 0;
@@ -284,7 +283,6 @@ k_rows_filtered(Params P) {
   }
   __syncthreads();
   if (!s_ok || s_cls != kFiltered) return;
-  if (P.fast_filtered && !(P.rows[row].status & 0x80000000u)) return;  // done by the fast path
   const int r = s_req;
   const int bf16 = P.bf16;
   const float c = kLog2e / __ldg(P.temp + r);
@@ -356,6 +354,21 @@ k_rows_filtered(Params P) {
   if (threadIdx.x == 0) {
     const float theta = (kp <= 0) ? -INFINITY : key_threshold((uint32_t)kp, bf16);
     finish_row(P, row, r, kFiltered, m, am, z, theta, c);
+  }
+}
+
+// Without the streaming pass's histogram: block b settles row b. With it:
+// the blocks share out the rows that pass listed as unsettled.
+__global__ void __launch_bounds__(kFilterThreads)
+k_rows_filtered(Params P) {
+  if (!P.fast_filtered) {
+    filtered_row(P, blockIdx.x);
+    return;
+  }
+  const unsigned n = *P.pending_count;
+  for (unsigned i = blockIdx.x; i < n; i += gridDim.x) {
+    filtered_row(P, P.pending_rows[i]);
+    __syncthreads();
   }
 }
 

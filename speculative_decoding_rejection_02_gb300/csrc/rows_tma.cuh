@@ -25,8 +25,8 @@ constexpr int kTmaConsumerWarps = 16;
 constexpr int kTmaConsumers = kTmaConsumerWarps * 32;
 constexpr int kTmaThreads = kTmaConsumers + 32;
 constexpr int kTmaStages = 3;
-// Stage size: 32 KB for the softmax / argmax rows; 24 KB next to the 128 KB
-// histogram of the top-k / top-p variant.
+// Stage size: 32 KB for the softmax / argmax rows; 24 KB next to the 24 KB
+// window histogram of the top-k / top-p variant (two CTAs per SM either way).
 __host__ __device__ constexpr int tma_stage_bytes(bool filt) { return filt ? 24576 : 32768; }
 __host__ __device__ constexpr int tma_vec_per_thread(bool filt) {
   return tma_stage_bytes(filt) / 16 / kTmaConsumers;
@@ -42,6 +42,7 @@ struct StageMeta {
   int last;  // 1 on the row's last stage
   int tk;    // top-k of the row's request (filtered rows)
   float tp;  // top-p of the row's request (filtered rows)
+  float delta;  // window half-width of the row's histogram (filtered rows)
 };
 
 __host__ __device__ constexpr size_t tma_ring_bytes(bool filt) {
@@ -49,9 +50,9 @@ __host__ __device__ constexpr size_t tma_ring_bytes(bool filt) {
          kTmaStages * sizeof(StageMeta);
 }
 constexpr size_t kTmaSmemBytes = tma_ring_bytes(false);
-// The top-k / top-p variant adds the 128 KB value histogram (16-byte aligned).
+// The top-k / top-p variant adds the window histogram (16-byte aligned).
 constexpr size_t kTmaHistOffset = (tma_ring_bytes(true) + 255) & ~size_t(255);
-constexpr size_t kTmaFiltSmemBytes = kTmaHistOffset + kHist16Bytes;
+constexpr size_t kTmaFiltSmemBytes = kTmaHistOffset + sizeof(WinHist);
 
 struct RowInfo {
   long long row;
@@ -65,8 +66,8 @@ struct RowInfo {
 // Warp-parallel lookup of the request owning `row` and its settings (all 32
 // lanes call it; every lane gets the result). Two or three dependent rounds
 // of loads instead of a serial binary search.
-// want_filtered: take only rows with top-k / top-p (true) or only the others.
-__device__ RowInfo warp_row_info(const Params& P, long long row, bool want_filtered) {
+// take_filtered: take every row (true) or skip the rows with top-k / top-p.
+__device__ RowInfo warp_row_info(const Params& P, long long row, bool take_filtered) {
   const int lane = threadIdx.x & 31;
   int lo = 0, hi = P.B;  // answer in [lo, hi)
   while (hi - lo > 1) {
@@ -115,16 +116,18 @@ __device__ RowInfo warp_row_info(const Params& P, long long row, bool want_filte
   info.x = __shfl_sync(0xFFFFFFFFu, x, 0);
   info.tk = __shfl_sync(0xFFFFFFFFu, tk, 0);
   info.tp = __shfl_sync(0xFFFFFFFFu, tp, 0);
-  info.cls = ((cls == kFiltered) != want_filtered) ? -1 : cls;
+  info.cls = (!take_filtered && cls == kFiltered) ? -1 : cls;
   info.c = (cls != kArgmaxOnly) ? kLog2e / T : 0.f;
   return info;
 }
 
-// FILT = false: argmax-only and plain-softmax rows (2 CTAs per SM).
-// FILT = true (bf16 only): rows with top-k / top-p, counted into a value
-// histogram (1 CTA per SM: the histogram takes 128 KB).
+// FILT = false: argmax-only and plain-softmax rows (batches without top-k /
+// top-p, or whose filtered rows all go to the exact slow kernel).
+// FILT = true (bf16 only): every row; on rows with top-k / top-p the
+// elements near the row max are also counted into the window histogram of
+// hist.cuh, and rows it cannot settle are listed for the slow kernel.
 template <bool BF16, bool FILT>
-__global__ void __launch_bounds__(kTmaThreads, FILT ? 1 : 2)
+__global__ void __launch_bounds__(kTmaThreads, 2)
 k_rows_tma(Params P, long long R) {
   static_assert(!FILT || BF16, "the histogram path is for bf16 rows");
   constexpr int kTmaStageBytes = tma_stage_bytes(FILT);
@@ -159,7 +162,7 @@ k_rows_tma(Params P, long long R) {
     RowInfo cur;
     cur.cls = -1;
     while (row < R) {  // first row with work
-      cur = warp_row_info(P, row, FILT);
+      cur = warp_row_info(P, row, FILT);  // FILT: every row
       if (cur.cls >= 0) break;
       row += gridDim.x;
     }
@@ -190,6 +193,7 @@ k_rows_tma(Params P, long long R) {
           M.last = (ch == nchunks - 1) ? 1 : 0;
           M.tk = cur.tk;
           M.tp = cur.tp;
+          M.delta = FILT ? win_delta(cur.c, cur.tk, cur.tp, P.V) : 0.f;
           mbar_arrive_expect_tx(&full[stage], bytes);
           bulk_load(ring + (size_t)stage * kTmaStageBytes, src + off, bytes, &full[stage]);
         }
@@ -242,11 +246,11 @@ k_rows_tma(Params P, long long R) {
   __shared__ int iscr[kTmaConsumerWarps];
   const int tid = threadIdx.x;
   constexpr int epc = 16 / esize;
-  // Value histogram of the current filtered row (FILT only): 16-bit counters.
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smem + kTmaHistOffset);
+  // Window histogram of the current filtered row (FILT only).
+  WinHist* hist = reinterpret_cast<WinHist*>(smem + kTmaHistOffset);
   if (FILT) {
     uint4* hz = reinterpret_cast<uint4*>(hist);
-    for (int i = tid; i < (int)(kHist16Bytes / 16); i += kTmaConsumers)
+    for (int i = tid; i < (int)(sizeof(WinHist) / 16); i += kTmaConsumers)
       hz[i] = make_uint4(0u, 0u, 0u, 0u);
     named_sync(1, kTmaConsumers);
   }
@@ -267,7 +271,8 @@ k_rows_tma(Params P, long long R) {
     if (M.row < 0) break;
     const uint4* buf = reinterpret_cast<const uint4*>(ring + (size_t)stage * kTmaStageBytes);
     const int nvec = M.n / epc;
-    const bool soft = (M.cls == kSoftmax);
+    // The row sum Z runs on softmax rows and (for top-p) on filtered rows.
+    const bool soft = (M.cls == kSoftmax) || (FILT && M.cls == kFiltered);
     // This thread's vectors of the stage, in increasing element order; the
     // missing ones read as -inf (no max, no mass).
     constexpr uint32_t pad = BF16 ? 0xFF80FF80u : 0xFF800000u;
@@ -345,18 +350,14 @@ k_rows_tma(Params P, long long R) {
       f2_unpack(acc1, a2, a3);
       s += (a0 + a1) + (a2 + a3);
     }
-    if (FILT) {
-      // Count every element under its raw bits (two 16-bit counters a word).
+    if (FILT && M.cls == kFiltered) {
+      // Count the elements at or above this thread's window floor (its
+      // running max minus D; -inf and the padding never count).
+      const float flo = fmaxf(vmax - M.delta, -3.402823466e38f);
 #pragma unroll
       for (int k = 0; k < kTmaVecPerThread; ++k) {
-        if (tid + k * kTmaConsumers >= nvec) continue;
         const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const uint32_t lo = w[t] & 0xFFFFu, hi = w[t] >> 16;
-          atomicAdd(&hist[lo >> 1], (lo & 1u) ? 0x10000u : 1u);
-          atomicAdd(&hist[hi >> 1], (hi & 1u) ? 0x10000u : 1u);
-        }
+        win_count(hist, w, flo, M.c);
       }
     }
     {
@@ -407,9 +408,17 @@ k_rows_tma(Params P, long long R) {
       named_sync(1, kTmaConsumers);
       m = bc_m;
       a = bc_i;
-      if (FILT) {
-        const HistResult hr = hist16_finish<kTmaConsumerWarps>(hist, m, M.c, M.tk, M.tp, P.V,
-                                                               tid, fscr, iscr);
+      if (FILT && M.cls == kFiltered) {
+        const float mc = m * M.c;
+        float part = 0.f;
+        if (vmax > -INFINITY && m > -INFINITY) part = s * ex2(vmc - mc);
+        part = warp_sum(part);
+        if (lane == 0) red_s[warp] = part;
+        named_sync(1, kTmaConsumers);
+        float zfull = 0.f;
+        for (int w = 0; w < kTmaConsumerWarps; ++w) zfull += red_s[w];
+        const HistResult hr = win_finish<kTmaConsumerWarps>(hist, m, M.c, zfull, m - M.delta,
+                                                            M.tk, M.tp, P.V, tid, fscr, iscr);
         if (tid == 0) {
           if (hr.pending || !(m > -INFINITY)) {
             RowStats ps;
@@ -422,6 +431,7 @@ k_rows_tma(Params P, long long R) {
             ps.status = kPendingSlow;
             ps.z = 0.f;
             P.rows[M.row] = ps;
+            P.pending_rows[atomicAdd(P.pending_count, 1u)] = M.row;
           } else {
             finish_row_x(P, M.row, M.cls, m, a == kNoIndex ? 0 : a, hr.z, hr.theta, M.c, M.x,
                          s_lx);

@@ -27,7 +27,8 @@ struct spec_verify_handle {
   unsigned long long* race_best;
   unsigned* race_counter;
   sv::RaceTask* race_list;
-  unsigned* race_count;
+  unsigned* race_count;  // [2]: races listed, rows left to the slow kernel
+  long long* pending_rows;
   unsigned* status;
   int max_slices;
   cudaEvent_t phase[4];
@@ -93,6 +94,8 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   P.race_counter = h->race_counter;
   P.race_list = h->race_list;
   P.race_count = h->race_count;
+  P.pending_rows = h->pending_rows;
+  P.pending_count = h->race_count + 1;
   P.status = h->status;
   const int slice = P.bf16 ? sv::kSliceBf16 : sv::kSliceF32;
   P.slices_per_row = (b->V + slice - 1) / slice;
@@ -106,7 +109,7 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
     return SPEC_ERR_CAPACITY;
   const bool timed = h->n_phase >= 4;
   if (timed) cudaEventRecord(h->phase[0], stream);
-  if (!greedy && cudaMemsetAsync(h->race_count, 0, sizeof(unsigned), stream) != cudaSuccess)
+  if (!greedy && cudaMemsetAsync(h->race_count, 0, 2 * sizeof(unsigned), stream) != cudaSuccess)
     return SPEC_ERR_CUDA;
   const int esize = P.bf16 ? 2 : 4;
   const bool rows_aligned = (((long long)b->V * esize) % 16 == 0) &&
@@ -114,7 +117,12 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   const bool filters = !greedy && (P.top_k || P.top_p);
   P.fast_filtered = (rows_aligned && h->tma_blocks > 0 && h->filt_blocks > 0 && P.bf16 &&
                      filters) ? 1 : 0;
-  if (rows_aligned && h->tma_blocks > 0) {
+  if (P.fast_filtered) {
+    // One pass over every row; the filtered rows it cannot settle are listed.
+    const long long fgrid = R < h->filt_blocks ? R : h->filt_blocks;
+    sv::k_rows_tma<true, true><<<(unsigned)fgrid, sv::kTmaThreads, sv::kTmaFiltSmemBytes,
+                                 stream>>>(P, R);
+  } else if (rows_aligned && h->tma_blocks > 0) {
     const long long grid = R < h->tma_blocks ? R : h->tma_blocks;
     if (P.bf16)
       sv::k_rows_tma<true, false><<<(unsigned)grid, sv::kTmaThreads, sv::kTmaSmemBytes, stream>>>(
@@ -122,16 +130,15 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
     else
       sv::k_rows_tma<false, false><<<(unsigned)grid, sv::kTmaThreads, sv::kTmaSmemBytes,
                                      stream>>>(P, R);
-    if (P.fast_filtered) {
-      const long long fgrid = R < h->filt_blocks ? R : h->filt_blocks;
-      sv::k_rows_tma<true, true><<<(unsigned)fgrid, sv::kTmaThreads, sv::kTmaFiltSmemBytes,
-                                   stream>>>(P, R);
-    }
   } else {
     sv::k_rows_stream<<<(unsigned)(R * P.slices_per_row), sv::kStreamThreads, 0, stream>>>(P);
   }
-  if (!greedy && (P.top_k || P.top_p))
-    sv::k_rows_filtered<<<(unsigned)R, sv::kFilterThreads, 0, stream>>>(P);
+  if (filters) {
+    // Every filtered row (one block each), or only the listed ones.
+    const long long cap = 2ll * h->sm_count;
+    const long long sgrid = P.fast_filtered ? (R < cap ? R : cap) : R;
+    sv::k_rows_filtered<<<(unsigned)sgrid, sv::kFilterThreads, 0, stream>>>(P);
+  }
   if (timed) cudaEventRecord(h->phase[1], stream);
   sv::k_accept<<<(b->B + sv::kAcceptWarps - 1) / sv::kAcceptWarps, sv::kAcceptWarps * 32, 0,
                  stream>>>(P);
@@ -215,10 +222,11 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   const size_t sz_best = align_up(n_rows * sizeof(unsigned long long));
   const size_t sz_rccnt = align_up(n_rows * sizeof(unsigned));
   const size_t sz_list = align_up(n_rows * sizeof(sv::RaceTask));
-  const size_t sz_lcnt = align_up(sizeof(unsigned));
+  const size_t sz_lcnt = align_up(2 * sizeof(unsigned));
+  const size_t sz_pend = align_up(n_rows * sizeof(long long));
   const size_t sz_stat = align_up(sizeof(unsigned));
   const size_t total = sz_rows + sz_part + sz_rcnt + sz_race + sz_best + sz_rccnt + sz_list +
-                       sz_lcnt + sz_stat;
+                       sz_lcnt + sz_pend + sz_stat;
   if (cudaMalloc(&h->ws, total) != cudaSuccess) {
     delete h;
     return SPEC_ERR_CUDA;
@@ -237,6 +245,7 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   h->race_counter = (unsigned*)p; p += sz_rccnt;
   h->race_list = (sv::RaceTask*)p; p += sz_list;
   h->race_count = (unsigned*)p; p += sz_lcnt;
+  h->pending_rows = (long long*)p; p += sz_pend;
   h->status = (unsigned*)p;
   *out = h;
   return SPEC_OK;
@@ -320,7 +329,8 @@ constexpr size_t kNaOffBest = kNaOffRace + na_align(kNaBatch * sizeof(sv::RaceDe
 constexpr size_t kNaOffRccnt = kNaOffBest + na_align(kNaRows * sizeof(unsigned long long));
 constexpr size_t kNaOffList = kNaOffRccnt + na_align(kNaRows * sizeof(unsigned));
 constexpr size_t kNaOffLcnt = kNaOffList + na_align(kNaRows * sizeof(sv::RaceTask));
-constexpr size_t kNaOffStat = kNaOffLcnt + na_align(sizeof(unsigned));
+constexpr size_t kNaOffPend = kNaOffLcnt + na_align(2 * sizeof(unsigned));
+constexpr size_t kNaOffStat = kNaOffPend + na_align(kNaRows * sizeof(long long));
 constexpr size_t kNaBytes = kNaOffStat + na_align(sizeof(unsigned));
 static_assert(kNaBytes <= SPEC_NOALLOC_SCRATCH_BYTES, "no-allocation scratch too small");
 
@@ -415,6 +425,7 @@ extern "C" int spec_verify_run_noalloc(const spec_verify_batch* b, void* stream,
   h.race_counter = (unsigned*)(nd.base + kNaOffRccnt);
   h.race_list = (sv::RaceTask*)(nd.base + kNaOffList);
   h.race_count = (unsigned*)(nd.base + kNaOffLcnt);
+  h.pending_rows = (long long*)(nd.base + kNaOffPend);
   h.status = device_status ? device_status : (unsigned*)(nd.base + kNaOffStat);
   h.max_slices = (int)kNaSlices;
   h.n_phase = 0;

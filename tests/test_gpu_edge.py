@@ -172,3 +172,43 @@ def test_filtered_rows_on_the_streaming_path(scale, V):
     b = make_batch(logits, g, ids, temps, q, tk, tp, dtype="bf16", seed=V)
     gpu, _ = check(b)
     assert gpu["status"] & ~np.uint32(0x8) == 0
+
+
+@pytest.mark.parametrize("case", ["wide_top_k", "tiny_temperature", "both_filters", "heavy_tail"])
+def test_window_histogram_cases(case):
+    """Regimes of the window histogram of the filtered row pass: top-k sets
+    reaching past the window (left to the exact slow kernel), narrow windows
+    at small temperature, top-k and top-p together, and a top-p boundary on
+    a value that thousands of tokens share."""
+    rng = np.random.default_rng(["wide_top_k", "tiny_temperature", "both_filters",
+                                 "heavy_tail"].index(case) + 91)
+    V, B = 4096, 30
+    g = rng.integers(0, 4, size=B)
+    N = int(g.sum())
+    tk = tp = None
+    if case == "wide_top_k":
+        logits = rng.normal(0, 15, size=(N + B, V))
+        temps = rng.choice([0.5, 1.0], size=B)
+        tk = rng.choice([1000, 3000, 4000], size=B)
+    elif case == "tiny_temperature":
+        logits = rng.normal(0, 2, size=(N + B, V))
+        temps = rng.choice([0.01, 0.05], size=B)
+        tp = rng.choice([0.5, 0.9, 0.999], size=B)
+    elif case == "both_filters":
+        logits = rng.normal(0, 3, size=(N + B, V))
+        temps = np.ones(B)
+        tk = rng.choice([20, 200], size=B)
+        tp = rng.choice([0.5, 0.95], size=B)
+    else:
+        logits = np.full((N + B, V), -5.0)
+        hot = rng.integers(0, V, size=(N + B, 40))
+        for r in range(N + B):
+            logits[r, hot[r]] = rng.uniform(-1, 3, size=40)
+        temps = np.ones(B)
+        tp = rng.choice([0.5, 0.9, 0.99], size=B)
+    q = rng.random((N, V)) ** 2
+    q /= q.sum(1, keepdims=True)
+    ids = np.array([rng.choice(V, p=q[n]) for n in range(N)], np.int32)
+    b = make_batch(logits, g, ids, temps, q, tk, tp, dtype="bf16", seed=17)
+    gpu, _ = check(b)
+    assert gpu["status"] & ~np.uint32(0x8) == 0
