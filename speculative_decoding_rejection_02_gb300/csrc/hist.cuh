@@ -86,11 +86,23 @@ __device__ __forceinline__ void win_add_rare(WinHist* h, uint32_t bits, float l,
   }
 }
 
+// Shared-memory add of 1 to the counter at byte address `addr`, issued as
+// one predicated instruction (no branch around it).
+__device__ __forceinline__ void red_add1_if(uint32_t addr, bool on) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "@p red.shared.add.u32 [%0], 1;\n\t}" ::"r"(addr),
+      "r"((uint32_t)on)
+      : "memory");
+}
+
 // Count the elements of 4 words of packed bf16 pairs that lie at or above
 // the floor `flo` (-inf never does). The common case is one predicated
 // shared-memory add per element; the rare out-of-range ones are redone by
 // the warp's lanes that hold any.
 __device__ __forceinline__ void win_count(WinHist* h, const uint32_t w[4], float flo, float c) {
+  const uint32_t base = smem_addr(h->cnt);
   bool rare = false;
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
@@ -99,8 +111,8 @@ __device__ __forceinline__ void win_count(WinHist* h, const uint32_t w[4], float
     bool f0, f1;
     const int k0 = win_slot(b0, f0), k1 = win_slot(b1, f1);
     const bool c0 = l0 >= flo, c1 = l1 >= flo;
-    if (c0 && f0) atomicAdd(&h->cnt[k0], 1u);
-    if (c1 && f1) atomicAdd(&h->cnt[k1], 1u);
+    red_add1_if(base + 4u * (uint32_t)k0, c0 && f0);
+    red_add1_if(base + 4u * (uint32_t)k1, c1 && f1);
     rare |= (c0 && !f0) || (c1 && !f1);
   }
   if (__any_sync(0xFFFFFFFFu, rare) && rare) {
