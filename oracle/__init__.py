@@ -35,6 +35,7 @@ ST_EMPTY_RESIDUAL = 8
 
 FLAG_NAIVE = 1
 FLAG_SAMPLER_MATCH = 2
+FLAG_EARLY_EXIT = 4
 
 
 def build(force: bool = False) -> str:

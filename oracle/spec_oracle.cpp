@@ -332,6 +332,8 @@ typedef struct {
   int64_t request_base;         // global index of request 0 (RNG key)
   unsigned flags;               // bit 0: naive resample-from-p control
                                 // bit 1: sampler-match acceptance
+                                // bit 2: early exit (rows after the first
+                                //        rejection are never examined)
 } or_batch;
 
 // Per-call outputs and the decision log used to excuse near-tie decisions.
@@ -382,14 +384,42 @@ static void or_verify_one(const or_batch* b, int r, const or_outputs* o) {
   for (int i = 0; i < gamma; ++i)
     if (!valid(draft(i))) status |= 4u;
 
+  // Early exit ([velog] "드래프트가 제안하고 타깃이 판정한다": the first
+  // rejection ends the round, the later positions are discarded): the rows
+  // are examined in position order and the scan stops at the first
+  // rejection, so no row after it is read. Reading: an unusable row after
+  // the stop therefore does not void the request, and p_i(x_i) is left
+  // unset (NaN) for the positions after the stop. Every decision taken is
+  // the one below.
+  const bool early = (b->flags & 4u) != 0 && !(b->flags & 2u);
+  int k_star = gamma;
+  bool stopped = false;  // early exit: the scan already found k_star
+
+  // The accept test of position i (step 2), once its row has been examined.
+  auto judge = [&](int i) -> bool {
+    const int x = draft(i);
+    if (!(T > 0.0)) return x == argmax_row[i];
+    const double p_x = o->p_at_draft[c0 + i];
+    const double q_x = b->draft_probs
+                           ? (valid(x) ? (double)b->draft_probs[(int64_t)(c0 + i) * V + x] : 0.0)
+                           : 1.0;
+    const double u = or_accept_uniform(b->seed, greq, i);
+    if (q_x > 0.0) o->accept_margin[c0 + i] = std::fabs(p_x / q_x - u) / u;
+    return or_accept(p_x, q_x, u) != 0;
+  };
+
   // Step 1: the target pass over all gamma+1 rows ([cortexys] 방법: the
   // target evaluates every candidate position in one parallel pass). Every
   // draft position gets p_i(x_i), whether or not the scan reaches it.
-  for (int i = 0; i <= gamma; ++i) {
+  for (int i = 0; i <= gamma && !stopped; ++i) {
     load_row(i);
     if (!(T > 0.0)) {
       argmax_row[i] = or_argmax(l.data(), V);
       if (i < gamma) o->p_at_draft[c0 + i] = (draft(i) == argmax_row[i]) ? 1.0 : 0.0;
+      if (early && i < gamma && !judge(i)) {
+        k_star = i;
+        stopped = true;
+      }
       continue;
     }
     or_row_info info;
@@ -401,6 +431,10 @@ static void or_verify_one(const or_batch* b, int r, const or_outputs* o) {
     }
     o->topp_margin[row0 + i] = info.topp_margin;
     if (i < gamma) o->p_at_draft[c0 + i] = valid(draft(i)) ? p[draft(i)] : 0.0;
+    if (early && i < gamma && !judge(i)) {
+      k_star = i;
+      stopped = true;
+    }
   }
 
   // Sampler-match acceptance ([mlxcel] "투기적 디코딩", section "mlxcel의
@@ -432,25 +466,14 @@ static void or_verify_one(const or_batch* b, int r, const or_outputs* o) {
     return;
   }
 
-  // Step 2: left-to-right accept scan; stop at the first rejection.
-  int k_star = gamma;
-  for (int i = 0; i < gamma; ++i) {
-    int x = draft(i);
-    bool ok;
-    if (!(T > 0.0)) {
-      ok = (x == argmax_row[i]);
-    } else {
-      double p_x = o->p_at_draft[c0 + i];
-      double q_x = b->draft_probs
-                       ? (valid(x) ? (double)b->draft_probs[(int64_t)(c0 + i) * V + x] : 0.0)
-                       : 1.0;
-      double u = or_accept_uniform(b->seed, greq, i);
-      if (q_x > 0.0) o->accept_margin[c0 + i] = std::fabs(p_x / q_x - u) / u;
-      ok = or_accept(p_x, q_x, u) != 0;
-    }
-    if (!ok) {
-      k_star = i;
-      break;
+  // Step 2: left-to-right accept scan; stop at the first rejection (already
+  // done above under early exit).
+  if (!early) {
+    for (int i = 0; i < gamma; ++i) {
+      if (!judge(i)) {
+        k_star = i;
+        break;
+      }
     }
   }
 
