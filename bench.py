@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--accept", default="rejection", choices=["rejection", "sampler-match"],
                     help="acceptance rule: the rejection rule, or sampler-match (the "
                          "target's sampler draws every position; drafts must equal it)")
+    ap.add_argument("--early-exit", action="store_true",
+                    help="stop reading a request's rows at its first rejection")
     ap.add_argument("--B", type=int, default=None,
                     help="resize the workload to B requests (profiling of small cases)")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -110,7 +112,12 @@ def algorithmic_bytes(batch, num_accepted) -> dict:
         q_rows = int(rejected.sum()) * V * 4
         judged_q = int(np.minimum(num_accepted + 1, gam)[hot].sum()) * 4
     small = (B + 1) * 4 + N * 4 + B * 4 * 3 + judged_q + (N + B) * 4 + B * 4
-    return dict(row_pass=rows, race_q=q_rows, small=small, total=rows + q_rows + small)
+    # The rows up to each request's first rejection: all that early exit reads.
+    needed = int(np.minimum(num_accepted + 1, gam + 1).sum()) * V * esize
+    if int(batch.get("flags", 0)) & 4:
+        rows = needed
+    return dict(row_pass=rows, race_q=q_rows, small=small, total=rows + q_rows + small,
+                rows_to_first_rejection=needed, all_rows=R * V * esize)
 
 
 class ClockSampler:
@@ -296,6 +303,8 @@ def main():
     batch["request_base"] = rank_request_base(rank, B)
     if args.accept == "sampler-match":
         batch["flags"] = sv.FLAG_SAMPLER_MATCH
+    if args.early_exit:
+        batch["flags"] = int(batch.get("flags", 0)) | sv.FLAG_EARLY_EXIT
     cu = batch["cu_num_draft"]
     N = int(cu[-1])
     R = N + B
@@ -398,13 +407,14 @@ def main():
         cpu = {"value": rate, "unit": "draft_positions/s", "cores": 1, "kind": "oracle",
                "sample": desc, "seconds": round(secs, 2)}
 
-    # row pass, accept scan, race; with top-k / top-p the filtered-row kernel,
-    # and for bf16 rows that are 16-byte aligned the histogram row pass too
+    # row pass, accept scan, race; with top-k / top-p also the exact kernel
+    # for the rows the row pass leaves unsettled
     filters = batch.get("top_k") is not None or batch.get("top_p") is not None
-    aligned_bf16 = batch["logits_dtype"] == "bf16" and (V * 2) % 16 == 0
-    launches_per_step = 3 + ((2 if aligned_bf16 else 1) if filters else 0)
+    launches_per_step = 3 + (1 if filters else 0)
     if args.accept == "sampler-match":
         launches_per_step += 1  # k_match
+    if args.early_exit:
+        launches_per_step = 3  # queue init, row pass, race
     if rank == 0:
         line = {
             "metric": "verified draft positions/sec and achieved HBM GB/s (fraction of GB300 peak)",
@@ -417,6 +427,7 @@ def main():
                        "l2": ("inputs larger than L2" if flush is None
                               else "L2 flushed between timed calls (512 MB write)"),
                        "acceptance": args.accept,
+                       "early_exit": bool(args.early_exit),
                        "parallelism": f"replicas x{world}"},
             "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak,
             "algorithmic_bytes_per_step": bytes_,

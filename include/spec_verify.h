@@ -89,6 +89,17 @@ extern "C" {
  * probability p(x), as the rejection rule does. Temperature-0 requests keep
  * the argmax match. Cannot be combined with SPEC_FLAG_NAIVE. */
 #define SPEC_FLAG_SAMPLER_MATCH 0x2u
+/* Early-exit verification (velog, "드래프트가 제안하고 타깃이 판정한다": the
+ * first rejection ends the round and the later positions are discarded):
+ * each request's target rows are read in position order and reading stops
+ * at the first rejection, so the rows after it are never read. Every emitted
+ * token and count is the one the full pass gives; the differences are that
+ * an unusable row (NaN, +inf, all -inf) after the stop does not void the
+ * request, and p_at_draft is NaN at the positions after the stop. Needs
+ * 16-byte aligned target rows (V * element size a multiple of 16, aligned
+ * base), and bf16 logits when top_k / top_p are given; otherwise
+ * SPEC_ERR_UNSUPPORTED. Cannot be combined with SPEC_FLAG_SAMPLER_MATCH. */
+#define SPEC_FLAG_EARLY_EXIT 0x4u
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
 
@@ -148,8 +159,9 @@ int spec_verify_init(spec_verify_handle** h, const spec_verify_config* cfg);
  * requests take the argmax-match path, the others the probabilistic one.
  *   h [in] handle; b [in] host pointer to the batch description (device
  *   arrays inside); stream [in] a cudaStream_t (NULL = legacy default stream).
- * b->flags may hold SPEC_FLAG_NAIVE or SPEC_FLAG_SAMPLER_MATCH, not both;
- * anything else is SPEC_ERR_INVALID_ARG.
+ * b->flags may hold SPEC_FLAG_NAIVE, SPEC_FLAG_SAMPLER_MATCH and
+ * SPEC_FLAG_EARLY_EXIT, but SPEC_FLAG_SAMPLER_MATCH with neither of the
+ * others; anything else is SPEC_ERR_INVALID_ARG.
  * Returns SPEC_OK, SPEC_ERR_NOT_INIT, SPEC_ERR_INVALID_ARG, SPEC_ERR_CAPACITY
  * or SPEC_ERR_CUDA (launch failure). Asynchronous.
  */

@@ -30,6 +30,7 @@ STATUS_TIMEOUT = 0x20
 
 FLAG_NAIVE = 0x1
 FLAG_SAMPLER_MATCH = 0x2
+FLAG_EARLY_EXIT = 0x4
 
 # The entry points declared in include/spec_verify.h.
 ENTRY_POINTS = (

@@ -10,6 +10,7 @@
 namespace sv {
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxParts = 8;  // queue items carry (row << 3) | part
 constexpr int kNoIndex = 0x7FFFFFFF;
 
 // Row classes decided on the device from the request's sampling settings.
@@ -71,6 +72,18 @@ struct RaceTask {
                 // sampler-match)
 };
 
+// One part of a row streamed by one CTA under early exit (rows are split
+// into parts so that a request's rows, which are judged one after another,
+// each spread over several SMs).
+struct __align__(16) PartStat {
+  float m;      // max over the part
+  float z;      // sum of 2^(l c - fl(m c)) over the part (softmax / filtered rows)
+  int argmax;   // lowest index of the part max (kNoIndex: none)
+  float lx;     // logit at the row's draft token, if the part holds it
+  int has_lx;   // 1 when lx is set
+  int pad[3];
+};
+
 // Device view of one call.
 struct Params {
   int B, V, N;
@@ -102,6 +115,17 @@ struct Params {
   unsigned* status;
   long long* pending_rows;  // filtered rows left to the exact slow kernel
   unsigned* pending_count;  // entries in pending_rows (race_count + 1)
+  // Early exit (SPEC_FLAG_EARLY_EXIT): the row pass's work queue.
+  int early;
+  long long* queue;         // [q_cap] items (row << 3) | part
+  unsigned* queue_ready;    // [q_cap] 1 once the slot holds its item
+  unsigned* queue_ctl;      // control words, see early.cuh
+  int q_cap;
+  int parts;                // parts per row (1: a row stays in one CTA)
+  long long part_bytes;     // bytes per part (the last one may be shorter)
+  PartStat* part_stats;     // [max_batch x kMaxParts]: one row in flight per request
+  unsigned* part_done;      // [max_batch] parts of the request's current row done
+  void* part_hist;          // [max_batch] WinHist: merged window histograms
   int slices_per_row;
   int race_slices;
 };

@@ -178,6 +178,52 @@ struct HistResult {
   int pending;  // 1: leave the row to the exact slow path
 };
 
+// Add this CTA's window histogram into a global one and clear it (the
+// threads 0 .. nt-1 of the caller's group, tid among them).
+__device__ __forceinline__ void win_flush(WinHist* h, WinHist* g, int tid, int nt) {
+  for (int i = tid; i < kWinItems; i += nt) {
+    const unsigned v = h->cnt[i];
+    if (v) {
+      atomicAdd(&g->cnt[i], v);
+      h->cnt[i] = 0u;
+    }
+  }
+  if (tid == 0) {
+    for (int k = 0; k < 2; ++k) {
+      if (h->tiny_cnt[k]) {
+        atomicAdd(&g->tiny_cnt[k], h->tiny_cnt[k]);
+        atomicAdd(&g->tiny_w[k], h->tiny_w[k]);
+      }
+      h->tiny_cnt[k] = 0u;
+      h->tiny_w[k] = 0.f;
+    }
+    if (h->out_of_range) atomicOr(&g->out_of_range, 1u);
+    h->out_of_range = 0u;
+  }
+}
+
+// Move a global window histogram into this CTA's (which is clear) and clear
+// the global one.
+__device__ __forceinline__ void win_take(WinHist* h, WinHist* g, int tid, int nt) {
+  for (int i = tid; i < kWinItems; i += nt) {
+    const unsigned v = __ldcg(&g->cnt[i]);
+    if (v) {
+      h->cnt[i] = v;
+      g->cnt[i] = 0u;
+    }
+  }
+  if (tid == 0) {
+    for (int k = 0; k < 2; ++k) {
+      h->tiny_cnt[k] = __ldcg(&g->tiny_cnt[k]);
+      h->tiny_w[k] = __ldcg(&g->tiny_w[k]);
+      g->tiny_cnt[k] = 0u;
+      g->tiny_w[k] = 0.f;
+    }
+    h->out_of_range = __ldcg(&g->out_of_range);
+    g->out_of_range = 0u;
+  }
+}
+
 // Row-end processing of the window histogram by the kWarps consumer warps
 // (all call it): m the row max, c = log2(e) / T, zfull the sum of
 // 2^(l c - m c) over the whole row, lo = m - D the window floor. Thread t

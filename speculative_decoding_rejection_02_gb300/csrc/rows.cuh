@@ -238,9 +238,11 @@ k_rows_stream(Params P) {
 // ---------------------------------------------------------------------------
 constexpr int kFilterThreads = 512;
 
-// Visit every element (value, index) of a row, in increasing index per thread.
+// Visit every element (value, index) of a row, in increasing index per
+// thread, thread `tid` of `nt`.
 template <typename F>
-__device__ __forceinline__ void row_for_each(const Params& P, long long row, F&& f) {
+__device__ __forceinline__ void row_for_each(const Params& P, long long row, int tid, int nt,
+                                             F&& f) {
   const int V = P.V;
   const int esize = P.bf16 ? 2 : 4;
   const char* rowp = (const char*)P.logits + row * (long long)V * esize;
@@ -249,14 +251,24 @@ __device__ __forceinline__ void row_for_each(const Params& P, long long row, F&&
     const int epc = 16 / esize;
     const int nchunk = V / epc;
     jt = nchunk * epc;
-    for (int ch = threadIdx.x; ch < nchunk; ch += blockDim.x) {
+    for (int ch = tid; ch < nchunk; ch += nt) {
       float e[8];
       const int n = unpack_chunk(__ldg((const uint4*)rowp + ch), P.bf16, e);
       for (int t = 0; t < n; ++t) f(e[t], ch * epc + t);
     }
   }
-  for (int j = jt + threadIdx.x; j < V; j += blockDim.x) f(load_logit(P, row, j), j);
+  for (int j = jt + tid; j < V; j += nt) f(load_logit(P, row, j), j);
 }
+
+// The whole block as a thread group (for filtered_row_stats).
+struct BlockGroup {
+  __device__ int tid() const { return threadIdx.x; }
+  __device__ int size() const { return blockDim.x; }
+  __device__ void sync() const { __syncthreads(); }
+  template <typename T>
+  __device__ T sum(T x) const { return block_sum(x); }
+  __device__ void argmax(float& v, int& i) const { block_argmax(v, i); }
+};
 
 __device__ __forceinline__ uint32_t elem_key(float v, int bf16) {
   const uint32_t k = float_key(v);
@@ -272,18 +284,10 @@ __device__ __forceinline__ float key_threshold(uint32_t k, int bf16) {
   return key_float(k);
 }
 
-// One filtered row, exactly, by the whole block (all threads call it).
-__device__ void filtered_row(const Params& P, long long row) {
-  __shared__ int s_req, s_cls, s_ok;
-  if (threadIdx.x == 0) {
-    int r = 0;
-    s_ok = locate_row(P, row, r);
-    s_req = r;
-    s_cls = s_ok ? row_class(P, r) : kArgmaxOnly;
-  }
-  __syncthreads();
-  if (!s_ok || s_cls != kFiltered) return;
-  const int r = s_req;
+// One filtered row of request r, exactly, by a thread group G (all of its
+// threads call it; thread 0 writes the row's statistics).
+template <typename G>
+__device__ __noinline__ void filtered_row_stats(const Params& P, const G& g, long long row, int r) {
   const int bf16 = P.bf16;
   const float c = kLog2e / __ldg(P.temp + r);
   const int tk = P.top_k ? __ldg(P.top_k + r) : 0;
@@ -294,17 +298,17 @@ __device__ void filtered_row(const Params& P, long long row) {
   float vmax = -INFINITY;
   int imax = kNoIndex;
   int nan_seen = 0;
-  row_for_each(P, row, [&](float v, int j) {
+  row_for_each(P, row, g.tid(), g.size(), [&](float v, int j) {
     if (v > vmax || (imax == kNoIndex && v == v)) { vmax = v; imax = j; }
     nan_seen |= (v != v);
   });
   float m = vmax;
   int am = imax;
-  block_argmax(m, am);
-  nan_seen = block_sum(nan_seen);
+  g.argmax(m, am);
+  nan_seen = g.sum(nan_seen);
   if (am == kNoIndex) am = 0;
   if (nan_seen || m == INFINITY || m == -INFINITY) {
-    if (threadIdx.x == 0)
+    if (g.tid() == 0)
       finish_row(P, row, r, kFiltered, nan_seen ? NAN : m, am,
                  (nan_seen || m == INFINITY) ? NAN : 0.f, -INFINITY, c);
     return;
@@ -318,17 +322,17 @@ __device__ void filtered_row(const Params& P, long long row) {
     while (hi - lo > 1) {
       const long long mid = (lo + hi) >> 1;
       int cnt = 0;
-      row_for_each(P, row, [&](float v, int) { cnt += ((long long)elem_key(v, bf16) >= mid); });
-      cnt = block_sum(cnt);
+      row_for_each(P, row, g.tid(), g.size(), [&](float v, int) { cnt += ((long long)elem_key(v, bf16) >= mid); });
+      cnt = g.sum(cnt);
       if (cnt >= tk) lo = mid; else hi = mid;
     }
     kk = lo;
   }
   float zk = 0.f;
-  row_for_each(P, row, [&](float v, int) {
+  row_for_each(P, row, g.tid(), g.size(), [&](float v, int) {
     if ((long long)elem_key(v, bf16) >= kk) zk += exp2f(fmaf(v, c, -mc));
   });
-  zk = block_sum(zk);
+  zk = g.sum(zk);
 
   long long kp = kk;  // final key threshold
   if (topp_on) {
@@ -337,24 +341,38 @@ __device__ void filtered_row(const Params& P, long long row) {
     while (hi - lo > 1) {
       const long long mid = (lo + hi) >> 1;
       float a = 0.f;
-      row_for_each(P, row, [&](float v, int) {
+      row_for_each(P, row, g.tid(), g.size(), [&](float v, int) {
         const long long k = elem_key(v, bf16);
         if (k > mid && k >= kk) a += exp2f(fmaf(v, c, -mc));
       });
-      a = block_sum(a);
+      a = g.sum(a);
       if (a < thr) hi = mid; else lo = mid;
     }
     kp = hi;
   }
   float z = 0.f;
-  row_for_each(P, row, [&](float v, int) {
+  row_for_each(P, row, g.tid(), g.size(), [&](float v, int) {
     if ((long long)elem_key(v, bf16) >= kp) z += exp2f(fmaf(v, c, -mc));
   });
-  z = block_sum(z);
-  if (threadIdx.x == 0) {
+  z = g.sum(z);
+  if (g.tid() == 0) {
     const float theta = (kp <= 0) ? -INFINITY : key_threshold((uint32_t)kp, bf16);
     finish_row(P, row, r, kFiltered, m, am, z, theta, c);
   }
+}
+
+// One filtered row, exactly, by the whole block (all threads call it).
+__device__ void filtered_row(const Params& P, long long row) {
+  __shared__ int s_req, s_cls, s_ok;
+  if (threadIdx.x == 0) {
+    int r = 0;
+    s_ok = locate_row(P, row, r);
+    s_req = r;
+    s_cls = s_ok ? row_class(P, r) : kArgmaxOnly;
+  }
+  __syncthreads();
+  if (!s_ok || s_cls != kFiltered) return;
+  filtered_row_stats(P, BlockGroup(), row, s_req);
 }
 
 // Without the streaming pass's histogram: block b settles row b. With it:

@@ -18,6 +18,7 @@
 #include "pipe.cuh"
 #include "rows.cuh"
 #include "hist.cuh"
+#include "early.cuh"
 
 namespace sv {
 
@@ -43,6 +44,11 @@ struct StageMeta {
   int tk;    // top-k of the row's request (filtered rows)
   float tp;  // top-p of the row's request (filtered rows)
   float delta;  // window half-width of the row's histogram (filtered rows)
+  int r;        // request of the row
+  int pos;      // position of the row within its request (0 .. gamma)
+  int gamma;    // draft tokens of the request
+  int c0;       // cu_num_draft[r]
+  int part;     // part of the row (early exit; 0 otherwise)
 };
 
 __host__ __device__ constexpr size_t tma_ring_bytes(bool filt) {
@@ -61,6 +67,7 @@ struct RowInfo {
   int x;
   int tk;
   float tp;
+  int r, pos, gamma, c0;  // request, position in it, its draft count, cu[r]
 };
 
 // Warp-parallel lookup of the request owning `row` and its settings (all 32
@@ -99,6 +106,10 @@ __device__ RowInfo warp_row_info(const Params& P, long long row, bool take_filte
     info.x = -1;
     info.tk = 0;
     info.tp = 1.f;
+    info.r = r;
+    info.pos = 0;
+    info.gamma = 0;
+    info.c0 = 0;
     return info;
   }
   int x = -1, tk = 0;
@@ -114,6 +125,10 @@ __device__ RowInfo warp_row_info(const Params& P, long long row, bool take_filte
   cls = __shfl_sync(0xFFFFFFFFu, cls, 0);
   T = __shfl_sync(0xFFFFFFFFu, T, 0);
   info.x = __shfl_sync(0xFFFFFFFFu, x, 0);
+  info.r = r;
+  info.pos = (int)i;
+  info.gamma = c1 - c0;
+  info.c0 = c0;
   info.tk = __shfl_sync(0xFFFFFFFFu, tk, 0);
   info.tp = __shfl_sync(0xFFFFFFFFu, tp, 0);
   info.cls = (!take_filtered && cls == kFiltered) ? -1 : cls;
@@ -121,12 +136,61 @@ __device__ RowInfo warp_row_info(const Params& P, long long row, bool take_filte
   return info;
 }
 
+// A part's statistics written by another CTA (read through L2).
+__device__ __forceinline__ PartStat load_part(const PartStat* p) {
+  const int4 a = __ldcg(reinterpret_cast<const int4*>(p));
+  const int4 b = __ldcg(reinterpret_cast<const int4*>(p) + 1);
+  PartStat q;
+  q.m = __int_as_float(a.x);
+  q.z = __int_as_float(a.y);
+  q.argmax = a.z;
+  q.lx = __int_as_float(a.w);
+  q.has_lx = b.x;
+  q.pad[0] = b.y;
+  q.pad[1] = b.z;
+  q.pad[2] = b.w;
+  return q;
+}
+
+// The kTmaConsumers consumer threads as a thread group (for the exact
+// filtered-row bisection inside the row pass); fs / is: one slot per warp.
+struct ConsumerGroup {
+  float* fs;
+  int* is;
+  __device__ int tid() const { return threadIdx.x; }
+  __device__ int size() const { return kTmaConsumers; }
+  __device__ void sync() const { named_sync(1, kTmaConsumers); }
+  __device__ float sum(float x) const {
+    return consumer_reduce<float, kTmaConsumerWarps>(x, fs, threadIdx.x,
+                                                     [](float a, float b) { return a + b; });
+  }
+  __device__ int sum(int x) const {
+    return consumer_reduce<int, kTmaConsumerWarps>(x, is, threadIdx.x,
+                                                   [](int a, int b) { return a + b; });
+  }
+  __device__ void argmax(float& v, int& i) const {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    warp_argmax(v, i);
+    if (lane == 0) {
+      fs[warp] = v;
+      is[warp] = i;
+    }
+    sync();
+    v = fs[0];
+    i = is[0];
+    for (int w = 1; w < kTmaConsumerWarps; ++w) argmax_combine(v, i, fs[w], is[w]);
+    sync();
+  }
+};
+
 // FILT = false: argmax-only and plain-softmax rows (batches without top-k /
 // top-p, or whose filtered rows all go to the exact slow kernel).
 // FILT = true (bf16 only): every row; on rows with top-k / top-p the
 // elements near the row max are also counted into the window histogram of
 // hist.cuh, and rows it cannot settle are listed for the slow kernel.
-template <bool BF16, bool FILT>
+// EARLY: rows come from the early-exit work queue (early.cuh) and each row's
+// position is judged at its end.
+template <bool BF16, bool FILT, bool EARLY = false>
 __global__ void __launch_bounds__(kTmaThreads, 2)
 k_rows_tma(Params P, long long R) {
   static_assert(!FILT || BF16, "the histogram path is for bf16 rows");
@@ -158,64 +222,122 @@ k_rows_tma(Params P, long long R) {
     uint32_t issued = 0, issued_parity = 0;
     bool ok = true;
     const int nchunks = (int)((row_bytes + kTmaStageBytes - 1) / kTmaStageBytes);
-    long long row = blockIdx.x;
-    RowInfo cur;
-    cur.cls = -1;
-    while (row < R) {  // first row with work
-      cur = warp_row_info(P, row, FILT);  // FILT: every row
-      if (cur.cls >= 0) break;
-      row += gridDim.x;
-    }
-    while (row < R && ok) {
-      RowInfo next;
-      next.cls = -1;
-      long long nrow = row + gridDim.x;
-      bool next_done = false;
-      const char* src = (const char*)P.logits + row * row_bytes;
-      for (int ch = 0; ch < nchunks; ++ch) {
-        int waited = 1;
-        if (lane == 0) waited = mbar_wait(&empty[stage], phase ^ 1u) ? 1 : 0;
-        waited = __shfl_sync(0xFFFFFFFFu, waited, 0);
-        if (!waited) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          const long long off = (long long)ch * kTmaStageBytes;
-          const uint32_t bytes = (uint32_t)min((long long)kTmaStageBytes, row_bytes - off);
-          StageMeta& M = meta[stage];
-          M.row = row;
-          M.cls = cur.cls;
-          M.c = cur.c;
-          M.x = cur.x;
-          M.j0 = (int)(off / esize);
-          M.n = (int)(bytes / esize);
-          M.last = (ch == nchunks - 1) ? 1 : 0;
-          M.tk = cur.tk;
-          M.tp = cur.tp;
-          M.delta = FILT ? win_delta(cur.c, cur.tk, cur.tp, P.V) : 0.f;
-          mbar_arrive_expect_tx(&full[stage], bytes);
-          bulk_load(ring + (size_t)stage * kTmaStageBytes, src + off, bytes, &full[stage]);
-        }
-        issued |= 1u << stage;
-        issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == kTmaStages) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        if (ch == 0) {
-          // Look the next row up while this one streams.
-          while (nrow < R) {
-            next = warp_row_info(P, nrow, FILT);
-            if (next.cls >= 0) break;
-            nrow += gridDim.x;
+    if constexpr (EARLY) {
+      // Rows come from the work queue; the next one is taken only after the
+      // current row is issued (it may not be queued yet).
+      for (;;) {
+        long long item = -1;
+        if (lane == 0) item = queue_pop(P);
+        item = __shfl_sync(0xFFFFFFFFu, item, 0);
+        if (item < 0) break;
+        const long long row = item >> 3;
+        const int part = (int)(item & 7);
+        const RowInfo cur = warp_row_info(P, row, true);
+        const char* src = (const char*)P.logits + row * row_bytes;
+        const float delta = FILT ? win_delta(cur.c, cur.tk, cur.tp, P.V) : 0.f;
+        const long long off0 = (long long)part * P.part_bytes;
+        const long long off1 = min(off0 + P.part_bytes, row_bytes);
+        const int nch = (int)((off1 - off0 + kTmaStageBytes - 1) / kTmaStageBytes);
+        for (int ch = 0; ch < nch && ok; ++ch) {
+          int waited = 1;
+          if (lane == 0) waited = mbar_wait(&empty[stage], phase ^ 1u) ? 1 : 0;
+          waited = __shfl_sync(0xFFFFFFFFu, waited, 0);
+          if (!waited) {
+            ok = false;
+            break;
           }
-          next_done = true;
+          if (lane == 0) {
+            const long long off = off0 + (long long)ch * kTmaStageBytes;
+            const uint32_t bytes = (uint32_t)min((long long)kTmaStageBytes, off1 - off);
+            StageMeta& M = meta[stage];
+            M.row = row;
+            M.cls = cur.cls;
+            M.c = cur.c;
+            M.x = cur.x;
+            M.j0 = (int)(off / esize);
+            M.n = (int)(bytes / esize);
+            M.last = (ch == nch - 1) ? 1 : 0;
+            M.tk = cur.tk;
+            M.tp = cur.tp;
+            M.delta = delta;
+            M.r = cur.r;
+            M.pos = cur.pos;
+            M.gamma = cur.gamma;
+            M.c0 = cur.c0;
+            M.part = part;
+            mbar_arrive_expect_tx(&full[stage], bytes);
+            bulk_load(ring + (size_t)stage * kTmaStageBytes, src + off, bytes, &full[stage]);
+          }
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kTmaStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
+        if (!ok) break;
       }
-      if (!next_done) break;
-      row = nrow;
-      cur = next;
+    } else {
+      long long row = blockIdx.x;
+      RowInfo cur;
+      cur.cls = -1;
+      while (row < R) {  // first row with work
+        cur = warp_row_info(P, row, FILT);  // FILT: every row
+        if (cur.cls >= 0) break;
+        row += gridDim.x;
+      }
+      while (row < R && ok) {
+        RowInfo next;
+        next.cls = -1;
+        long long nrow = row + gridDim.x;
+        bool next_done = false;
+        const char* src = (const char*)P.logits + row * row_bytes;
+        const float delta = FILT ? win_delta(cur.c, cur.tk, cur.tp, P.V) : 0.f;
+        for (int ch = 0; ch < nchunks; ++ch) {
+          int waited = 1;
+          if (lane == 0) waited = mbar_wait(&empty[stage], phase ^ 1u) ? 1 : 0;
+          waited = __shfl_sync(0xFFFFFFFFu, waited, 0);
+          if (!waited) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) {
+            const long long off = (long long)ch * kTmaStageBytes;
+            const uint32_t bytes = (uint32_t)min((long long)kTmaStageBytes, row_bytes - off);
+            StageMeta& M = meta[stage];
+            M.row = row;
+            M.cls = cur.cls;
+            M.c = cur.c;
+            M.x = cur.x;
+            M.j0 = (int)(off / esize);
+            M.n = (int)(bytes / esize);
+            M.last = (ch == nchunks - 1) ? 1 : 0;
+            M.tk = cur.tk;
+            M.tp = cur.tp;
+            M.delta = delta;
+            mbar_arrive_expect_tx(&full[stage], bytes);
+            bulk_load(ring + (size_t)stage * kTmaStageBytes, src + off, bytes, &full[stage]);
+          }
+          issued |= 1u << stage;
+          issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+          if (++stage == kTmaStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (ch == 0) {
+            // Look the next row up while this one streams.
+            while (nrow < R) {
+              next = warp_row_info(P, nrow, FILT);
+              if (next.cls >= 0) break;
+              nrow += gridDim.x;
+            }
+            next_done = true;
+          }
+        }
+        if (!next_done) break;
+        row = nrow;
+        cur = next;
+      }
     }
     if (lane == 0) {
       // Every issued copy has landed before the block may exit. This runs
@@ -241,11 +363,14 @@ k_rows_tma(Params P, long long R) {
   __shared__ float red_m[kTmaConsumerWarps], red_s[kTmaConsumerWarps];
   __shared__ int red_i[kTmaConsumerWarps];
   __shared__ float bc_m, s_lx;
+  __shared__ int s_has_lx, s_last_part;
+  __shared__ float s_zfull;
   __shared__ int bc_i;
   __shared__ float fscr[kTmaConsumerWarps];
   __shared__ int iscr[kTmaConsumerWarps];
   const int tid = threadIdx.x;
   constexpr int epc = 16 / esize;
+  if (tid == 0) s_has_lx = 0;
   // Window histogram of the current filtered row (FILT only).
   WinHist* hist = reinterpret_cast<WinHist*>(smem + kTmaHistOffset);
   if (FILT) {
@@ -378,6 +503,7 @@ k_rows_tma(Params P, long long R) {
           for (int e = 1; e < epc; ++e)
             if (e == dx - vx * epc) lx = f[e];
           s_lx = lx;
+          s_has_lx = 1;
         }
       }
     }
@@ -408,19 +534,94 @@ k_rows_tma(Params P, long long R) {
       named_sync(1, kTmaConsumers);
       m = bc_m;
       a = bc_i;
+      float zmerged = 0.f;
+      if (EARLY && P.parts > 1) {
+        // End of one part of the row: publish the part's statistics (and add
+        // its window histogram to the request's global one). The CTA that
+        // ends the row's last part merges them and judges the position.
+        const float mc = m * M.c;
+        float part = 0.f;
+        if (soft && vmax > -INFINITY && m > -INFINITY) part = s * ex2(vmc - mc);
+        part = warp_sum(part);
+        if (lane == 0) red_s[warp] = part;
+        WinHist* ghist = reinterpret_cast<WinHist*>(P.part_hist) + M.r;
+        if (FILT && M.cls == kFiltered) {
+          win_flush(hist, ghist, tid, kTmaConsumers);
+          __threadfence();
+        }
+        named_sync(1, kTmaConsumers);
+        if (tid == 0) {
+          PartStat ps;
+          ps.m = m;
+          ps.z = 0.f;
+          if (soft)
+            for (int w = 0; w < kTmaConsumerWarps; ++w) ps.z += red_s[w];
+          ps.argmax = a;
+          ps.lx = s_has_lx ? s_lx : 0.f;
+          ps.has_lx = s_has_lx;
+          ps.pad[0] = ps.pad[1] = ps.pad[2] = 0;
+          s_has_lx = 0;
+          PartStat* mine = P.part_stats + (size_t)M.r * kMaxParts;
+          mine[M.part] = ps;
+          __threadfence();
+          const unsigned prev = atomicAdd(P.part_done + M.r, 1u);
+          s_last_part = (prev == (unsigned)P.parts - 1u) ? 1 : 0;
+          if (s_last_part) {
+            __threadfence();
+            P.part_done[M.r] = 0u;
+            float mm = -INFINITY, zz = 0.f, lxx = 0.f;
+            int aa = kNoIndex;
+            for (int k = 0; k < P.parts; ++k) {
+              const PartStat q = load_part(mine + k);
+              argmax_combine(mm, aa, q.m, q.argmax);
+              if (q.has_lx) lxx = q.lx;
+            }
+            const float mmc = mm * M.c;
+            for (int k = 0; k < P.parts; ++k) {
+              const PartStat q = load_part(mine + k);
+              if (q.argmax != kNoIndex && q.m > -INFINITY) zz += q.z * ex2(q.m * M.c - mmc);
+            }
+            bc_m = mm;
+            bc_i = aa;
+            s_zfull = zz;
+            s_lx = lxx;
+          }
+        }
+        named_sync(1, kTmaConsumers);
+        if (!s_last_part) {
+          vmax = -INFINITY;
+          vmc = 0.f;
+          s = 0.f;
+          imax = kNoIndex;
+          continue;
+        }
+        m = bc_m;
+        a = bc_i;
+        zmerged = s_zfull;
+        if (FILT && M.cls == kFiltered) {
+          win_take(hist, ghist, tid, kTmaConsumers);
+          named_sync(1, kTmaConsumers);
+        }
+      }
       if (FILT && M.cls == kFiltered) {
         const float mc = m * M.c;
         float part = 0.f;
         if (vmax > -INFINITY && m > -INFINITY) part = s * ex2(vmc - mc);
-        part = warp_sum(part);
-        if (lane == 0) red_s[warp] = part;
-        named_sync(1, kTmaConsumers);
-        float zfull = 0.f;
-        for (int w = 0; w < kTmaConsumerWarps; ++w) zfull += red_s[w];
+        if (!(EARLY && P.parts > 1)) part = warp_sum(part);
+        float zfull = zmerged;
+        if (!(EARLY && P.parts > 1)) {
+          if (lane == 0) red_s[warp] = part;
+          named_sync(1, kTmaConsumers);
+          for (int w = 0; w < kTmaConsumerWarps; ++w) zfull += red_s[w];
+        }
         const HistResult hr = win_finish<kTmaConsumerWarps>(hist, m, M.c, zfull, m - M.delta,
                                                             M.tk, M.tp, P.V, tid, fscr, iscr);
-        if (tid == 0) {
-          if (hr.pending || !(m > -INFINITY)) {
+        const bool unsettled = hr.pending || !(m > -INFINITY);
+        if (unsettled && EARLY) {
+          // The judgement needs this row now: settle it exactly here.
+          filtered_row_stats(P, ConsumerGroup{fscr, iscr}, M.row, M.r);
+        } else if (tid == 0) {
+          if (unsettled) {
             RowStats ps;
             ps.m = m;
             ps.c = M.c;
@@ -437,6 +638,7 @@ k_rows_tma(Params P, long long R) {
                          s_lx);
           }
         }
+        if (EARLY && tid == 0) early_decide(P, M.r, M.pos, M.gamma, M.c0);
         named_sync(1, kTmaConsumers);
         vmax = -INFINITY;
         vmc = 0.f;
@@ -445,16 +647,20 @@ k_rows_tma(Params P, long long R) {
         continue;
       }
       const float mc = m * M.c;
+      const bool merged_row = EARLY && P.parts > 1;
       float part = 0.f;
-      if (soft && vmax > -INFINITY && m > -INFINITY) part = s * ex2(vmc - mc);
-      part = warp_sum(part);
-      if (lane == 0) red_s[warp] = part;
-      named_sync(1, kTmaConsumers);
+      if (!merged_row) {
+        if (soft && vmax > -INFINITY && m > -INFINITY) part = s * ex2(vmc - mc);
+        part = warp_sum(part);
+        if (lane == 0) red_s[warp] = part;
+        named_sync(1, kTmaConsumers);
+      }
       if (tid == 0) {
-        float z = 0.f;
-        if (soft)
+        float z = merged_row ? zmerged : 0.f;
+        if (soft && !merged_row)
           for (int w = 0; w < kTmaConsumerWarps; ++w) z += red_s[w];
         finish_row_x(P, M.row, M.cls, m, a == kNoIndex ? 0 : a, z, -INFINITY, M.c, M.x, s_lx);
+        if (EARLY) early_decide(P, M.r, M.pos, M.gamma, M.c0);
       }
       named_sync(1, kTmaConsumers);
       vmax = -INFINITY;

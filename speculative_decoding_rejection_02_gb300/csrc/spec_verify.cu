@@ -29,6 +29,13 @@ struct spec_verify_handle {
   sv::RaceTask* race_list;
   unsigned* race_count;  // [2]: races listed, rows left to the slow kernel
   long long* pending_rows;
+  long long* queue;      // early exit: [q_cap] items
+  unsigned* queue_ready;  // [q_cap]
+  unsigned* queue_ctl;    // [kQueueCtl]
+  int q_cap;
+  sv::PartStat* part_stats;  // [max_batch x kMaxParts] (NULL: rows are not split)
+  unsigned* part_done;       // [max_batch]
+  void* part_hist;           // [max_batch] WinHist
   unsigned* status;
   int max_slices;
   cudaEvent_t phase[4];
@@ -41,6 +48,29 @@ namespace {
 
 size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Shared-memory sizes of every row-pass instantiation (current device).
+bool set_row_pass_smem() {
+  const int plain = (int)sv::kTmaSmemBytes, filt = (int)sv::kTmaFiltSmemBytes;
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  return cudaFuncSetAttribute(sv::k_rows_tma<true, false>, a, plain) == cudaSuccess &&
+         cudaFuncSetAttribute(sv::k_rows_tma<false, false>, a, plain) == cudaSuccess &&
+         cudaFuncSetAttribute(sv::k_rows_tma<true, true>, a, filt) == cudaSuccess &&
+         cudaFuncSetAttribute(sv::k_rows_tma<true, false, true>, a, plain) == cudaSuccess &&
+         cudaFuncSetAttribute(sv::k_rows_tma<false, false, true>, a, plain) == cudaSuccess &&
+         cudaFuncSetAttribute(sv::k_rows_tma<true, true, true>, a, filt) == cudaSuccess;
+}
+
+// Control words of the early-exit queue, and its slots beyond one per row
+// part: each persistent CTA takes one more ticket than it gets items.
+constexpr size_t kQueueCtl = 4;
+constexpr size_t kQueueSpare = 1024;
+// Early exit splits a row into parts of about this many bytes (at most
+// sv::kMaxParts) so that each judged row spreads over several SMs: rows with
+// top-k / top-p (slow per element) in parts of ~128 KB, the others in parts
+// of ~512 KB (measured: smaller parts only add per-part overhead there).
+constexpr long long kPartTarget = 512 * 1024;
+constexpr long long kPartTargetFiltered = 128 * 1024;
+
 int check_batch(const spec_verify_config* cfg, const spec_verify_batch* b, bool greedy) {
   if (!cfg || !b) return SPEC_ERR_INVALID_ARG;
   if (b->B < 0 || b->N < 0 || b->V < 1) return SPEC_ERR_INVALID_ARG;
@@ -50,9 +80,20 @@ int check_batch(const spec_verify_config* cfg, const spec_verify_batch* b, bool 
     return SPEC_ERR_INVALID_ARG;
   if (b->N > 0 && !b->draft_token_ids) return SPEC_ERR_INVALID_ARG;
   if (!greedy && !b->temperature) return SPEC_ERR_INVALID_ARG;
-  if (!greedy && ((b->flags & ~(SPEC_FLAG_NAIVE | SPEC_FLAG_SAMPLER_MATCH)) ||
-                  ((b->flags & SPEC_FLAG_NAIVE) && (b->flags & SPEC_FLAG_SAMPLER_MATCH))))
-    return SPEC_ERR_INVALID_ARG;
+  if (!greedy) {
+    const unsigned known = SPEC_FLAG_NAIVE | SPEC_FLAG_SAMPLER_MATCH | SPEC_FLAG_EARLY_EXIT;
+    if ((b->flags & ~known) ||
+        ((b->flags & SPEC_FLAG_SAMPLER_MATCH) &&
+         (b->flags & (SPEC_FLAG_NAIVE | SPEC_FLAG_EARLY_EXIT))))
+      return SPEC_ERR_INVALID_ARG;
+    if (b->flags & SPEC_FLAG_EARLY_EXIT) {
+      const long long esize = (b->logits_dtype == SPEC_BF16) ? 2 : 4;
+      const bool aligned = ((long long)b->V * esize) % 16 == 0 &&
+                           (reinterpret_cast<uintptr_t>(b->target_logits) & 15) == 0;
+      const bool filters = b->top_k || b->top_p;
+      if (!aligned || (filters && b->logits_dtype != SPEC_BF16)) return SPEC_ERR_UNSUPPORTED;
+    }
+  }
   if (b->B > cfg->max_batch || b->V > cfg->max_vocab ||
       (long long)b->N + b->B > cfg->max_rows)
     return SPEC_ERR_CAPACITY;
@@ -96,6 +137,16 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   P.race_count = h->race_count;
   P.pending_rows = h->pending_rows;
   P.pending_count = h->race_count + 1;
+  P.early = (!greedy && (b->flags & SPEC_FLAG_EARLY_EXIT)) ? 1 : 0;
+  P.queue = h->queue;
+  P.queue_ready = h->queue_ready;
+  P.queue_ctl = h->queue_ctl;
+  P.q_cap = h->q_cap;
+  P.parts = 1;
+  P.part_bytes = 0;
+  P.part_stats = h->part_stats;
+  P.part_done = h->part_done;
+  P.part_hist = h->part_hist;
   P.status = h->status;
   const int slice = P.bf16 ? sv::kSliceBf16 : sv::kSliceF32;
   P.slices_per_row = (b->V + slice - 1) / slice;
@@ -117,6 +168,59 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   const bool filters = !greedy && (P.top_k || P.top_p);
   P.fast_filtered = (rows_aligned && h->tma_blocks > 0 && h->filt_blocks > 0 && P.bf16 &&
                      filters) ? 1 : 0;
+  if (P.early) {
+    // Rows from the work queue, judged as they finish; no accept kernel.
+    if (!rows_aligned || h->tma_blocks <= 0 || (filters && !P.fast_filtered))
+      return SPEC_ERR_UNSUPPORTED;
+    // Split each row into parts of about the target size (whole stages),
+    // when the workspace has room for it.
+    const long long row_bytes = (long long)b->V * esize;
+    const long long stage = P.fast_filtered ? sv::tma_stage_bytes(true) : sv::tma_stage_bytes(false);
+    const long long target = P.fast_filtered ? kPartTargetFiltered : kPartTarget;
+    int parts = (int)((row_bytes + target - 1) / target);
+    parts = parts < 1 ? 1 : (parts > sv::kMaxParts ? sv::kMaxParts : parts);
+    long long part_bytes = ((row_bytes + parts - 1) / parts + stage - 1) / stage * stage;
+    parts = (int)((row_bytes + part_bytes - 1) / part_bytes);
+    // The queue takes every row part plus one closing ticket per CTA.
+    const long long tickets = (long long)(P.fast_filtered ? h->filt_blocks : h->tma_blocks);
+    if (!h->part_stats || R * parts + tickets > h->q_cap) parts = 1;
+    P.parts = parts;
+    P.part_bytes = parts > 1 ? part_bytes : row_bytes;
+    if (cudaMemsetAsync(h->queue_ctl, 0, kQueueCtl * sizeof(unsigned), stream) != cudaSuccess ||
+        cudaMemsetAsync(h->queue_ready, 0, (size_t)h->q_cap * sizeof(unsigned), stream) !=
+            cudaSuccess)
+      return SPEC_ERR_CUDA;
+    if (parts > 1 &&
+        (cudaMemsetAsync(h->part_done, 0, (size_t)b->B * sizeof(unsigned), stream) != cudaSuccess ||
+         (filters && cudaMemsetAsync(h->part_hist, 0, (size_t)b->B * sizeof(sv::WinHist),
+                                     stream) != cudaSuccess)))
+      return SPEC_ERR_CUDA;
+    sv::k_early_init<<<(b->B + 255) / 256, 256, 0, stream>>>(P);
+    const int blocks = P.fast_filtered ? h->filt_blocks : h->tma_blocks;
+    const long long items = (long long)b->B * parts;  // in flight at most
+    const int grid = items < blocks ? (int)items : blocks;
+    if (P.fast_filtered)
+      sv::k_rows_tma<true, true, true><<<grid, sv::kTmaThreads, sv::kTmaFiltSmemBytes, stream>>>(
+          P, R);
+    else if (P.bf16)
+      sv::k_rows_tma<true, false, true><<<grid, sv::kTmaThreads, sv::kTmaSmemBytes, stream>>>(
+          P, R);
+    else
+      sv::k_rows_tma<false, false, true><<<grid, sv::kTmaThreads, sv::kTmaSmemBytes, stream>>>(
+          P, R);
+    if (timed) {
+      cudaEventRecord(h->phase[1], stream);
+      cudaEventRecord(h->phase[2], stream);
+    }
+    sv::k_race<<<(unsigned)(races * P.race_slices), sv::kRaceThreads,
+                 sv::race_smem_bytes(P.bf16 ? 2 : 4), stream>>>(P);
+    if (timed) cudaEventRecord(h->phase[3], stream);
+    if (cudaPeekAtLastError() != cudaSuccess) {
+      cudaGetLastError();
+      return SPEC_ERR_CUDA;
+    }
+    return SPEC_OK;
+  }
   if (P.fast_filtered) {
     // One pass over every row; the filtered rows it cannot settle are listed.
     const long long fgrid = R < h->filt_blocks ? R : h->filt_blocks;
@@ -183,22 +287,14 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   h->sm_count = prop.multiProcessorCount;
   int per_sm = 0;
   int filt_per_sm = 0;
-  if (cudaFuncSetAttribute(sv::k_rows_tma<true, false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)sv::kTmaSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(sv::k_rows_tma<false, false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)sv::kTmaSmemBytes) != cudaSuccess ||
+  if (!set_row_pass_smem() ||
       cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv::k_rows_tma<true, false>,
                                                     sv::kTmaThreads,
                                                     sv::kTmaSmemBytes) != cudaSuccess) {
     cudaGetLastError();
     per_sm = 0;
   }
-  if (cudaFuncSetAttribute(sv::k_rows_tma<true, true>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)sv::kTmaFiltSmemBytes) != cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&filt_per_sm, sv::k_rows_tma<true, true>,
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&filt_per_sm, sv::k_rows_tma<true, true>,
                                                     sv::kTmaThreads,
                                                     sv::kTmaFiltSmemBytes) != cudaSuccess) {
     cudaGetLastError();
@@ -224,9 +320,17 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   const size_t sz_list = align_up(n_rows * sizeof(sv::RaceTask));
   const size_t sz_lcnt = align_up(2 * sizeof(unsigned));
   const size_t sz_pend = align_up(n_rows * sizeof(long long));
+  const size_t qcap = n_rows * sv::kMaxParts + kQueueSpare;
+  const size_t sz_queue = align_up(qcap * sizeof(long long));
+  const size_t sz_qready = align_up(qcap * sizeof(unsigned));
+  const size_t sz_qctl = align_up(kQueueCtl * sizeof(unsigned));
+  const size_t sz_pstat = align_up(n_b * sv::kMaxParts * sizeof(sv::PartStat));
+  const size_t sz_pdone = align_up(n_b * sizeof(unsigned));
+  const size_t sz_phist = align_up(n_b * sizeof(sv::WinHist));
   const size_t sz_stat = align_up(sizeof(unsigned));
   const size_t total = sz_rows + sz_part + sz_rcnt + sz_race + sz_best + sz_rccnt + sz_list +
-                       sz_lcnt + sz_pend + sz_stat;
+                       sz_lcnt + sz_pend + sz_queue + sz_qready + sz_qctl + sz_pstat + sz_pdone +
+                       sz_phist + sz_stat;
   if (cudaMalloc(&h->ws, total) != cudaSuccess) {
     delete h;
     return SPEC_ERR_CUDA;
@@ -246,6 +350,13 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   h->race_list = (sv::RaceTask*)p; p += sz_list;
   h->race_count = (unsigned*)p; p += sz_lcnt;
   h->pending_rows = (long long*)p; p += sz_pend;
+  h->queue = (long long*)p; p += sz_queue;
+  h->queue_ready = (unsigned*)p; p += sz_qready;
+  h->queue_ctl = (unsigned*)p; p += sz_qctl;
+  h->q_cap = (int)qcap;
+  h->part_stats = (sv::PartStat*)p; p += sz_pstat;
+  h->part_done = (unsigned*)p; p += sz_pdone;
+  h->part_hist = p; p += sz_phist;
   h->status = (unsigned*)p;
   *out = h;
   return SPEC_OK;
@@ -330,7 +441,12 @@ constexpr size_t kNaOffRccnt = kNaOffBest + na_align(kNaRows * sizeof(unsigned l
 constexpr size_t kNaOffList = kNaOffRccnt + na_align(kNaRows * sizeof(unsigned));
 constexpr size_t kNaOffLcnt = kNaOffList + na_align(kNaRows * sizeof(sv::RaceTask));
 constexpr size_t kNaOffPend = kNaOffLcnt + na_align(2 * sizeof(unsigned));
-constexpr size_t kNaOffStat = kNaOffPend + na_align(kNaRows * sizeof(long long));
+// Early exit without row parts: one queue slot per row, plus the spare.
+constexpr size_t kNaQueueCap = kNaRows + kQueueSpare;
+constexpr size_t kNaOffQueue = kNaOffPend + na_align(kNaRows * sizeof(long long));
+constexpr size_t kNaOffQready = kNaOffQueue + na_align(kNaQueueCap * sizeof(long long));
+constexpr size_t kNaOffQctl = kNaOffQready + na_align(kNaQueueCap * sizeof(unsigned));
+constexpr size_t kNaOffStat = kNaOffQctl + na_align(kQueueCtl * sizeof(unsigned));
 constexpr size_t kNaBytes = kNaOffStat + na_align(sizeof(unsigned));
 static_assert(kNaBytes <= SPEC_NOALLOC_SCRATCH_BYTES, "no-allocation scratch too small");
 
@@ -381,15 +497,7 @@ extern "C" int spec_verify_run_noalloc(const spec_verify_batch* b, void* stream,
         return SPEC_ERR_CUDA;
       }
       int per_sm = 0, filt_per_sm = 0;
-      if (cudaFuncSetAttribute(sv::k_rows_tma<true, false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)sv::kTmaSmemBytes) != cudaSuccess ||
-          cudaFuncSetAttribute(sv::k_rows_tma<false, false>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)sv::kTmaSmemBytes) != cudaSuccess ||
-          cudaFuncSetAttribute(sv::k_rows_tma<true, true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)sv::kTmaFiltSmemBytes) != cudaSuccess ||
+      if (!set_row_pass_smem() ||
           cudaFuncSetAttribute(sv::k_race, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)sv::race_smem_bytes(4)) != cudaSuccess ||
           cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv::k_rows_tma<true, false>,
@@ -426,6 +534,10 @@ extern "C" int spec_verify_run_noalloc(const spec_verify_batch* b, void* stream,
   h.race_list = (sv::RaceTask*)(nd.base + kNaOffList);
   h.race_count = (unsigned*)(nd.base + kNaOffLcnt);
   h.pending_rows = (long long*)(nd.base + kNaOffPend);
+  h.queue = (long long*)(nd.base + kNaOffQueue);
+  h.queue_ready = (unsigned*)(nd.base + kNaOffQready);
+  h.queue_ctl = (unsigned*)(nd.base + kNaOffQctl);
+  h.q_cap = (int)kNaQueueCap;
   h.status = device_status ? device_status : (unsigned*)(nd.base + kNaOffStat);
   h.max_slices = (int)kNaSlices;
   h.n_phase = 0;

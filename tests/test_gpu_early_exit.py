@@ -1,0 +1,119 @@
+"""Early-exit verification on the GPU (velog "드래프트가 제안하고 타깃이
+판정한다": the first rejection ends the round), through the C ABI, against
+the oracle under the same flag and against the GPU's own full pass."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from parity import assert_parity, check_structure, compare, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _early(b):
+    b = dict(b)
+    b["flags"] = int(b.get("flags", 0)) | oracle.FLAG_EARLY_EXIT
+    return b
+
+
+def _unread_are_nan(b, out):
+    cu = b["cu_num_draft"]
+    for r in range(b["B"]):
+        c0, c1 = int(cu[r]), int(cu[r + 1])
+        k = int(out["num_accepted"][r])
+        assert np.all(np.isnan(out["p_at_draft"][c0 + k + 1:c1])), r
+
+
+@pytest.mark.parametrize("name,B,V", [
+    ("c2", None, None),      # fp32 rows, no filters
+    ("c2", 6, 32008),        # fp32, ragged tail inside the last stage
+    ("c3", 27, 40000),       # every temperature / filter combination
+    ("c4", 24, 50000),       # one-hot drafts, top-p
+    ("c5", 40, 70000),
+    ("c5", 33, 65536),
+])
+def test_scaled_workloads(name, B, V):
+    b = _early(synth.make(name, B=B, V=V))
+    gpu = run_gpu(b)
+    ref = oracle.verify(b)
+    assert gpu["status"] == 0
+    check_structure(b, gpu)
+    assert_parity(compare(b, gpu, ref))
+    _unread_are_nan(b, gpu)
+
+
+@pytest.mark.parametrize("name", ["c3", "c4", "c5"])
+def test_same_round_as_the_full_pass(name):
+    b = synth.make(name, B=64 if name != "c3" else None, V=None)
+    full = run_gpu(b)
+    early = run_gpu(_early(b))
+    assert early["status"] == 0
+    assert np.array_equal(full["out_tokens"], early["out_tokens"])
+    assert np.array_equal(full["num_accepted"], early["num_accepted"])
+    cu = b["cu_num_draft"]
+    for r in range(b["B"]):
+        c0, c1 = int(cu[r]), int(cu[r + 1])
+        upto = min(int(full["num_accepted"][r]) + 1, c1 - c0)
+        # a row split over several CTAs sums Z in another order: last bits
+        assert np.allclose(full["p_at_draft"][c0:c0 + upto], early["p_at_draft"][c0:c0 + upto],
+                           rtol=1e-5, atol=0)
+
+
+@pytest.mark.parametrize("name,n_sample", [("c4", 12), ("c5", 16)])
+def test_full_size_sampled(name, n_sample):
+    b = _early(synth.make(name))
+    gpu = run_gpu(b)
+    assert gpu["status"] == 0
+    check_structure(b, gpu)
+    reqs = np.sort(np.random.default_rng(11).choice(b["B"], size=n_sample, replace=False))
+    ref = oracle.verify(b, requests=reqs)
+    assert_parity(compare(b, gpu, ref, requests=reqs))
+
+
+def test_rows_after_the_stop_are_never_read():
+    b = synth.make("c3", B=36, V=4000)
+    clean = run_gpu(b)
+    cu = b["cu_num_draft"]
+    t = b["target_logits"].copy()
+    planted = []
+    for r in range(b["B"]):
+        c0, c1 = int(cu[r]), int(cu[r + 1])
+        k = int(clean["num_accepted"][r])
+        if k + 1 <= c1 - c0:
+            t[c0 + r + k + 1, 5] = 0x7FC0  # bf16 NaN in the first row after the stop
+            planted.append(r)
+    assert len(planted) > 5
+    nb = dict(b)
+    nb["target_logits"] = t
+    early = run_gpu(_early(nb))
+    assert early["status"] == 0  # the NaN rows were never read
+    assert np.array_equal(early["out_tokens"], clean["out_tokens"])
+    assert np.array_equal(early["num_accepted"], clean["num_accepted"])
+    full = run_gpu(nb)
+    assert full["status"] & 0x1  # the full pass reads them
+
+
+def test_edge_rounds():
+    # gamma = 0 requests, a long round, T = 0 and T > 0 mixed, unusable row at the stop
+    rng = np.random.default_rng(5)
+    V = 1024
+    gam = np.array([0, 3, 40, 1, 0, 5, 2])
+    B = gam.size
+    cu = np.concatenate([[0], np.cumsum(gam)]).astype(np.int32)
+    N = int(cu[-1])
+    logits = rng.normal(0, 2, size=(N + B, V)).astype(np.float32)
+    ids = np.empty(N, np.int32)
+    for r in range(B):
+        for i in range(int(gam[r])):
+            ids[cu[r] + i] = int(np.argmax(logits[cu[r] + r + i]))  # argmax drafts: long rounds
+    logits[cu[5] + 5 + 0, 3] = np.inf  # request 5 is voided at its first row
+    b = dict(B=B, V=V, cu_num_draft=cu, draft_token_ids=ids,
+             target_logits=synth.f32_to_bf16_bits(logits), logits_dtype="bf16", draft_probs=None,
+             temperature=np.array([1, 0, 1, 0.7, 0, 1, 1], np.float32), top_k=None, top_p=None,
+             seed=9, request_base=0, flags=oracle.FLAG_EARLY_EXIT)
+    gpu = run_gpu(b)
+    ref = oracle.verify(b)
+    assert gpu["status"] & 0x1
+    assert_parity(compare(b, gpu, ref))
+    assert gpu["num_accepted"][5] == 0 and np.all(gpu["out_tokens"][cu[5] + 5:cu[6] + 6] == -1)
