@@ -75,6 +75,9 @@ extern "C" {
 #define SPEC_STATUS_BAD_OFFSETS 0x10u   /* cu_num_draft not 0 .. N, non-decreasing */
 #define SPEC_STATUS_TIMEOUT 0x20u       /* an on-chip pipeline wait gave up (the
                                            outputs of the call are not valid) */
+#define SPEC_STATUS_UNSETTLED 0x40u     /* vocab-sharded call: a top-k / top-p row
+                                           the window histogram could not settle;
+                                           its request emits nothing */
 
 /* Batch flags. */
 #define SPEC_FLAG_NAIVE 0x1u /* negative control: resample rejected positions
@@ -247,6 +250,87 @@ void spec_verify_destroy(spec_verify_handle* h);
 
 /* spec_verify_strerror — static description of a return code. */
 const char* spec_verify_strerror(int code);
+
+/*
+ * ---------------------------------------------------------------------------
+ * Vocab-sharded (tensor-parallel) verification.
+ *
+ * The verification of one batch when each of n ranks holds the target
+ * logits (and draft probabilities) of a contiguous slice of the vocabulary
+ * only. It computes what spec_verify_run computes (velog sections above):
+ * the row statistics are sums, maxima and a value histogram, so they
+ * combine across slices; the exponential race is a maximum of w_j / E_j with
+ * E_j keyed by the global index j, so each rank races its own columns and
+ * the winners combine by a maximum. Between the calls below the caller
+ * all-reduces the named spec_shard arrays over the n ranks (NCCL, gloo),
+ * in this order:
+ *   spec_verify_shard_rows      then all-reduce MAX: m
+ *   spec_verify_shard_rescale   then all-reduce SUM: z, qx, hist, hist_w;
+ *                                    MIN: argmax; MAX: lx
+ *   spec_verify_shard_judge     then all-reduce MAX: best
+ *   spec_verify_shard_race_p    then all-reduce MAX: best_p
+ *   spec_verify_shard_emit      (out_tokens, num_accepted as spec_verify_run)
+ * Every rank passes the same cu_num_draft, draft_token_ids (global ids),
+ * temperature, top_k, top_p, seed and request_base; b->V is the local
+ * slice width and target_logits / draft_probs hold the local columns
+ * ([(N+B) x V] and [N x V]). Requirements: 16-byte aligned local rows
+ * (b->V * element size a multiple of 16, aligned base), v0 a multiple of 4,
+ * bf16 logits when top_k / top_p are given, no flags; otherwise
+ * SPEC_ERR_UNSUPPORTED. A top-k / top-p row whose thresholds the window
+ * histogram cannot settle (a threshold on a value of magnitude below 2^-16
+ * or at least 2^8, or a top-k set reaching more than 30 / c below the max)
+ * sets SPEC_STATUS_UNSETTLED and its request emits nothing. The caller owns
+ * every array; all are device memory. The handle keeps state between the
+ * five calls of one batch: one batch at a time per handle, same stream.
+ * ---------------------------------------------------------------------------
+ */
+#define SPEC_SHARD_HIST_INTS 6148 /* ints per row of spec_shard.hist */
+
+typedef struct {
+  long long v0;        /* global index of the first local column */
+  int V_global;        /* the full vocabulary size */
+  float* m;            /* [N+B] local row max; the caller makes it the global max */
+  float* z;            /* [N+B] sum of 2^((l - m) log2(e) / T) over the local columns
+                          (T > 0 rows), rescaled to the global max by
+                          spec_verify_shard_rescale */
+  int* argmax;         /* [N+B] lowest global index of the local max; after the
+                          rescale INT_MAX unless the local max is the global one */
+  float* lx;           /* [N+B] logit at the row's draft token when it is a local
+                          column, else -inf */
+  float* qx;           /* [N] q(x) when x is a local column, else 0; NULL when
+                          draft_probs is NULL */
+  int* hist;           /* [(N+B) x SPEC_SHARD_HIST_INTS] window histogram counts of
+                          top-k / top-p rows (NULL when the batch has no top_k and
+                          no top_p) */
+  float* hist_w;       /* [(N+B) x 2] weights of its two merged counters (NULL as hist) */
+  unsigned long long* best;    /* [B] race winner of the local columns, (score bits
+                                  << 32) | (0xFFFFFFFF - global index); 0: none */
+  unsigned long long* best_p;  /* [B] the race on p for requests whose combined best
+                                  is 0 (every residual weight 0); 0 otherwise */
+} spec_shard;
+
+/* spec_verify_shard_rows — local row statistics and window histograms of
+ * the local columns. Same returns as spec_verify_run. */
+int spec_verify_shard_rows(spec_verify_handle* h, const spec_verify_batch* b,
+                           const spec_shard* sh, void* stream);
+/* spec_verify_shard_rescale — with sh->m holding the global maxima: rescale
+ * z to them, keep argmax only where the local max is the global one, gather
+ * q(x) of local draft tokens into qx. */
+int spec_verify_shard_rescale(spec_verify_handle* h, const spec_verify_batch* b,
+                              const spec_shard* sh, void* stream);
+/* spec_verify_shard_judge — from the combined statistics: the rows'
+ * thresholds and Z, the accept scan (num_accepted and the accepted tokens
+ * are final here), and the race over the local columns into best. */
+int spec_verify_shard_judge(spec_verify_handle* h, const spec_verify_batch* b,
+                            const spec_shard* sh, void* stream);
+/* spec_verify_shard_race_p — for requests whose combined best is 0, the
+ * race over p of the local columns into best_p (0 for the others). */
+int spec_verify_shard_race_p(spec_verify_handle* h, const spec_verify_batch* b,
+                             const spec_shard* sh, void* stream);
+/* spec_verify_shard_emit — write each request's recovered / bonus token
+ * from the combined best (best_p where best is 0). */
+int spec_verify_shard_emit(spec_verify_handle* h, const spec_verify_batch* b,
+                           const spec_shard* sh, void* stream);
 
 #ifdef __cplusplus
 }

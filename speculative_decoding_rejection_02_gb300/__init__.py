@@ -27,6 +27,9 @@ STATUS_BAD_TOKEN = 0x4
 STATUS_EMPTY_RESIDUAL = 0x8
 STATUS_BAD_OFFSETS = 0x10
 STATUS_TIMEOUT = 0x20
+STATUS_UNSETTLED = 0x40
+
+SHARD_HIST_INTS = 6148  # ints per row of the sharded window histogram
 
 FLAG_NAIVE = 0x1
 FLAG_SAMPLER_MATCH = 0x2
@@ -37,7 +40,11 @@ ENTRY_POINTS = (
     "spec_verify_init", "spec_verify_run", "spec_verify_greedy", "spec_verify_status",
     "spec_verify_check_batch", "spec_verify_set_phase_events", "spec_verify_run_noalloc",
     "spec_verify_destroy", "spec_verify_strerror",
+    "spec_verify_shard_rows", "spec_verify_shard_rescale", "spec_verify_shard_judge",
+    "spec_verify_shard_race_p", "spec_verify_shard_emit",
 )
+
+_SHARD_CALLS = ENTRY_POINTS[-5:]
 
 
 class SpecVerifyError(RuntimeError):
@@ -60,6 +67,15 @@ class Batch(C.Structure):
         ("top_k", C.c_void_p), ("top_p", C.c_void_p),
         ("seed", C.c_ulonglong), ("request_base", C.c_longlong), ("flags", C.c_uint),
         ("out_tokens", C.c_void_p), ("num_accepted", C.c_void_p), ("p_at_draft", C.c_void_p),
+    ]
+
+
+class Shard(C.Structure):
+    _fields_ = [
+        ("v0", C.c_longlong), ("V_global", C.c_int),
+        ("m", C.c_void_p), ("z", C.c_void_p), ("argmax", C.c_void_p), ("lx", C.c_void_p),
+        ("qx", C.c_void_p), ("hist", C.c_void_p), ("hist_w", C.c_void_p),
+        ("best", C.c_void_p), ("best_p", C.c_void_p),
     ]
 
 
@@ -92,6 +108,9 @@ def lib():
             L.spec_verify_destroy.restype = None
             L.spec_verify_strerror.argtypes = [C.c_int]
             L.spec_verify_strerror.restype = C.c_char_p
+            for name in _SHARD_CALLS:
+                getattr(L, name).argtypes = [C.c_void_p, C.POINTER(Batch), C.POINTER(Shard),
+                                             C.c_void_p]
             for name in ENTRY_POINTS:
                 getattr(L, name)  # raises if the library lacks a declared symbol
             _lib = L
@@ -215,6 +234,14 @@ class Verifier:
                "spec_verify_greedy")
         return b
 
+    def shard(self, step: str, b: DeviceBatch, sh: "ShardBuffers", stream=None):
+        """One step of a vocab-sharded call: "rows", "rescale", "judge",
+        "race_p" or "emit" (the caller all-reduces in between; see tp.py)."""
+        name = f"spec_verify_shard_{step}"
+        s, shs = b.struct(), sh.struct()
+        _check(getattr(self._lib, name)(self._h, C.byref(s), C.byref(shs), self._stream(stream)),
+               name)
+
     def status(self) -> int:
         bits = C.c_uint(0)
         rc = self._lib.spec_verify_status(self._h, C.byref(bits))
@@ -246,6 +273,34 @@ class Verifier:
             self.close()
         except Exception:
             pass
+
+
+class ShardBuffers:
+    """Device arrays exchanged between the ranks of a vocab-sharded call."""
+
+    def __init__(self, b: DeviceBatch, v0: int, V_global: int, filters: bool):
+        import torch
+        dev = b.target_logits.device
+        R, N, B = b.N + b.B, b.N, b.B
+        self.v0, self.V_global = int(v0), int(V_global)
+        self.m = torch.empty(R, dtype=torch.float32, device=dev)
+        self.z = torch.empty(R, dtype=torch.float32, device=dev)
+        self.argmax = torch.empty(R, dtype=torch.int32, device=dev)
+        self.lx = torch.empty(R, dtype=torch.float32, device=dev)
+        self.qx = (torch.empty(max(N, 1), dtype=torch.float32, device=dev)
+                   if b.draft_probs is not None else None)
+        self.hist = (torch.empty((R, SHARD_HIST_INTS), dtype=torch.int32, device=dev)
+                     if filters else None)
+        self.hist_w = torch.empty((R, 2), dtype=torch.float32, device=dev) if filters else None
+        # (score bits << 32) | ~index: non-negative as int64, so MAX combines them
+        self.best = torch.empty(max(B, 1), dtype=torch.int64, device=dev)
+        self.best_p = torch.empty(max(B, 1), dtype=torch.int64, device=dev)
+
+    def struct(self) -> Shard:
+        return Shard(v0=self.v0, V_global=self.V_global, m=_ptr(self.m), z=_ptr(self.z),
+                     argmax=_ptr(self.argmax), lx=_ptr(self.lx), qx=_ptr(self.qx),
+                     hist=_ptr(self.hist), hist_w=_ptr(self.hist_w), best=_ptr(self.best),
+                     best_p=_ptr(self.best_p))
 
 
 def check_batch(cfg: Config, b: Batch) -> int:

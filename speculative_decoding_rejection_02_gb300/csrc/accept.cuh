@@ -110,7 +110,8 @@ k_accept(Params P) {
   unsigned st = 0;
   for (int i = lane; i <= gamma; i += 32) st |= P.rows[row0 + i].status;
   st = __reduce_or_sync(0xFFFFFFFFu, st);
-  if (!greedy && (st & (SPEC_STATUS_NONFINITE | SPEC_STATUS_NO_FINITE))) {
+  if (!greedy &&
+      (st & (SPEC_STATUS_NONFINITE | SPEC_STATUS_NO_FINITE | SPEC_STATUS_UNSETTLED))) {
     // Unusable target row: nothing is emitted for this request.
     for (int i = lane; i <= gamma; i += 32) P.out_tokens[row0 + i] = -1;
     if (P.p_at_draft)
@@ -135,7 +136,7 @@ k_accept(Params P) {
     bool ok = true;
     if (i < gamma) {
       const int x = __ldg(P.ids + c0 + i);
-      const bool valid = (x >= 0 && x < P.V);
+      const bool valid = (x >= 0 && x < P.Vg);
       bad_tok |= valid ? 0u : 1u;
       const RowStats s = P.rows[row0 + i];
       float pa;
@@ -144,8 +145,10 @@ k_accept(Params P) {
         pa = ok ? 1.f : 0.f;
       } else {
         pa = s.p_x;
-        const float qx =
-            P.q ? (valid ? __ldg(P.q + (long long)(c0 + i) * P.V + x) : 0.f) : 1.f;
+        // q(x): gathered here, or combined across the ranks of a sharded call
+        const float qx = !P.q ? 1.f
+                         : P.shard ? P.sh_qx[c0 + i]
+                         : (valid ? __ldg(P.q + (long long)(c0 + i) * P.V + x) : 0.f);
         if (k == gamma) {
           const double u = accept_uniform(P.seed, greq, i);
           ok = (qx > 0.f) && ((double)pa / (double)qx >= u);
@@ -176,7 +179,7 @@ k_accept(Params P) {
         d.x = x;
         if (P.flags & SPEC_FLAG_NAIVE) d.mode = kRaceP;
         else if (P.q) d.mode = kRaceResidual;
-        else d.mode = (x >= 0 && x < P.V) ? kRaceMasked : kRaceP;
+        else d.mode = (x >= 0 && x < P.Vg) ? kRaceMasked : kRaceP;
       } else {
         d.mode = kRaceP;
       }

@@ -128,6 +128,19 @@ struct Params {
   void* part_hist;          // [max_batch] WinHist: merged window histograms
   int slices_per_row;
   int race_slices;
+  // Vocab-sharded calls: the local columns are global v0 .. v0 + V - 1.
+  int v0;                    // 0 otherwise
+  int Vg;                    // the full vocabulary (V otherwise)
+  int shard;                 // 1 in a sharded call
+  float* sh_m;
+  float* sh_z;
+  int* sh_arg;
+  float* sh_lx;
+  float* sh_qx;
+  int* sh_hist;              // [R x SPEC_SHARD_HIST_INTS]
+  float* sh_hist_w;          // [R x 2]
+  unsigned long long* sh_best;    // race output of a sharded call
+  const unsigned long long* sh_skip;  // race on p only where this combined best is 0
 };
 
 // ---------------------------------------------------------------------------

@@ -46,9 +46,11 @@ __host__ __device__ constexpr size_t race_smem_bytes(int logit_bytes) {
 
 // What the scoring needs about the race row.
 struct RaceView {
-  int V, row, qrow, kstar, mode, x;
+  int V, row, qrow, kstar, mode, x;  // V, x: local columns (x = -1: none)
   float c, mc, inv_z, theta, z;
   long long greq;
+  int v0;        // global index of local column 0 (vocab-sharded calls; else 0)
+  uint32_t g0;   // v0 / 4: the Philox draw of local group g is draw g0 + g
 };
 
 __device__ __forceinline__ RaceView race_view(const Params& P, int r, int row, int qrow,
@@ -60,7 +62,9 @@ __device__ __forceinline__ RaceView race_view(const Params& P, int r, int row, i
   v.qrow = qrow;
   v.kstar = kstar;
   v.mode = mode;
-  v.x = x;
+  v.x = (x >= P.v0 && x - P.v0 < P.V) ? x - P.v0 : -1;
+  v.v0 = P.v0;
+  v.g0 = (uint32_t)P.v0 >> 2;
   v.c = c;
   v.mc = m * c;
   v.inv_z = inv_z;
@@ -102,17 +106,18 @@ __device__ __forceinline__ float race_logit_floor(const RaceView& v, float best)
   return fmaxf(t, nextafterf(v.theta, -INFINITY));
 }
 
-// One candidate entry j, scored exactly as the race scores it: the packed
-// (score, ~j), or 0 when w_j = 0.
-__device__ unsigned long long race_candidate(const Params& P, const RaceView& v, int j) {
+// One candidate entry, global index jg, scored exactly as the race scores
+// it: the packed (score, ~jg), or 0 when it is not a local column or w = 0.
+__device__ unsigned long long race_candidate(const Params& P, const RaceView& v, int jg) {
+  const int j = jg - v.v0;
   if (j < 0 || j >= P.V || !(v.z > 0.f)) return 0ull;
   const float l = load_logit(P, v.row, j);
   const float q = (v.mode == kRaceResidual) ? __ldg(P.q + (long long)v.qrow * P.V + j) : 0.f;
   const float w = race_w(race_p(l, v), q, j, v.mode, v.x);
   if (!(w > 0.f)) return 0ull;
-  const uint4 r = race_words(P.seed, v.greq, v.kstar, (uint32_t)j >> 2);
+  const uint4 r = race_words(P.seed, v.greq, v.kstar, v.g0 + ((uint32_t)j >> 2));
   const uint32_t words[4] = {r.x, r.y, r.z, r.w};
-  return race_pack(race_score(w, words[j & 3]), j);
+  return race_pack(race_score(w, words[j & 3]), jg);
 }
 
 struct RaceItem {
@@ -163,7 +168,7 @@ __device__ __forceinline__ void race_batch(const Params& P, const RaceView& v, i
   __syncwarp();
   for (int t = lane; t < n_items; t += 32) {
     const RaceItem it = qw[t];
-    const uint4 r = race_words(P.seed, v.greq, v.kstar, it.g);
+    const uint4 r = race_words(P.seed, v.greq, v.kstar, v.g0 + it.g);
     const uint32_t words[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -232,8 +237,12 @@ k_race(Params P) {
   const RaceTask task = P.race_list[t % n_race];
   const int r = task.r;
   const int slot = task.slot;
-  const RaceView v = race_view(P, r, task.row, task.qrow, task.kstar, task.mode, task.x, task.m,
-                               task.c, task.inv_z, task.theta, task.z);
+  // Second race of a sharded call: only where every residual weight was 0,
+  // and on p.
+  if (P.sh_skip && P.sh_skip[r] != 0ull) return;
+  const RaceView v = race_view(P, r, task.row, task.qrow, task.kstar,
+                               P.sh_skip ? (int)kRaceP : task.mode, task.x, task.m, task.c,
+                               task.inv_z, task.theta, task.z);
   const int V = P.V;
   const uint32_t groups = (uint32_t)((V + 3) / 4);
   const uint32_t g0 = (uint32_t)slice * (kRaceSlice / 4);
@@ -274,10 +283,11 @@ k_race(Params P) {
     }
   }
 
-  // The best so far (seeded by the accept scan, raised by earlier slices).
+  // The best so far (seeded by the accept scan, raised by earlier slices);
+  // packed with global indices, kept here as local ones.
   const unsigned long long lb = __ldcg(P.race_best + slot);
   float best = lb ? __uint_as_float((uint32_t)(lb >> 32)) : 0.f;
-  int best_j = lb ? (int)(0xFFFFFFFFu - (uint32_t)lb) : kNoIndex;
+  int best_j = lb ? (int)(0xFFFFFFFFu - (uint32_t)lb) - v.v0 : kNoIndex;
   if (v.z > 0.f) {
     if (staged && best_j == kNoIndex) {
       // No bound yet (the argmax token had weight 0 and no earlier slice has
@@ -303,7 +313,7 @@ k_race(Params P) {
       }
       block_argmax(wb, jb);
       if (jb != kNoIndex && wb > 0.f) {
-        const uint4 rw = race_words(P.seed, v.greq, v.kstar, (uint32_t)jb >> 2);
+        const uint4 rw = race_words(P.seed, v.greq, v.kstar, v.g0 + ((uint32_t)jb >> 2));
         const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
         best = race_score(wb, words[jb & 3]);
         best_j = jb;
@@ -360,7 +370,8 @@ k_race(Params P) {
   }
   block_argmax(best, best_j);
   if (threadIdx.x == 0) {
-    if (best_j != kNoIndex && best > 0.f) atomicMax(P.race_best + slot, race_pack(best, best_j));
+    if (best_j != kNoIndex && best > 0.f)
+      atomicMax(P.race_best + slot, race_pack(best, best_j + v.v0));
     __threadfence();
     const unsigned prev = atomicAdd(P.race_counter + slot, 1u);
     s_last = (prev == (unsigned)P.race_slices - 1u);
@@ -373,6 +384,11 @@ k_race(Params P) {
   }
   __syncthreads();
   const unsigned long long packed = s_packed;
+  if (P.shard) {
+    // Sharded call: this rank's winner, combined across ranks by the caller.
+    if (threadIdx.x == 0) P.sh_best[r] = packed;
+    return;
+  }
   int tok;
   if (packed == 0ull) {
     // Every weight was 0 (rounding only): draw from p over the whole row.

@@ -56,7 +56,7 @@ __device__ void finish_row_x(const Params& P, long long row, int cls, float m, i
     else if (m == -INFINITY) st |= SPEC_STATUS_NO_FINITE;
   }
   float p_x = 0.f;
-  if (x >= 0 && x < P.V) {
+  if (x >= 0 && x < P.Vg) {
     if (cls == kArgmaxOnly) {
       p_x = (x == argmax) ? 1.f : 0.f;
     } else if (st == 0) {

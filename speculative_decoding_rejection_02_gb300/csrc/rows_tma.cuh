@@ -190,7 +190,10 @@ struct ConsumerGroup {
 // hist.cuh, and rows it cannot settle are listed for the slow kernel.
 // EARLY: rows come from the early-exit work queue (early.cuh) and each row's
 // position is judged at its end.
-template <bool BF16, bool FILT, bool EARLY = false>
+// SHARD: the rows hold one rank's columns of a vocab-sharded call; the row
+// end exports the local statistics (and window histogram) instead of
+// finishing the row (shard.cuh combines them).
+template <bool BF16, bool FILT, bool EARLY = false, bool SHARD = false>
 __global__ void __launch_bounds__(kTmaThreads, 2)
 k_rows_tma(Params P, long long R) {
   static_assert(!FILT || BF16, "the histogram path is for bf16 rows");
@@ -234,7 +237,7 @@ k_rows_tma(Params P, long long R) {
         const int part = (int)(item & 7);
         const RowInfo cur = warp_row_info(P, row, true);
         const char* src = (const char*)P.logits + row * row_bytes;
-        const float delta = FILT ? win_delta(cur.c, cur.tk, cur.tp, P.V) : 0.f;
+        const float delta = FILT ? win_delta(cur.c, cur.tk, cur.tp, P.Vg) : 0.f;
         const long long off0 = (long long)part * P.part_bytes;
         const long long off1 = min(off0 + P.part_bytes, row_bytes);
         const int nch = (int)((off1 - off0 + kTmaStageBytes - 1) / kTmaStageBytes);
@@ -292,7 +295,10 @@ k_rows_tma(Params P, long long R) {
         long long nrow = row + gridDim.x;
         bool next_done = false;
         const char* src = (const char*)P.logits + row * row_bytes;
-        const float delta = FILT ? win_delta(cur.c, cur.tk, cur.tp, P.V) : 0.f;
+        const float delta = FILT ? win_delta(cur.c, cur.tk, cur.tp, P.Vg) : 0.f;
+        // the draft token as a local column (-1: another rank's)
+        const int xl = SHARD ? ((cur.x >= P.v0 && cur.x - P.v0 < P.V) ? cur.x - P.v0 : -1)
+                             : cur.x;
         for (int ch = 0; ch < nchunks; ++ch) {
           int waited = 1;
           if (lane == 0) waited = mbar_wait(&empty[stage], phase ^ 1u) ? 1 : 0;
@@ -308,7 +314,7 @@ k_rows_tma(Params P, long long R) {
             M.row = row;
             M.cls = cur.cls;
             M.c = cur.c;
-            M.x = cur.x;
+            M.x = xl;
             M.j0 = (int)(off / esize);
             M.n = (int)(bytes / esize);
             M.last = (ch == nchunks - 1) ? 1 : 0;
@@ -534,6 +540,53 @@ k_rows_tma(Params P, long long R) {
       named_sync(1, kTmaConsumers);
       m = bc_m;
       a = bc_i;
+      if constexpr (SHARD) {
+        // Local statistics of this rank's columns (global indices).
+        const float mc = m * M.c;
+        float part = 0.f;
+        if (soft && vmax > -INFINITY && m > -INFINITY) part = s * ex2(vmc - mc);
+        part = warp_sum(part);
+        if (lane == 0) red_s[warp] = part;
+        if (FILT && M.cls == kFiltered) {
+          int* hout = P.sh_hist + M.row * (long long)SPEC_SHARD_HIST_INTS;
+          for (int i = tid; i < kWinItems; i += kTmaConsumers) {
+            if (i != kWinTinyNeg && i != kWinTinyPos) {
+              hout[i] = (int)hist->cnt[i];
+              hist->cnt[i] = 0u;
+            }
+          }
+          named_sync(1, kTmaConsumers);
+          if (tid == 0) {
+            hout[kWinTinyNeg] = (int)hist->tiny_cnt[0];
+            hout[kWinTinyPos] = (int)hist->tiny_cnt[1];
+            hout[kWinItems] = (int)hist->out_of_range;
+            hout[kWinItems + 1] = 0;
+            P.sh_hist_w[2 * M.row] = hist->tiny_w[0];
+            P.sh_hist_w[2 * M.row + 1] = hist->tiny_w[1];
+            hist->tiny_cnt[0] = hist->tiny_cnt[1] = 0u;
+            hist->tiny_w[0] = hist->tiny_w[1] = 0.f;
+            hist->out_of_range = 0u;
+          }
+        }
+        named_sync(1, kTmaConsumers);
+        if (tid == 0) {
+          float z = 0.f;
+          if (soft)
+            for (int w = 0; w < kTmaConsumerWarps; ++w) z += red_s[w];
+          P.sh_m[M.row] = m;
+          P.sh_z[M.row] = z;
+          P.sh_arg[M.row] = (a == kNoIndex) ? 0x7FFFFFFF : a + P.v0;
+          P.sh_lx[M.row] = s_has_lx ? s_lx : -INFINITY;
+          P.rows[M.row].m = m;  // the local max, for the rescale
+          s_has_lx = 0;
+        }
+        named_sync(1, kTmaConsumers);
+        vmax = -INFINITY;
+        vmc = 0.f;
+        s = 0.f;
+        imax = kNoIndex;
+        continue;
+      }
       float zmerged = 0.f;
       if (EARLY && P.parts > 1) {
         // End of one part of the row: publish the part's statistics (and add

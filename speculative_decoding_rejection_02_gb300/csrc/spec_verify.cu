@@ -15,6 +15,7 @@
 #include "race.cuh"
 #include "rows.cuh"
 #include "rows_tma.cuh"
+#include "shard.cuh"
 
 struct spec_verify_handle {
   spec_verify_config cfg;
@@ -57,7 +58,12 @@ bool set_row_pass_smem() {
          cudaFuncSetAttribute(sv::k_rows_tma<true, true>, a, filt) == cudaSuccess &&
          cudaFuncSetAttribute(sv::k_rows_tma<true, false, true>, a, plain) == cudaSuccess &&
          cudaFuncSetAttribute(sv::k_rows_tma<false, false, true>, a, plain) == cudaSuccess &&
-         cudaFuncSetAttribute(sv::k_rows_tma<true, true, true>, a, filt) == cudaSuccess;
+         cudaFuncSetAttribute(sv::k_rows_tma<true, true, true>, a, filt) == cudaSuccess &&
+         cudaFuncSetAttribute(sv::k_rows_tma<true, false, false, true>, a, plain) ==
+             cudaSuccess &&
+         cudaFuncSetAttribute(sv::k_rows_tma<false, false, false, true>, a, plain) ==
+             cudaSuccess &&
+         cudaFuncSetAttribute(sv::k_rows_tma<true, true, false, true>, a, filt) == cudaSuccess;
 }
 
 // Control words of the early-exit queue, and its slots beyond one per row
@@ -100,14 +106,10 @@ int check_batch(const spec_verify_config* cfg, const spec_verify_batch* b, bool 
   return SPEC_OK;
 }
 
-int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t stream, bool greedy) {
-  if (!h) return SPEC_ERR_NOT_INIT;
-  int rc = check_batch(&h->cfg, b, greedy);
-  if (rc != SPEC_OK) return rc;
-  if (b->B == 0) return SPEC_OK;
-  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return SPEC_ERR_CUDA;
-
+// The kernel parameters of a call: the batch and the handle's workspace.
+sv::Params make_params(spec_verify_handle* h, const spec_verify_batch* b, bool greedy) {
   sv::Params P;
+  std::memset(&P, 0, sizeof P);
   P.B = b->B;
   P.V = b->V;
   P.N = b->N;
@@ -151,7 +153,19 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   const int slice = P.bf16 ? sv::kSliceBf16 : sv::kSliceF32;
   P.slices_per_row = (b->V + slice - 1) / slice;
   P.race_slices = (b->V + sv::kRaceSlice - 1) / sv::kRaceSlice;
+  P.v0 = 0;
+  P.Vg = b->V;
+  return P;
+}
 
+int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t stream, bool greedy) {
+  if (!h) return SPEC_ERR_NOT_INIT;
+  int rc = check_batch(&h->cfg, b, greedy);
+  if (rc != SPEC_OK) return rc;
+  if (b->B == 0) return SPEC_OK;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return SPEC_ERR_CUDA;
+
+  sv::Params P = make_params(h, b, greedy);
   const long long R = (long long)b->N + b->B;
   const bool match = !greedy && (P.flags & SPEC_FLAG_SAMPLER_MATCH);
   // Races: one per request (its k* row), or one per row under sampler-match.
@@ -404,6 +418,140 @@ void spec_verify_destroy(spec_verify_handle* h) {
   cudaDeviceSynchronize();
   cudaFree(h->ws);
   delete h;
+}
+
+// ---------------------------------------------------------------------------
+// Vocab-sharded verification (the protocol is in include/spec_verify.h).
+// ---------------------------------------------------------------------------
+static int shard_setup(spec_verify_handle* h, const spec_verify_batch* b, const spec_shard* sh,
+                       sv::Params& P, bool& filters) {
+  if (!h) return SPEC_ERR_NOT_INIT;
+  if (!sh) return SPEC_ERR_INVALID_ARG;
+  int rc = check_batch(&h->cfg, b, false);
+  if (rc != SPEC_OK) return rc;
+  if (b->flags) return SPEC_ERR_UNSUPPORTED;
+  if (sh->v0 < 0 || (sh->v0 & 3) || sh->V_global < 1 || sh->v0 + b->V > sh->V_global ||
+      sh->V_global > 0x7FFFFFFF - 8)
+    return SPEC_ERR_INVALID_ARG;
+  if (b->B == 0) return SPEC_OK;
+  const long long esize = (b->logits_dtype == SPEC_BF16) ? 2 : 4;
+  filters = b->top_k || b->top_p;
+  const bool aligned = ((long long)b->V * esize) % 16 == 0 &&
+                       (reinterpret_cast<uintptr_t>(b->target_logits) & 15) == 0;
+  if (!aligned || h->tma_blocks <= 0 || (filters && (esize != 2 || h->filt_blocks <= 0)))
+    return SPEC_ERR_UNSUPPORTED;
+  if (!sh->m || !sh->z || !sh->argmax || !sh->lx || !sh->best || !sh->best_p ||
+      (b->draft_probs && !sh->qx) || (filters && (!sh->hist || !sh->hist_w)))
+    return SPEC_ERR_INVALID_ARG;
+  if (cudaSetDevice(h->cfg.device) != cudaSuccess) return SPEC_ERR_CUDA;
+  P = make_params(h, b, false);
+  P.shard = 1;
+  P.v0 = (int)sh->v0;
+  P.Vg = sh->V_global;
+  P.sh_m = sh->m;
+  P.sh_z = sh->z;
+  P.sh_arg = sh->argmax;
+  P.sh_lx = sh->lx;
+  P.sh_qx = b->draft_probs ? sh->qx : nullptr;
+  P.sh_hist = sh->hist;
+  P.sh_hist_w = sh->hist_w;
+  P.sh_best = sh->best;
+  P.sh_skip = nullptr;
+  return SPEC_OK;
+}
+
+static int launched() {
+  if (cudaPeekAtLastError() != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_CUDA;
+  }
+  return SPEC_OK;
+}
+
+int spec_verify_shard_rows(spec_verify_handle* h, const spec_verify_batch* b,
+                           const spec_shard* sh, void* stream) {
+  sv::Params P;
+  bool filters = false;
+  int rc = shard_setup(h, b, sh, P, filters);
+  if (rc != SPEC_OK || b->B == 0) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  const long long R = (long long)b->N + b->B;
+  if (filters) {
+    const long long grid = R < h->filt_blocks ? R : h->filt_blocks;
+    sv::k_rows_tma<true, true, false, true><<<(unsigned)grid, sv::kTmaThreads,
+                                               sv::kTmaFiltSmemBytes, s>>>(P, R);
+  } else {
+    const long long grid = R < h->tma_blocks ? R : h->tma_blocks;
+    if (P.bf16)
+      sv::k_rows_tma<true, false, false, true><<<(unsigned)grid, sv::kTmaThreads,
+                                                  sv::kTmaSmemBytes, s>>>(P, R);
+    else
+      sv::k_rows_tma<false, false, false, true><<<(unsigned)grid, sv::kTmaThreads,
+                                                   sv::kTmaSmemBytes, s>>>(P, R);
+  }
+  return launched();
+}
+
+int spec_verify_shard_rescale(spec_verify_handle* h, const spec_verify_batch* b,
+                              const spec_shard* sh, void* stream) {
+  sv::Params P;
+  bool filters = false;
+  int rc = shard_setup(h, b, sh, P, filters);
+  if (rc != SPEC_OK || b->B == 0) return rc;
+  const long long R = (long long)b->N + b->B;
+  const long long n = R > b->N ? R : b->N;
+  sv::k_shard_rescale<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>(P);
+  return launched();
+}
+
+int spec_verify_shard_judge(spec_verify_handle* h, const spec_verify_batch* b,
+                            const spec_shard* sh, void* stream) {
+  sv::Params P;
+  bool filters = false;
+  int rc = shard_setup(h, b, sh, P, filters);
+  if (rc != SPEC_OK || b->B == 0) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  const long long R = (long long)b->N + b->B;
+  if ((long long)b->B * P.race_slices > 0x7FFFFFFFll) return SPEC_ERR_CAPACITY;
+  sv::k_shard_finish<<<(unsigned)R, sv::kShardFinishThreads, filters ? sizeof(sv::WinHist) : 0,
+                       s>>>(P);
+  if (cudaMemsetAsync(h->race_count, 0, 2 * sizeof(unsigned), s) != cudaSuccess ||
+      cudaMemsetAsync(sh->best, 0, (size_t)b->B * sizeof(unsigned long long), s) != cudaSuccess)
+    return SPEC_ERR_CUDA;
+  sv::k_accept<<<(b->B + sv::kAcceptWarps - 1) / sv::kAcceptWarps, sv::kAcceptWarps * 32, 0, s>>>(
+      P);
+  sv::k_race<<<(unsigned)((long long)b->B * P.race_slices), sv::kRaceThreads,
+               sv::race_smem_bytes(P.bf16 ? 2 : 4), s>>>(P);
+  return launched();
+}
+
+int spec_verify_shard_race_p(spec_verify_handle* h, const spec_verify_batch* b,
+                             const spec_shard* sh, void* stream) {
+  sv::Params P;
+  bool filters = false;
+  int rc = shard_setup(h, b, sh, P, filters);
+  if (rc != SPEC_OK || b->B == 0) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  P.sh_skip = sh->best;
+  P.sh_best = sh->best_p;
+  if (cudaMemsetAsync(sh->best_p, 0, (size_t)b->B * sizeof(unsigned long long), s) !=
+      cudaSuccess)
+    return SPEC_ERR_CUDA;
+  sv::k_shard_race_reset<<<(b->B + 255) / 256, 256, 0, s>>>(P);
+  sv::k_race<<<(unsigned)((long long)b->B * P.race_slices), sv::kRaceThreads,
+               sv::race_smem_bytes(P.bf16 ? 2 : 4), s>>>(P);
+  return launched();
+}
+
+int spec_verify_shard_emit(spec_verify_handle* h, const spec_verify_batch* b,
+                           const spec_shard* sh, void* stream) {
+  sv::Params P;
+  bool filters = false;
+  int rc = shard_setup(h, b, sh, P, filters);
+  if (rc != SPEC_OK || b->B == 0) return rc;
+  sv::k_shard_emit<<<(b->B + 255) / 256, 256, 0, (cudaStream_t)stream>>>(P, sh->best,
+                                                                          sh->best_p);
+  return launched();
 }
 
 const char* spec_verify_strerror(int code) {
