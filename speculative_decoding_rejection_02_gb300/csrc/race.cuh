@@ -120,20 +120,38 @@ __device__ unsigned long long race_candidate(const Params& P, const RaceView& v,
   return race_pack(race_score(w, words[j & 3]), jg);
 }
 
+// A queued group (entries 4g .. 4g+3); its weights are recomputed from the
+// group's logits when the queue is worked off, so an item is 4 bytes.
 struct RaceItem {
-  uint32_t g;  // group (entries 4g .. 4g+3)
-  float w[4];  // their weights
+  uint32_t g;
 };
+
+// The weights of group g (0 beyond the row), computed as race_batch's
+// first pass computes them: fetch(g, l, q) supplies the logits and draft
+// probabilities.
+template <typename Fetch>
+__device__ __forceinline__ void race_group_w(const RaceView& v, int mode, uint32_t g, Fetch& fetch,
+                                             float w[4]) {
+  float l[4], q[4];
+  fetch(g, l, q);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const int j = (int)(g * 4u) + e;
+    w[e] = (j < v.V) ? race_w(race_p(l[e], v), q[e], j, mode, v.x) : 0.f;
+  }
+}
 
 // Score one batch: this thread's kRaceGroups groups (group ids gk[k], their
 // logits l[k][] and draft probabilities q[k][]; ids >= g1 are absent). All
 // 32 lanes of the warp call it together. `qw` is the warp's queue of
-// 32 * kRaceGroups items.
+// 32 * kRaceGroups items; fetch(g, l, q) gives any group's logits and draft
+// probabilities again.
+template <typename Fetch>
 __device__ __forceinline__ void race_batch(const Params& P, const RaceView& v, int mode,
                                            const uint32_t gk[kRaceGroups], uint32_t g1,
                                            float l[kRaceGroups][4], float q[kRaceGroups][4],
                                            float& best, int& best_j, float& lthr,
-                                           RaceItem* qw) {
+                                           RaceItem* qw, Fetch fetch) {
   // Decide every group against one snapshot of the best (the best only
   // grows, so an older snapshot prunes less but never wrongly).
   const float cut = best;
@@ -155,20 +173,15 @@ __device__ __forceinline__ void race_batch(const Params& P, const RaceView& v, i
       need = (wmax > 0.f) && (wmax * kInvEMin > cut);
     }
     const unsigned m = __ballot_sync(0xFFFFFFFFu, need);
-    if (need) {
-      RaceItem& it = qw[n_items + __popc(m & ((1u << lane) - 1u))];
-      it.g = g;
-      it.w[0] = w[0];
-      it.w[1] = w[1];
-      it.w[2] = w[2];
-      it.w[3] = w[3];
-    }
+    if (need) qw[n_items + __popc(m & ((1u << lane) - 1u))].g = g;
     n_items += __popc(m);
   }
   __syncwarp();
   for (int t = lane; t < n_items; t += 32) {
-    const RaceItem it = qw[t];
-    const uint4 r = race_words(P.seed, v.greq, v.kstar, v.g0 + it.g);
+    const uint32_t gq = qw[t].g;
+    float wq[4];
+    race_group_w(v, mode, gq, fetch, wq);
+    const uint4 r = race_words(P.seed, v.greq, v.kstar, v.g0 + gq);
     const uint32_t words[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -176,9 +189,9 @@ __device__ __forceinline__ void race_batch(const Params& P, const RaceView& v, i
       // is exact and the factor (1 + 2e-6) covers the roundings of the
       // score and of this test. Entries that fail cannot reach `cut`.
       const float v1 = 1.f - race_uniform_from_word(words[e]);
-      if (it.w[e] > 0.f && it.w[e] * 1.000002f > cut * v1) {
-        const float sc = race_score(it.w[e], words[e]);
-        const int j = (int)(it.g * 4u) + e;
+      if (wq[e] > 0.f && wq[e] * 1.000002f > cut * v1) {
+        const float sc = race_score(wq[e], words[e]);
+        const int j = (int)(gq * 4u) + e;
         if (sc > best || (sc == best && j < best_j)) {
           best = sc;
           best_j = j;
@@ -217,11 +230,21 @@ __device__ void race_range_global(const Params& P, const RaceView& v, int mode, 
         q[k][e] = (in && mode == kRaceResidual) ? __ldg(P.q + (long long)v.qrow * V + j) : 0.f;
       }
     }
-    race_batch(P, v, mode, gk, g1, l, q, best, best_j, lthr, qw);
+    race_batch(P, v, mode, gk, g1, l, q, best, best_j, lthr, qw,
+               [&](uint32_t g, float* lf, float* qf) {
+#pragma unroll
+                 for (int e = 0; e < 4; ++e) {
+                   const int j = (int)(g * 4u) + e;
+                   const bool in = j < V;
+                   lf[e] = in ? load_logit(P, v.row, j) : -INFINITY;
+                   qf[e] = (in && mode == kRaceResidual)
+                               ? __ldg(P.q + (long long)v.qrow * V + j) : 0.f;
+                 }
+               });
   }
 }
 
-__global__ void __launch_bounds__(kRaceThreads)
+__global__ void __launch_bounds__(kRaceThreads, 4)
 k_race(Params P) {
   extern __shared__ __align__(128) unsigned char race_smem[];
   __shared__ int s_last;
@@ -362,7 +385,19 @@ k_race(Params P) {
             }
           }
         }
-        race_batch(P, v, v.mode, gk, g1, l, q, best, best_j, lthr, qw);
+        race_batch(P, v, v.mode, gk, g1, l, q, best, best_j, lthr, qw,
+                   [&](uint32_t g, float* lf, float* qf) {
+#pragma unroll
+                     for (int e = 0; e < 4; ++e) {
+                       const int le = (int)((g - g0) * 4u) + e;
+                       const bool in = le < n;
+                       lf[e] = in ? (P.bf16 ? bf16_lo((uint32_t)*reinterpret_cast<
+                                                      const unsigned short*>(lbuf + (size_t)le * 2))
+                                            : *reinterpret_cast<const float*>(lbuf + (size_t)le * 4))
+                                  : -INFINITY;
+                       qf[e] = (in && resid) ? qbuf[le] : 0.f;
+                     }
+                   });
       }
     } else {
       race_range_global(P, v, v.mode, g0, g1, best, best_j, queue);
