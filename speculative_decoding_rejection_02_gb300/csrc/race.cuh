@@ -266,6 +266,9 @@ k_race(Params P) {
   const RaceView v = race_view(P, r, task.row, task.qrow, task.kstar,
                                P.sh_skip ? (int)kRaceP : task.mode, task.x, task.m, task.c,
                                task.inv_z, task.theta, task.z);
+  // The best so far (seeded by the accept scan, raised by earlier slices),
+  // read now so that its latency overlaps the copies below.
+  const unsigned long long lb = __ldcg(P.race_best + slot);
   const int V = P.V;
   const uint32_t groups = (uint32_t)((V + 3) / 4);
   const uint32_t g0 = (uint32_t)slice * (kRaceSlice / 4);
@@ -306,9 +309,7 @@ k_race(Params P) {
     }
   }
 
-  // The best so far (seeded by the accept scan, raised by earlier slices);
-  // packed with global indices, kept here as local ones.
-  const unsigned long long lb = __ldcg(P.race_best + slot);
+  // Packed with global indices, kept here as local ones.
   float best = lb ? __uint_as_float((uint32_t)(lb >> 32)) : 0.f;
   int best_j = lb ? (int)(0xFFFFFFFFu - (uint32_t)lb) - v.v0 : kNoIndex;
   if (v.z > 0.f) {
