@@ -33,16 +33,23 @@
 namespace sv {
 
 constexpr int kRaceThreads = 256;
-constexpr int kRaceSlice = 8192;  // entries per task (multiple of 16 * kRaceThreads)
+// Entries per task (multiples of 16 * kRaceThreads): 8192 when the call
+// has draft probabilities (the slice's q is staged too), else 16384.
+constexpr int kRaceSlice = 8192;
+constexpr int kRaceSliceNoQ = 16384;
+__host__ __device__ constexpr int race_slice(bool has_q) { return has_q ? kRaceSlice : kRaceSliceNoQ; }
 constexpr int kRaceGroups = 4;    // groups of 4 entries per thread per batch
 // Above 1 / E_min, E_min = -ln(1 - 2^-24) ~ 5.96e-8 the smallest E a race
 // uniform can give: no entry scores more than w * kInvEMin.
 constexpr float kInvEMin = 1.7e7f;
-// Shared memory of the staged path: the slice's logits and its draft
-// probabilities (fp32).
-__host__ __device__ constexpr size_t race_smem_bytes(int logit_bytes) {
-  return (size_t)kRaceSlice * logit_bytes + (size_t)kRaceSlice * 4;
+// Shared memory of the staged path: the slice's logits and, when the call
+// has draft probabilities, theirs (fp32).
+__host__ __device__ constexpr size_t race_smem_bytes(int logit_bytes, bool has_q) {
+  return has_q ? (size_t)kRaceSlice * (logit_bytes + 4) : (size_t)kRaceSliceNoQ * logit_bytes;
 }
+// The largest of the above.
+constexpr size_t kRaceSmemMax = race_smem_bytes(4, true) > race_smem_bytes(4, false)
+                                    ? race_smem_bytes(4, true) : race_smem_bytes(4, false);
 
 // What the scoring needs about the race row.
 struct RaceView {
@@ -271,16 +278,17 @@ k_race(Params P) {
   const unsigned long long lb = __ldcg(P.race_best + slot);
   const int V = P.V;
   const uint32_t groups = (uint32_t)((V + 3) / 4);
-  const uint32_t g0 = (uint32_t)slice * (kRaceSlice / 4);
-  const uint32_t g1 = min(groups, g0 + (uint32_t)(kRaceSlice / 4));
+  const int slice_n = race_slice(P.q != nullptr);
+  const uint32_t g0 = (uint32_t)slice * (uint32_t)(slice_n / 4);
+  const uint32_t g1 = min(groups, g0 + (uint32_t)(slice_n / 4));
   const int j0 = (int)(g0 * 4u);
-  const int n = min(kRaceSlice, V - j0);
+  const int n = min(slice_n, V - j0);
   const int esize = P.bf16 ? 2 : 4;
   const bool resid = (v.mode == kRaceResidual);
   const char* lsrc = (const char*)P.logits + ((long long)v.row * V + j0) * esize;
   const char* qsrc = resid ? (const char*)(P.q + (long long)v.qrow * V + j0) : nullptr;
   unsigned char* lbuf = race_smem;
-  float* qbuf = reinterpret_cast<float*>(race_smem + (size_t)kRaceSlice * esize);
+  float* qbuf = reinterpret_cast<float*>(race_smem + (size_t)slice_n * esize);
 
   // Stage the slice with bulk copies when every address and size allows it.
   if (threadIdx.x == 0) {

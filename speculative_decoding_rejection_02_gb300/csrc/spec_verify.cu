@@ -152,7 +152,8 @@ sv::Params make_params(spec_verify_handle* h, const spec_verify_batch* b, bool g
   P.status = h->status;
   const int slice = P.bf16 ? sv::kSliceBf16 : sv::kSliceF32;
   P.slices_per_row = (b->V + slice - 1) / slice;
-  P.race_slices = (b->V + sv::kRaceSlice - 1) / sv::kRaceSlice;
+  const int rslice = sv::race_slice(P.q != nullptr);
+  P.race_slices = (b->V + rslice - 1) / rslice;
   P.v0 = 0;
   P.Vg = b->V;
   return P;
@@ -227,7 +228,7 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
       cudaEventRecord(h->phase[2], stream);
     }
     sv::k_race<<<(unsigned)(races * P.race_slices), sv::kRaceThreads,
-                 sv::race_smem_bytes(P.bf16 ? 2 : 4), stream>>>(P);
+                 sv::race_smem_bytes(P.bf16 ? 2 : 4, P.q != nullptr), stream>>>(P);
     if (timed) cudaEventRecord(h->phase[3], stream);
     if (cudaPeekAtLastError() != cudaSuccess) {
       cudaGetLastError();
@@ -263,7 +264,7 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   if (timed) cudaEventRecord(h->phase[2], stream);
   if (!greedy) {
     sv::k_race<<<(unsigned)(races * P.race_slices), sv::kRaceThreads,
-                 sv::race_smem_bytes(P.bf16 ? 2 : 4), stream>>>(P);
+                 sv::race_smem_bytes(P.bf16 ? 2 : 4, P.q != nullptr), stream>>>(P);
     if (match)
       sv::k_match<<<(b->B + sv::kAcceptWarps - 1) / sv::kAcceptWarps, sv::kAcceptWarps * 32, 0,
                     stream>>>(P);
@@ -317,7 +318,7 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   h->tma_blocks = per_sm * prop.multiProcessorCount;
   h->filt_blocks = filt_per_sm * prop.multiProcessorCount;
   if (cudaFuncSetAttribute(sv::k_race, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)sv::race_smem_bytes(4)) != cudaSuccess) {
+                           (int)sv::kRaceSmemMax) != cudaSuccess) {
     delete h;
     return SPEC_ERR_CUDA;
   }
@@ -521,7 +522,7 @@ int spec_verify_shard_judge(spec_verify_handle* h, const spec_verify_batch* b,
   sv::k_accept<<<(b->B + sv::kAcceptWarps - 1) / sv::kAcceptWarps, sv::kAcceptWarps * 32, 0, s>>>(
       P);
   sv::k_race<<<(unsigned)((long long)b->B * P.race_slices), sv::kRaceThreads,
-               sv::race_smem_bytes(P.bf16 ? 2 : 4), s>>>(P);
+               sv::race_smem_bytes(P.bf16 ? 2 : 4, P.q != nullptr), s>>>(P);
   return launched();
 }
 
@@ -539,7 +540,7 @@ int spec_verify_shard_race_p(spec_verify_handle* h, const spec_verify_batch* b,
     return SPEC_ERR_CUDA;
   sv::k_shard_race_reset<<<(b->B + 255) / 256, 256, 0, s>>>(P);
   sv::k_race<<<(unsigned)((long long)b->B * P.race_slices), sv::kRaceThreads,
-               sv::race_smem_bytes(P.bf16 ? 2 : 4), s>>>(P);
+               sv::race_smem_bytes(P.bf16 ? 2 : 4, P.q != nullptr), s>>>(P);
   return launched();
 }
 
@@ -647,7 +648,7 @@ extern "C" int spec_verify_run_noalloc(const spec_verify_batch* b, void* stream,
       int per_sm = 0, filt_per_sm = 0;
       if (!set_row_pass_smem() ||
           cudaFuncSetAttribute(sv::k_race, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)sv::race_smem_bytes(4)) != cudaSuccess ||
+                               (int)sv::kRaceSmemMax) != cudaSuccess ||
           cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, sv::k_rows_tma<true, false>,
                                                         sv::kTmaThreads,
                                                         sv::kTmaSmemBytes) != cudaSuccess ||
