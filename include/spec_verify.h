@@ -113,8 +113,16 @@ typedef struct {
   int max_batch;       /* largest B of any call */
   long long max_rows;  /* largest N + B (target rows) of any call */
   int max_vocab;       /* largest V of any call */
-  unsigned flags;      /* reserved: 0 */
+  unsigned flags;      /* SPEC_CONFIG_* (0 in normal use) */
 } spec_verify_config;
+
+/* Handle flags (spec_verify_config.flags). */
+#define SPEC_CONFIG_TEST_WAIT_TIMEOUT 0x1u /* test only (no counterpart on the pages):
+                                              early-exit calls leave their work queue
+                                              empty and its waits give up after a few
+                                              polls, so the call ends with
+                                              SPEC_STATUS_TIMEOUT and garbage outputs;
+                                              no asynchronous copy is issued */
 
 typedef struct {
   int B;                       /* requests in the batch, >= 0 */

@@ -35,6 +35,8 @@ FLAG_NAIVE = 0x1
 FLAG_SAMPLER_MATCH = 0x2
 FLAG_EARLY_EXIT = 0x4
 
+CONFIG_TEST_WAIT_TIMEOUT = 0x1  # test only: early-exit queue waits run out
+
 # The entry points declared in include/spec_verify.h.
 ENTRY_POINTS = (
     "spec_verify_init", "spec_verify_run", "spec_verify_greedy", "spec_verify_status",
@@ -208,10 +210,11 @@ def upload(batch: dict, device="cuda", with_p=True, pin=False) -> DeviceBatch:
 class Verifier:
     """One library handle (one workspace) on one CUDA device."""
 
-    def __init__(self, max_batch: int, max_rows: int, max_vocab: int, device: int = 0):
+    def __init__(self, max_batch: int, max_rows: int, max_vocab: int, device: int = 0,
+                 config_flags: int = 0):
         self._lib = lib()
         self.cfg = Config(device=device, max_batch=max_batch, max_rows=max_rows,
-                          max_vocab=max_vocab, flags=0)
+                          max_vocab=max_vocab, flags=config_flags)
         h = C.c_void_p()
         _check(self._lib.spec_verify_init(C.byref(h), C.byref(self.cfg)), "spec_verify_init")
         self._h = h

@@ -117,6 +117,7 @@ struct Params {
   unsigned* pending_count;  // entries in pending_rows (race_count + 1)
   // Early exit (SPEC_FLAG_EARLY_EXIT): the row pass's work queue.
   int early;
+  int test_stall;           // 1: leave the early-exit queue empty, short waits (tests)
   long long* queue;         // [q_cap] items (row << 3) | part
   unsigned* queue_ready;    // [q_cap] 1 once the slot holds its item
   unsigned* queue_ctl;      // control words, see early.cuh

@@ -23,6 +23,7 @@
 namespace sv {
 
 constexpr uint32_t kQueueTryLimit = 1u << 19;  // polls of ~0.2-1 us: half a second at most
+constexpr uint32_t kQueueTestTryLimit = 64;    // SPEC_CONFIG_TEST_WAIT_TIMEOUT
 
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
@@ -46,7 +47,8 @@ __device__ long long queue_pop(const Params& P) {
   unsigned* ctl = P.queue_ctl;
   const unsigned h = atomicAdd(ctl + kQTaken, 1u);
   if (h >= (unsigned)P.q_cap) return -1;
-  for (uint32_t it = 0; it < kQueueTryLimit; ++it) {
+  const uint32_t limit = P.test_stall ? kQueueTestTryLimit : kQueueTryLimit;
+  for (uint32_t it = 0; it < limit; ++it) {
     if (ld_acquire(&P.queue_ready[h])) return __ldcg(&P.queue[h]);
     if (ld_acquire(ctl + kQDone) >= (unsigned)P.B) return -1;
     __nanosleep(200);
@@ -93,6 +95,8 @@ __global__ void k_early_init(Params P) {
     request_done(P);
     return;
   }
+  // Test only: nothing is queued, so every reader's wait runs out.
+  if (P.test_stall) return;
   for (int part = 0; part < P.parts; ++part) queue_push(P, (((long long)c0 + r) << 3) | part);
 }
 

@@ -140,6 +140,7 @@ sv::Params make_params(spec_verify_handle* h, const spec_verify_batch* b, bool g
   P.pending_rows = h->pending_rows;
   P.pending_count = h->race_count + 1;
   P.early = (!greedy && (b->flags & SPEC_FLAG_EARLY_EXIT)) ? 1 : 0;
+  P.test_stall = (h->cfg.flags & SPEC_CONFIG_TEST_WAIT_TIMEOUT) ? 1 : 0;
   P.queue = h->queue;
   P.queue_ready = h->queue_ready;
   P.queue_ctl = h->queue_ctl;
@@ -291,6 +292,7 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   if (!cfg || cfg->max_batch < 1 || cfg->max_rows < 1 || cfg->max_vocab < 1)
     return SPEC_ERR_INVALID_ARG;
   if (cfg->max_rows < cfg->max_batch) return SPEC_ERR_INVALID_ARG;
+  if (cfg->flags & ~SPEC_CONFIG_TEST_WAIT_TIMEOUT) return SPEC_ERR_INVALID_ARG;
   if (cudaSetDevice(cfg->device) != cudaSuccess) return SPEC_ERR_CUDA;
   cudaDeviceProp prop;
   if (cudaGetDeviceProperties(&prop, cfg->device) != cudaSuccess) return SPEC_ERR_CUDA;

@@ -212,3 +212,26 @@ def test_window_histogram_cases(case):
     b = make_batch(logits, g, ids, temps, q, tk, tp, dtype="bf16", seed=17)
     gpu, _ = check(b)
     assert gpu["status"] & ~np.uint32(0x8) == 0
+
+
+def test_bounded_wait_times_out_and_the_context_survives():
+    """A wait that cannot be satisfied ends with SPEC_STATUS_TIMEOUT instead
+    of hanging: a test-only handle flag leaves the early-exit work queue
+    empty (nothing will ever fill the slots the readers wait on) and gives
+    those waits a few polls. The same process then verifies a batch
+    correctly with a normal handle."""
+    import torch
+
+    import speculative_decoding_rejection_02_gb300 as sv
+    b = synth.make("c5", B=16, V=20000)
+    b["flags"] = sv.FLAG_EARLY_EXIT
+    R = b["target_logits"].shape[0]
+    ver = sv.Verifier(max_batch=16, max_rows=R, max_vocab=20000,
+                      config_flags=sv.CONFIG_TEST_WAIT_TIMEOUT)
+    db = sv.upload(b, "cuda:0")
+    ver.run(db)
+    torch.cuda.synchronize()
+    assert ver.status() & sv.STATUS_TIMEOUT
+    ver.close()
+    gpu, _ = check(b)
+    assert gpu["status"] == 0
