@@ -94,14 +94,16 @@ extern "C" {
 #define SPEC_FLAG_SAMPLER_MATCH 0x2u
 /* Early-exit verification (velog, "드래프트가 제안하고 타깃이 판정한다": the
  * first rejection ends the round and the later positions are discarded):
- * each request's target rows are read in position order and reading stops
- * at the first rejection, so the rows after it are never read. Every emitted
+ * only the rows up to each request's first rejection count. Every emitted
  * token and count is the one the full pass gives; the differences are that
- * an unusable row (NaN, +inf, all -inf) after the stop does not void the
- * request, and p_at_draft is NaN at the positions after the stop. Needs
- * 16-byte aligned target rows (V * element size a multiple of 16, aligned
- * base), and bf16 logits when top_k / top_p are given; otherwise
- * SPEC_ERR_UNSUPPORTED. Cannot be combined with SPEC_FLAG_SAMPLER_MATCH. */
+ * an unusable row (NaN, +inf, all -inf) or an invalid draft token after the
+ * stop does not void the request or set a status bit, and p_at_draft is NaN
+ * at the positions after the stop. When the batch has enough requests to
+ * keep every SM busy (B at least twice the row pass's resident CTAs) and its
+ * rows are 16-byte aligned (bf16 if top_k / top_p are given), the rows are
+ * read position by position and the rows after the stop are never read;
+ * otherwise every row is read (faster for small batches) with the same
+ * results. Cannot be combined with SPEC_FLAG_SAMPLER_MATCH. */
 #define SPEC_FLAG_EARLY_EXIT 0x4u
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
@@ -117,6 +119,9 @@ typedef struct {
 } spec_verify_config;
 
 /* Handle flags (spec_verify_config.flags). */
+#define SPEC_CONFIG_EARLY_QUEUE 0x2u       /* test only: early-exit calls read their rows
+                                              position by position whenever the rows
+                                              allow it, whatever the batch size */
 #define SPEC_CONFIG_TEST_WAIT_TIMEOUT 0x1u /* test only (no counterpart on the pages):
                                               early-exit calls leave their work queue
                                               empty and its waits give up after a few

@@ -36,6 +36,7 @@ FLAG_SAMPLER_MATCH = 0x2
 FLAG_EARLY_EXIT = 0x4
 
 CONFIG_TEST_WAIT_TIMEOUT = 0x1  # test only: early-exit queue waits run out
+CONFIG_EARLY_QUEUE = 0x2        # test only: early exit always takes the work queue
 
 # The entry points declared in include/spec_verify.h.
 ENTRY_POINTS = (

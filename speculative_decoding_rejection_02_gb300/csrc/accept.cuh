@@ -20,6 +20,19 @@ namespace sv {
 
 constexpr int kAcceptWarps = 8;  // requests per CTA
 
+// A request with an unusable target row emits nothing (the whole warp).
+__device__ __forceinline__ void void_request(const Params& P, int r, int c0, int gamma,
+                                             long long row0, const RaceDesc& d) {
+  const int lane = threadIdx.x & 31;
+  for (int i = lane; i <= gamma; i += 32) P.out_tokens[row0 + i] = -1;
+  if (P.p_at_draft)
+    for (int i = lane; i < gamma; i += 32) P.p_at_draft[c0 + i] = 0.f;
+  if (lane == 0) {
+    P.num_accepted[r] = 0;
+    P.race[r] = d;
+  }
+}
+
 // Sampler-match acceptance (mlxcel "투기적 디코딩", section "mlxcel의 프롬프트
 // 조회"): the target's sampler draws y_i from p_i at every position
 // i = 0 .. gamma and x_i is accepted iff it equals y_i. Each row of the
@@ -106,20 +119,18 @@ k_accept(Params P) {
   const int gamma = c1 - c0;
   const long long row0 = (long long)c0 + r;
   const bool greedy = P.greedy_call || !(__ldg(P.temp + r) > 0.f);
+  // Early-exit semantics on the full pass (every row was read, but only the
+  // rows up to the first rejection count): unusable rows and invalid draft
+  // tokens after it are ignored, p_at_draft is NaN after it.
+  const bool early_sem = (P.flags & SPEC_FLAG_EARLY_EXIT) != 0;
+  constexpr unsigned kUnusable =
+      SPEC_STATUS_NONFINITE | SPEC_STATUS_NO_FINITE | SPEC_STATUS_UNSETTLED;
 
   unsigned st = 0;
   for (int i = lane; i <= gamma; i += 32) st |= P.rows[row0 + i].status;
   st = __reduce_or_sync(0xFFFFFFFFu, st);
-  if (!greedy &&
-      (st & (SPEC_STATUS_NONFINITE | SPEC_STATUS_NO_FINITE | SPEC_STATUS_UNSETTLED))) {
-    // Unusable target row: nothing is emitted for this request.
-    for (int i = lane; i <= gamma; i += 32) P.out_tokens[row0 + i] = -1;
-    if (P.p_at_draft)
-      for (int i = lane; i < gamma; i += 32) P.p_at_draft[c0 + i] = 0.f;
-    if (lane == 0) {
-      P.num_accepted[r] = 0;
-      P.race[r] = d;
-    }
+  if (!greedy && !early_sem && (st & kUnusable)) {
+    void_request(P, r, c0, gamma, row0, d);
     return;
   }
 
@@ -159,7 +170,28 @@ k_accept(Params P) {
     const unsigned rej = __ballot_sync(0xFFFFFFFFu, !ok);
     if (k == gamma && rej) k = base + __ffs(rej) - 1;
   }
-  if (__reduce_or_sync(0xFFFFFFFFu, bad_tok)) st |= SPEC_STATUS_BAD_TOKEN;
+  bad_tok = __reduce_or_sync(0xFFFFFFFFu, bad_tok);
+  if (early_sem) {
+    // An invalid draft token is always rejected, so under early exit only
+    // the one at the stop can be judged.
+    const int xk = (k < gamma) ? __ldg(P.ids + c0 + k) : 0;
+    bad_tok = (k < gamma && !(xk >= 0 && xk < P.Vg)) ? 1u : 0u;
+  }
+  if (bad_tok) st |= SPEC_STATUS_BAD_TOKEN;
+  if (early_sem) {
+    // Only the rows up to the stop count (a rejection always comes at or
+    // before an unusable row: its p(x) is 0).
+    unsigned st_k = 0;
+    for (int i = lane; i <= k; i += 32) st_k |= P.rows[row0 + i].status;
+    st_k = __reduce_or_sync(0xFFFFFFFFu, st_k);
+    if (!greedy && (st_k & kUnusable)) {
+      if (lane == 0) atomicOr(P.status, st_k & kUnusable);
+      void_request(P, r, c0, gamma, row0, d);
+      return;
+    }
+    if (P.p_at_draft)
+      for (int i = k + 1 + lane; i < gamma; i += 32) P.p_at_draft[c0 + i] = __int_as_float(0x7FC00000);
+  }
 
   for (int i = lane; i <= gamma; i += 32) {
     int t = -1;

@@ -110,6 +110,7 @@ __device__ __noinline__ void early_decide(const Params& P, int r, int pos, int g
   const bool greedy = P.greedy_call || !(__ldg(P.temp + r) > 0.f);
   if (!greedy && (s.status & (SPEC_STATUS_NONFINITE | SPEC_STATUS_NO_FINITE))) {
     // Unusable target row: nothing is emitted for this request.
+    atomicOr(P.status, s.status & (SPEC_STATUS_NONFINITE | SPEC_STATUS_NO_FINITE));
     for (int i = 0; i <= gamma; ++i) P.out_tokens[row0 + i] = -1;
     if (P.p_at_draft)
       for (int i = 0; i < gamma; ++i) P.p_at_draft[c0 + i] = 0.f;

@@ -73,7 +73,9 @@ __device__ void finish_row_x(const Params& P, long long row, int cls, float m, i
   s.status = st;
   s.z = z;
   P.rows[row] = s;
-  if (st) atomicOr(P.status, st);
+  // Under early exit a row's problems count only if the row is at or before
+  // its request's stop: the accept step reports them then.
+  if (st && !(P.flags & SPEC_FLAG_EARLY_EXIT)) atomicOr(P.status, st);
 }
 
 // The draft token of target row `row` of request r (-1 for the last row).

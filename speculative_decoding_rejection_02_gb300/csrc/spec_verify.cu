@@ -92,13 +92,6 @@ int check_batch(const spec_verify_config* cfg, const spec_verify_batch* b, bool 
         ((b->flags & SPEC_FLAG_SAMPLER_MATCH) &&
          (b->flags & (SPEC_FLAG_NAIVE | SPEC_FLAG_EARLY_EXIT))))
       return SPEC_ERR_INVALID_ARG;
-    if (b->flags & SPEC_FLAG_EARLY_EXIT) {
-      const long long esize = (b->logits_dtype == SPEC_BF16) ? 2 : 4;
-      const bool aligned = ((long long)b->V * esize) % 16 == 0 &&
-                           (reinterpret_cast<uintptr_t>(b->target_logits) & 15) == 0;
-      const bool filters = b->top_k || b->top_p;
-      if (!aligned || (filters && b->logits_dtype != SPEC_BF16)) return SPEC_ERR_UNSUPPORTED;
-    }
   }
   if (b->B > cfg->max_batch || b->V > cfg->max_vocab ||
       (long long)b->N + b->B > cfg->max_rows)
@@ -185,9 +178,16 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   P.fast_filtered = (rows_aligned && h->tma_blocks > 0 && h->filt_blocks > 0 && P.bf16 &&
                      filters) ? 1 : 0;
   if (P.early) {
+    // The work queue pays off when the batch's requests can keep every SM
+    // busy; otherwise (and for rows the bulk copies cannot take) the full
+    // pass runs and the accept scan applies the same early-exit semantics.
+    const int qblocks = P.fast_filtered ? h->filt_blocks : h->tma_blocks;
+    const bool queue_ok = rows_aligned && h->tma_blocks > 0 && (!filters || P.fast_filtered);
+    const bool big = (long long)b->B >= 2ll * qblocks;
+    if (!queue_ok || !(big || (h->cfg.flags & SPEC_CONFIG_EARLY_QUEUE))) P.early = 0;
+  }
+  if (P.early) {
     // Rows from the work queue, judged as they finish; no accept kernel.
-    if (!rows_aligned || h->tma_blocks <= 0 || (filters && !P.fast_filtered))
-      return SPEC_ERR_UNSUPPORTED;
     // Split each row into parts of about the target size (whole stages),
     // when the workspace has room for it.
     const long long row_bytes = (long long)b->V * esize;
@@ -292,7 +292,8 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   if (!cfg || cfg->max_batch < 1 || cfg->max_rows < 1 || cfg->max_vocab < 1)
     return SPEC_ERR_INVALID_ARG;
   if (cfg->max_rows < cfg->max_batch) return SPEC_ERR_INVALID_ARG;
-  if (cfg->flags & ~SPEC_CONFIG_TEST_WAIT_TIMEOUT) return SPEC_ERR_INVALID_ARG;
+  if (cfg->flags & ~(SPEC_CONFIG_TEST_WAIT_TIMEOUT | SPEC_CONFIG_EARLY_QUEUE))
+    return SPEC_ERR_INVALID_ARG;
   if (cudaSetDevice(cfg->device) != cudaSuccess) return SPEC_ERR_CUDA;
   cudaDeviceProp prop;
   if (cudaGetDeviceProperties(&prop, cfg->device) != cudaSuccess) return SPEC_ERR_CUDA;

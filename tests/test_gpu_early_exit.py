@@ -1,6 +1,9 @@
 """Early-exit verification on the GPU (velog "드래프트가 제안하고 타깃이
 판정한다": the first rejection ends the round), through the C ABI, against
-the oracle under the same flag and against the GPU's own full pass."""
+the oracle under the same flag and against the GPU's own full pass. Both
+schedules are run: rows read position by position through the work queue
+(forced with a test-only handle flag) and the full pass with early-exit
+judgement (what the library picks for small batches)."""
 import numpy as np
 import pytest
 
@@ -9,6 +12,20 @@ import synth
 from parity import assert_parity, check_structure, compare, run_gpu
 
 pytestmark = pytest.mark.gpu
+
+SCHEDULES = ["queue", "full"]
+
+
+def _run(b, schedule, greedy=False):
+    import speculative_decoding_rejection_02_gb300 as sv
+    R = b["target_logits"].shape[0]
+    flags = sv.CONFIG_EARLY_QUEUE if schedule == "queue" else 0
+    ver = sv.Verifier(max_batch=max(b["B"], 1), max_rows=max(R, 1), max_vocab=b["V"],
+                      config_flags=flags)
+    try:
+        return run_gpu(b, greedy=greedy, verifier=ver)
+    finally:
+        ver.close()
 
 
 def _early(b):
@@ -28,14 +45,17 @@ def _unread_are_nan(b, out):
 @pytest.mark.parametrize("name,B,V", [
     ("c2", None, None),      # fp32 rows, no filters
     ("c2", 6, 32008),        # fp32, ragged tail inside the last stage
+    ("c2", 6, 32001),        # misaligned fp32 rows: always the full pass
+    ("c3", 27, 40003),       # odd V with filters: the full pass and the exact filter kernel
     ("c3", 27, 40000),       # every temperature / filter combination
     ("c4", 24, 50000),       # one-hot drafts, top-p
     ("c5", 40, 70000),
     ("c5", 33, 65536),
 ])
-def test_scaled_workloads(name, B, V):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_scaled_workloads(name, B, V, schedule):
     b = _early(synth.make(name, B=B, V=V))
-    gpu = run_gpu(b)
+    gpu = _run(b, schedule)
     ref = oracle.verify(b)
     assert gpu["status"] == 0
     check_structure(b, gpu)
@@ -44,10 +64,11 @@ def test_scaled_workloads(name, B, V):
 
 
 @pytest.mark.parametrize("name", ["c3", "c4", "c5"])
-def test_same_round_as_the_full_pass(name):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_same_round_as_the_full_pass(name, schedule):
     b = synth.make(name, B=64 if name != "c3" else None, V=None)
     full = run_gpu(b)
-    early = run_gpu(_early(b))
+    early = _run(_early(b), schedule)
     assert early["status"] == 0
     assert np.array_equal(full["out_tokens"], early["out_tokens"])
     assert np.array_equal(full["num_accepted"], early["num_accepted"])
@@ -63,7 +84,7 @@ def test_same_round_as_the_full_pass(name):
 @pytest.mark.parametrize("name,n_sample", [("c4", 12), ("c5", 16)])
 def test_full_size_sampled(name, n_sample):
     b = _early(synth.make(name))
-    gpu = run_gpu(b)
+    gpu = run_gpu(b)  # the library's own choice of schedule
     assert gpu["status"] == 0
     check_structure(b, gpu)
     reqs = np.sort(np.random.default_rng(11).choice(b["B"], size=n_sample, replace=False))
@@ -71,7 +92,10 @@ def test_full_size_sampled(name, n_sample):
     assert_parity(compare(b, gpu, ref, requests=reqs))
 
 
-def test_rows_after_the_stop_are_never_read():
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_rows_after_the_stop_do_not_count(schedule):
+    """NaN planted in the row after each stop: never read by the queue, read
+    but without effect by the full pass."""
     b = synth.make("c3", B=36, V=4000)
     clean = run_gpu(b)
     cu = b["cu_num_draft"]
@@ -86,15 +110,16 @@ def test_rows_after_the_stop_are_never_read():
     assert len(planted) > 5
     nb = dict(b)
     nb["target_logits"] = t
-    early = run_gpu(_early(nb))
-    assert early["status"] == 0  # the NaN rows were never read
+    early = _run(_early(nb), schedule)
+    assert early["status"] == 0  # the NaN rows do not count
     assert np.array_equal(early["out_tokens"], clean["out_tokens"])
     assert np.array_equal(early["num_accepted"], clean["num_accepted"])
     full = run_gpu(nb)
     assert full["status"] & 0x1  # the full pass reads them
 
 
-def test_edge_rounds():
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_edge_rounds(schedule):
     # gamma = 0 requests, a long round, T = 0 and T > 0 mixed, unusable row at the stop
     rng = np.random.default_rng(5)
     V = 1024
@@ -112,7 +137,7 @@ def test_edge_rounds():
              target_logits=synth.f32_to_bf16_bits(logits), logits_dtype="bf16", draft_probs=None,
              temperature=np.array([1, 0, 1, 0.7, 0, 1, 1], np.float32), top_k=None, top_p=None,
              seed=9, request_base=0, flags=oracle.FLAG_EARLY_EXIT)
-    gpu = run_gpu(b)
+    gpu = _run(b, schedule)
     ref = oracle.verify(b)
     assert gpu["status"] & 0x1
     assert_parity(compare(b, gpu, ref))

@@ -227,7 +227,7 @@ def test_bounded_wait_times_out_and_the_context_survives():
     b["flags"] = sv.FLAG_EARLY_EXIT
     R = b["target_logits"].shape[0]
     ver = sv.Verifier(max_batch=16, max_rows=R, max_vocab=20000,
-                      config_flags=sv.CONFIG_TEST_WAIT_TIMEOUT)
+                      config_flags=sv.CONFIG_TEST_WAIT_TIMEOUT | sv.CONFIG_EARLY_QUEUE)
     db = sv.upload(b, "cuda:0")
     ver.run(db)
     torch.cuda.synchronize()
