@@ -73,8 +73,10 @@ extern "C" {
 #define SPEC_STATUS_BAD_TOKEN 0x4u      /* draft token id outside [0, V) */
 #define SPEC_STATUS_EMPTY_RESIDUAL 0x8u /* all residual weights 0: raced on p */
 #define SPEC_STATUS_BAD_OFFSETS 0x10u   /* cu_num_draft not 0 .. N, non-decreasing */
-#define SPEC_STATUS_TIMEOUT 0x20u       /* an on-chip pipeline wait gave up (the
-                                           outputs of the call are not valid) */
+#define SPEC_STATUS_TIMEOUT 0x20u       /* an on-chip pipeline wait gave up: the
+                                           outputs of the call are not valid, and
+                                           the handle's workspace may be left
+                                           dirty (destroy it and create another) */
 #define SPEC_STATUS_UNSETTLED 0x40u     /* vocab-sharded call: a top-k / top-p row
                                            the window histogram could not settle;
                                            its request emits nothing */
