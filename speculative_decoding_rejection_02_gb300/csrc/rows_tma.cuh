@@ -1,18 +1,21 @@
-// Persistent, bulk-copy pipelined target-row pass for argmax-only and
-// plain-softmax rows (the same statistics as k_rows_stream, for rows whose
-// byte length is a multiple of 16).
+// Persistent, bulk-copy pipelined target-row pass (the same statistics as
+// k_rows_stream, for rows whose byte length is a multiple of 16).
 //
 // Each CTA owns rows blockIdx.x, blockIdx.x + gridDim.x, ... and streams
 // every row exactly once from HBM through a ring of shared-memory stages:
 //  * warp 16 (producer) looks up the next row's request and settings with
 //    warp-parallel loads while the current row streams, and lane 0 issues
-//    one 1-D bulk copy (TMA) per 32 KB stage, signalling an mbarrier;
+//    one 1-D bulk copy (TMA) per stage, signalling an mbarrier;
 //  * warps 0..15 (consumers) wait on the stage, fold it into per-thread
 //    (max, lowest argmax, online sum of exp2((l - m) log2e / T)) in
 //    registers, capture the logit at the row's draft token, release the
 //    stage, and at the row's end reduce over the 512 consumers and write the
 //    row statistics and p(x).
-// No slice partials and no atomics: a row never leaves its CTA.
+// Variants (template flags below): rows with top-k / top-p also counted
+// into the window histogram (FILT); rows taken from the early-exit work
+// queue and judged at their end, possibly in parts (EARLY); one rank's
+// columns of a vocab-sharded call, exporting local statistics (SHARD).
+// Without parts a row never leaves its CTA.
 #pragma once
 #include "common.cuh"
 #include "pipe.cuh"
