@@ -235,3 +235,51 @@ def test_bounded_wait_times_out_and_the_context_survives():
     ver.close()
     gpu, _ = check(b)
     assert gpu["status"] == 0
+
+
+TOP_P_CASES = ["late_max", "one_far_logit", "masked_first_stage", "flat_rows", "tiny_top_p",
+               "wide_top_p", "far_negative"]
+
+
+@pytest.mark.parametrize("case", TOP_P_CASES)
+def test_top_p_only_multi_stage_cases(case):
+    """Top-p without top-k on aligned bf16 rows of several 12288-element
+    stages of the filtered row pass: the row max far above the first
+    stage's, one logit far above the rest, a first stage of -inf only, rows
+    of one or two values, top-p sets of one token and of nearly the whole
+    row, and logits far below zero."""
+    rng = np.random.default_rng(TOP_P_CASES.index(case) + 301)
+    V, B = 37864, 12
+    g = rng.integers(0, 4, size=B)
+    N = int(g.sum())
+    R = N + B
+    temps = rng.choice([0.5, 1.0, 2.0], size=B)
+    tp = rng.choice([0.3, 0.9, 0.99], size=B)
+    logits = rng.normal(0, 2, size=(R, V))
+    if case == "late_max":
+        cols = 20000 + rng.integers(0, 17000, size=R)
+        logits[np.arange(R), cols] = 20.0
+        logits[: R // 2, cols[0] // 2 + 14000] = 12.0
+    elif case == "one_far_logit":
+        logits[:, :12288] = rng.normal(0, 0.5, size=(R, 12288))
+        logits[np.arange(R), 25000 + rng.integers(0, 12000, size=R)] = 150.0
+        temps = np.full(B, 0.5)
+    elif case == "masked_first_stage":
+        logits[:, :13000] = -np.inf
+    elif case == "flat_rows":
+        logits[:] = 0.75
+        logits[::3, ::7] = 0.5
+    elif case == "tiny_top_p":
+        tp = np.full(B, 0.001)
+    elif case == "wide_top_p":
+        logits = rng.normal(0, 6, size=(R, V))
+        tp = rng.choice([0.999, 0.99999], size=B)
+    else:
+        logits = rng.normal(-180, 3, size=(R, V))
+        temps = rng.choice([0.25, 1.0], size=B)
+    q = rng.random((N, V)) ** 2
+    q /= q.sum(1, keepdims=True)
+    ids = np.array([rng.choice(V, p=q[n]) for n in range(N)], np.int32)
+    b = make_batch(logits, g, ids, temps, q, None, tp, dtype="bf16", seed=29)
+    gpu, _ = check(b)
+    assert gpu["status"] & ~np.uint32(0x8) == 0
