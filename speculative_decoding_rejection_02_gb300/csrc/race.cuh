@@ -259,6 +259,7 @@ k_race(Params P) {
   __shared__ RaceItem queue[kRaceThreads * kRaceGroups];
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_staged;
+  __shared__ unsigned long long s_lb;
 
   const unsigned n_race = *P.race_count;
   const unsigned t = blockIdx.x;
@@ -273,9 +274,6 @@ k_race(Params P) {
   const RaceView v = race_view(P, r, task.row, task.qrow, task.kstar,
                                P.sh_skip ? (int)kRaceP : task.mode, task.x, task.m, task.c,
                                task.inv_z, task.theta, task.z);
-  // The best so far (seeded by the accept scan, raised by earlier slices),
-  // read now so that its latency overlaps the copies below.
-  const unsigned long long lb = __ldcg(P.race_best + slot);
   const int V = P.V;
   const uint32_t groups = (uint32_t)((V + 3) / 4);
   const int slice_n = race_slice(P.q != nullptr);
@@ -304,8 +302,14 @@ k_race(Params P) {
       bulk_load(lbuf, lsrc, lbytes, &bar);
       if (resid) bulk_load(qbuf, qsrc, qbytes, &bar);
     }
+    // The best so far (seeded by the accept scan, raised by other slices
+    // as they finish), read once while the copies fly: the whole block must
+    // start from the same value, since it decides below whether the block
+    // takes the branch with block-wide barriers.
+    s_lb = __ldcg(P.race_best + slot);
   }
   __syncthreads();
+  const unsigned long long lb = s_lb;
   const bool staged = s_staged != 0;
   if (staged) {
     // Every thread waits for the copies (bounded); all agree on the outcome.

@@ -283,3 +283,21 @@ def test_top_p_only_multi_stage_cases(case):
     b = make_batch(logits, g, ids, temps, q, None, tp, dtype="bf16", seed=29)
     gpu, _ = check(b)
     assert gpu["status"] & ~np.uint32(0x8) == 0
+
+
+def test_masked_races_repeat_exactly():
+    """Every draft token is its row's argmax and one-hot, so each rejection
+    races with the argmax masked and no seeded best: the race's first slice
+    starts from its own heaviest entry while later slices publish theirs.
+    Sixteen calls must all give the oracle's tokens (a block that disagreed
+    about its starting best once paired a weight with the wrong index)."""
+    rng = np.random.default_rng(404)
+    V, B = 131072, 256
+    g = np.ones(B, np.int32)
+    logits = rng.normal(0, 2, size=(2 * B, V)).astype(np.float32)
+    ids = np.argmax(synth.bf16_bits_to_f32(synth.f32_to_bf16_bits(logits))[0::2], axis=1)
+    b = make_batch(logits, g, ids.astype(np.int32), np.ones(B), dtype="bf16", seed=41)
+    ref = oracle.verify(b)
+    for _ in range(16):
+        gpu = run_gpu(b)
+        assert_parity(compare(b, gpu, ref))
