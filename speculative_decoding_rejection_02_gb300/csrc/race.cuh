@@ -42,10 +42,18 @@ constexpr int kRaceGroups = 4;    // groups of 4 entries per thread per batch
 // Above 1 / E_min, E_min = -ln(1 - 2^-24) ~ 5.96e-8 the smallest E a race
 // uniform can give: no entry scores more than w * kInvEMin.
 constexpr float kInvEMin = 1.7e7f;
-// Shared memory of the staged path: the slice's logits and, when the call
-// has draft probabilities, theirs (fp32).
+// Units of 8 consecutive entries (two Philox groups) per thread of a staged
+// slice, and the shared-memory queue of 16-bit group indices that holds up
+// to two per unit.
+__host__ __device__ constexpr int race_units(bool has_q) { return race_slice(has_q) / 8 / kRaceThreads; }
+__host__ __device__ constexpr size_t race_queue_bytes(bool has_q) {
+  return (size_t)kRaceThreads * 2 * race_units(has_q) * sizeof(uint16_t);
+}
+// Shared memory of the staged path: the slice's logits, when the race is
+// on residual weights the slice's draft probabilities (fp32), and the queue.
 __host__ __device__ constexpr size_t race_smem_bytes(int logit_bytes, bool has_q) {
-  return has_q ? (size_t)kRaceSlice * (logit_bytes + 4) : (size_t)kRaceSliceNoQ * logit_bytes;
+  return has_q ? (size_t)kRaceSlice * (logit_bytes + 4) + race_queue_bytes(true)
+               : (size_t)kRaceSliceNoQ * logit_bytes + race_queue_bytes(false);
 }
 // The largest of the above.
 constexpr size_t kRaceSmemMax = race_smem_bytes(4, true) > race_smem_bytes(4, false)
@@ -251,12 +259,218 @@ __device__ void race_range_global(const Params& P, const RaceView& v, int mode, 
   }
 }
 
+// ---------------------------------------------------------------------------
+// Scoring of a slice staged in shared memory
+// ---------------------------------------------------------------------------
+// The slice holds n entries (n a multiple of 4), logits at `lbuf` and, for a
+// race on residual weights (HAS_Q), draft probabilities at `qbuf`. Thread t
+// takes the units (8 entries, two Philox groups) t, t + blockDim.x, ...:
+//  1. per group, the logit floor of the best so far, then the weights and
+//     the kInvEMin bound decide whether the group needs its Philox draw;
+//  2. the warp packs the groups that do into its queue (one prefix sum);
+//  3. the lanes take the queued groups one each, recompute the weights,
+//     draw, and score only entries whose bound w / (1 - U) can reach the
+//     lane's best.
+// The arithmetic of p and w is race_p / race_w's (packed in pairs, the same
+// IEEE operations), so scores equal those of the global-memory path. A
+// masked draft token was set to -inf in the staged slice by the caller: its
+// p, and so its weight, is 0.
+
+// The 8 logits of unit u (fp32 slices: the second half of a tail unit may
+// lie past n; the caller ignores it).
+template <bool BF16>
+__device__ __forceinline__ void race_unit_logits(const unsigned char* lbuf, int u, float l[8]) {
+  if (BF16) {
+    const uint4 b = reinterpret_cast<const uint4*>(lbuf)[u];
+    l[0] = bf16_lo(b.x); l[1] = bf16_hi(b.x); l[2] = bf16_lo(b.y); l[3] = bf16_hi(b.y);
+    l[4] = bf16_lo(b.z); l[5] = bf16_hi(b.z); l[6] = bf16_lo(b.w); l[7] = bf16_hi(b.w);
+  } else {
+    const float4 a = reinterpret_cast<const float4*>(lbuf)[2 * u];
+    const float4 b = reinterpret_cast<const float4*>(lbuf)[2 * u + 1];
+    l[0] = a.x; l[1] = a.y; l[2] = a.z; l[3] = a.w;
+    l[4] = b.x; l[5] = b.y; l[6] = b.z; l[7] = b.w;
+  }
+}
+
+// The 4 logits of group g.
+template <bool BF16>
+__device__ __forceinline__ void race_group_logits(const unsigned char* lbuf, int g, float l[4]) {
+  if (BF16) {
+    const uint2 b = reinterpret_cast<const uint2*>(lbuf)[g];
+    l[0] = bf16_lo(b.x); l[1] = bf16_hi(b.x); l[2] = bf16_lo(b.y); l[3] = bf16_hi(b.y);
+  } else {
+    const float4 a = reinterpret_cast<const float4*>(lbuf)[g];
+    l[0] = a.x; l[1] = a.y; l[2] = a.z; l[3] = a.w;
+  }
+}
+
+// Weights of one group: p = ex2(l c - m c) / Z (0 below theta when THETA),
+// and w = max(p - q, 0) when HAS_Q, else w = p.
+template <bool HAS_Q, bool THETA>
+__device__ __forceinline__ void race_w4(const float l[4], const float4 q, const RaceView& v,
+                                        float w[4]) {
+  const unsigned long long c2 = f2_pack(v.c, v.c);
+  const unsigned long long nmc2 = f2_pack(-v.mc, -v.mc);
+  const unsigned long long iz2 = f2_pack(v.inv_z, v.inv_z);
+  const float qq[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    float z0, z1;
+    f2_unpack(f2_fma(f2_pack(l[2 * t], l[2 * t + 1]), c2, nmc2), z0, z1);
+    unsigned long long p2 = f2_mul(f2_pack(ex2(z0), ex2(z1)), iz2);
+    if (HAS_Q) p2 = f2_sub(p2, f2_pack(qq[2 * t], qq[2 * t + 1]));
+    f2_unpack(p2, w[2 * t], w[2 * t + 1]);
+  }
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (HAS_Q) w[e] = fmaxf(w[e], 0.f);
+    if (THETA) w[e] = (l[e] >= v.theta) ? w[e] : 0.f;
+  }
+}
+
+__device__ __forceinline__ float max4(const float a[4]) {
+  return fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
+}
+
+// The heaviest entry of the slice in this thread's units (lowest index on
+// ties): the race's first bound when nothing better is known.
+template <bool BF16, bool HAS_Q, bool THETA>
+__device__ void race_slice_heaviest(const RaceView& v, const unsigned char* lbuf,
+                                    const float* qbuf, int n, int j0, float& wb, int& jb) {
+  const int units = (n + 7) >> 3;
+  for (int u = threadIdx.x; u < units; u += blockDim.x) {
+    float l[8], w[8];
+    race_unit_logits<BF16>(lbuf, u, l);
+    const float4 q0 = HAS_Q ? reinterpret_cast<const float4*>(qbuf)[2 * u] : make_float4(0, 0, 0, 0);
+    const float4 q1 = HAS_Q ? reinterpret_cast<const float4*>(qbuf)[2 * u + 1] : make_float4(0, 0, 0, 0);
+    race_w4<HAS_Q, THETA>(l, q0, v, w);
+    race_w4<HAS_Q, THETA>(l + 4, q1, v, w + 4);
+    const int ne = min(8, n - 8 * u);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (e < ne && w[e] > wb) {
+        wb = w[e];
+        jb = j0 + 8 * u + e;
+      }
+  }
+}
+
+template <bool BF16, bool HAS_Q, bool THETA>
+__device__ void race_slice_smem(const Params& P, const RaceView& v, const unsigned char* lbuf,
+                                const float* qbuf, int n, int j0, float& best, int& best_j,
+                                uint16_t* queue) {
+  // Units per thread: at most those of the larger slice; the queue holds
+  // two groups per unit of this call's slice size.
+  constexpr int kUnits = race_units(false);
+  const int upt = race_units(P.q != nullptr);
+  const int lane = threadIdx.x & 31;
+  const int units = (n + 7) >> 3;
+  const float cut = best;
+  const float lthr = race_logit_floor(v, best);
+
+  // 1. Which of this thread's groups need their draw (bit 2k + h: group h
+  // of the thread's k-th unit).
+  uint32_t need = 0;
+#pragma unroll 2
+  for (int k = 0; k < kUnits; ++k) {
+    const int u = (int)threadIdx.x + k * (int)blockDim.x;
+    if (u >= units) break;
+    float l[8];
+    race_unit_logits<BF16>(lbuf, u, l);
+    const float m0 = max4(l);
+    const float m1 = (8 * u + 8 <= n) ? max4(l + 4) : -INFINITY;
+    const bool a0 = m0 > lthr, a1 = m1 > lthr;
+    if (a0 || a1) {
+      const float4 q0 = HAS_Q ? reinterpret_cast<const float4*>(qbuf)[2 * u] : make_float4(0, 0, 0, 0);
+      const float4 q1 = HAS_Q ? reinterpret_cast<const float4*>(qbuf)[2 * u + 1] : make_float4(0, 0, 0, 0);
+      float w[8];
+      race_w4<HAS_Q, THETA>(l, q0, v, w);
+      race_w4<HAS_Q, THETA>(l + 4, q1, v, w + 4);
+      const float w0 = max4(w), w1 = max4(w + 4);
+      if (a0 && w0 > 0.f && w0 * kInvEMin > cut) need |= 1u << (2 * k);
+      if (a1 && w1 > 0.f && w1 * kInvEMin > cut) need |= 2u << (2 * k);
+    }
+  }
+
+  // 2. Pack them into the warp's queue.
+  const int cnt = __popc(need);
+  int incl = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+  uint16_t* qw = queue + (threadIdx.x >> 5) * (32 * 2 * upt);
+  int at = incl - cnt;
+  while (need) {
+    const int b = __ffs(need) - 1;
+    need &= need - 1u;
+    const int u = (int)threadIdx.x + (b >> 1) * (int)blockDim.x;
+    qw[at++] = (uint16_t)(2 * u + (b & 1));
+  }
+  __syncwarp();
+
+  // 3. Draw and score the queued groups on dense lanes.
+  const uint32_t gbase = v.g0 + ((uint32_t)j0 >> 2);
+  for (int t = lane; t < total; t += 32) {
+    const int g = qw[t];
+    float l[4], w[4];
+    race_group_logits<BF16>(lbuf, g, l);
+    const float4 q = HAS_Q ? reinterpret_cast<const float4*>(qbuf)[g] : make_float4(0, 0, 0, 0);
+    race_w4<HAS_Q, THETA>(l, q, v, w);
+    const uint4 r = race_words(P.seed, v.greq, v.kstar, gbase + (uint32_t)g);
+    const uint32_t words[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      // -ln U >= 1 - U, so w / (1 - U) bounds the score; 1 - U is exact and
+      // the factor (1 + 2e-6) covers the roundings of the score and of this
+      // test. Entries that fail cannot reach this lane's best (nor tie it).
+      const float v1 = 1.f - race_uniform_from_word(words[e]);
+      if (w[e] > 0.f && w[e] * 1.000002f > best * v1) {
+        const float sc = race_score(w[e], words[e]);
+        const int j = j0 + 4 * g + e;
+        if (sc > best || (sc == best && j < best_j)) {
+          best = sc;
+          best_j = j;
+        }
+      }
+    }
+  }
+}
+
+// Calls f(bf16, has_q, theta) with the three flags as compile-time
+// constants (std::integral_constant-like tags).
+template <bool B>
+struct RaceFlag {
+  static constexpr bool value = B;
+};
+template <typename F>
+__device__ __forceinline__ void race_dispatch(bool bf16, bool has_q, bool theta, F&& f) {
+  if (bf16) {
+    if (has_q) {
+      if (theta) f(RaceFlag<true>{}, RaceFlag<true>{}, RaceFlag<true>{});
+      else f(RaceFlag<true>{}, RaceFlag<true>{}, RaceFlag<false>{});
+    } else {
+      if (theta) f(RaceFlag<true>{}, RaceFlag<false>{}, RaceFlag<true>{});
+      else f(RaceFlag<true>{}, RaceFlag<false>{}, RaceFlag<false>{});
+    }
+  } else {
+    if (has_q) {
+      if (theta) f(RaceFlag<false>{}, RaceFlag<true>{}, RaceFlag<true>{});
+      else f(RaceFlag<false>{}, RaceFlag<true>{}, RaceFlag<false>{});
+    } else {
+      if (theta) f(RaceFlag<false>{}, RaceFlag<false>{}, RaceFlag<true>{});
+      else f(RaceFlag<false>{}, RaceFlag<false>{}, RaceFlag<false>{});
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kRaceThreads, 4)
 k_race(Params P) {
   extern __shared__ __align__(128) unsigned char race_smem[];
   __shared__ int s_last;
   __shared__ unsigned long long s_packed;
-  __shared__ RaceItem queue[kRaceThreads * kRaceGroups];
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_staged;
   __shared__ unsigned long long s_lb;
@@ -324,96 +538,41 @@ k_race(Params P) {
   // Packed with global indices, kept here as local ones.
   float best = lb ? __uint_as_float((uint32_t)(lb >> 32)) : 0.f;
   int best_j = lb ? (int)(0xFFFFFFFFu - (uint32_t)lb) - v.v0 : kNoIndex;
+  // Behind the staged slice: the queue of the staged scoring. Unstaged
+  // tasks use the slice area for the global path's queue instead.
+  uint16_t* queue = reinterpret_cast<uint16_t*>(
+      race_smem + (size_t)slice_n * esize + (P.q ? (size_t)slice_n * 4 : 0));
+  RaceItem* gqueue = reinterpret_cast<RaceItem*>(race_smem);
   if (v.z > 0.f) {
-    if (staged && best_j == kNoIndex) {
-      // No bound yet (the argmax token had weight 0 and no earlier slice has
-      // finished): score this slice's heaviest entry first and start from it.
-      float wb = 0.f;
-      int jb = kNoIndex;
-      for (int le = (int)threadIdx.x * 4; le < n; le += (int)blockDim.x * 4) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          if (le + e < n) {
-            const float lv = P.bf16 ? bf16_lo((uint32_t)*reinterpret_cast<const unsigned short*>(
-                                          lbuf + (size_t)(le + e) * 2))
-                                    : *reinterpret_cast<const float*>(lbuf + (size_t)(le + e) * 4);
-            const float qv = resid ? qbuf[le + e] : 0.f;
-            const int j = j0 + le + e;
-            const float w = race_w(race_p(lv, v), qv, j, v.mode, v.x);
-            if (w > wb) {
-              wb = w;
-              jb = j;
-            }
-          }
-        }
-      }
-      block_argmax(wb, jb);
-      if (jb != kNoIndex && wb > 0.f) {
-        const uint4 rw = race_words(P.seed, v.greq, v.kstar, v.g0 + ((uint32_t)jb >> 2));
-        const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
-        best = race_score(wb, words[jb & 3]);
-        best_j = jb;
-      }
-    }
     if (staged) {
-      float lthr = race_logit_floor(v, best);
-      RaceItem* qw = queue + (threadIdx.x >> 5) * (32 * kRaceGroups);
-      const uint32_t stride = blockDim.x;
-      const uint32_t span = stride * kRaceGroups;
-      for (uint32_t gw = g0 + (threadIdx.x & ~31u); gw < g1; gw += span) {
-        const uint32_t gb = gw + (threadIdx.x & 31u);
-        float l[kRaceGroups][4], q[kRaceGroups][4];
-        uint32_t gk[kRaceGroups];
-#pragma unroll
-        for (int k = 0; k < kRaceGroups; ++k) {
-          gk[k] = gb + (uint32_t)k * stride;
-          const int le = (int)((gk[k] - g0) * 4u);  // entry within the slice
-          const bool in = gk[k] < g1 && le + 3 < n;
-          if (in) {
-            if (P.bf16) {
-              const uint2 b = *reinterpret_cast<const uint2*>(lbuf + (size_t)le * 2);
-              l[k][0] = bf16_lo(b.x);
-              l[k][1] = bf16_hi(b.x);
-              l[k][2] = bf16_lo(b.y);
-              l[k][3] = bf16_hi(b.y);
-            } else {
-              const float4 f = *reinterpret_cast<const float4*>(lbuf + (size_t)le * 4);
-              l[k][0] = f.x; l[k][1] = f.y; l[k][2] = f.z; l[k][3] = f.w;
-            }
-            if (resid) {
-              const float4 f = *reinterpret_cast<const float4*>(qbuf + le);
-              q[k][0] = f.x; q[k][1] = f.y; q[k][2] = f.z; q[k][3] = f.w;
-            } else {
-              q[k][0] = q[k][1] = q[k][2] = q[k][3] = 0.f;
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const bool ine = gk[k] < g1 && le + e < n;
-              l[k][e] = ine ? (P.bf16 ? bf16_lo((uint32_t)*reinterpret_cast<const unsigned short*>(
-                                            lbuf + (size_t)(le + e) * 2))
-                                      : *reinterpret_cast<const float*>(lbuf + (size_t)(le + e) * 4))
-                            : -INFINITY;
-              q[k][e] = (ine && resid) ? qbuf[le + e] : 0.f;
-            }
+      // A one-hot draft's token is masked by giving it logit -inf here.
+      if (v.mode == kRaceMasked && v.x >= j0 && v.x < j0 + n && threadIdx.x == 0) {
+        if (P.bf16) reinterpret_cast<unsigned short*>(lbuf)[v.x - j0] = 0xFF80u;
+        else reinterpret_cast<float*>(lbuf)[v.x - j0] = -INFINITY;
+      }
+      __syncthreads();
+      const bool theta = v.theta > -INFINITY;
+      race_dispatch(P.bf16 != 0, resid, theta, [&](auto bf16, auto hq, auto th) {
+        constexpr bool kB = decltype(bf16)::value, kQ = decltype(hq)::value,
+                       kT = decltype(th)::value;
+        if (best_j == kNoIndex) {
+          // No bound yet (the argmax token had weight 0 and no earlier slice
+          // has finished): score this slice's heaviest entry first.
+          float wb = 0.f;
+          int jb = kNoIndex;
+          race_slice_heaviest<kB, kQ, kT>(v, lbuf, qbuf, n, j0, wb, jb);
+          block_argmax(wb, jb);
+          if (jb != kNoIndex && wb > 0.f) {
+            const uint4 rw = race_words(P.seed, v.greq, v.kstar, v.g0 + ((uint32_t)jb >> 2));
+            const uint32_t words[4] = {rw.x, rw.y, rw.z, rw.w};
+            best = race_score(wb, words[jb & 3]);
+            best_j = jb;
           }
         }
-        race_batch(P, v, v.mode, gk, g1, l, q, best, best_j, lthr, qw,
-                   [&](uint32_t g, float* lf, float* qf) {
-#pragma unroll
-                     for (int e = 0; e < 4; ++e) {
-                       const int le = (int)((g - g0) * 4u) + e;
-                       const bool in = le < n;
-                       lf[e] = in ? (P.bf16 ? bf16_lo((uint32_t)*reinterpret_cast<
-                                                      const unsigned short*>(lbuf + (size_t)le * 2))
-                                            : *reinterpret_cast<const float*>(lbuf + (size_t)le * 4))
-                                  : -INFINITY;
-                       qf[e] = (in && resid) ? qbuf[le] : 0.f;
-                     }
-                   });
-      }
+        race_slice_smem<kB, kQ, kT>(P, v, lbuf, qbuf, n, j0, best, best_j, queue);
+      });
     } else {
-      race_range_global(P, v, v.mode, g0, g1, best, best_j, queue);
+      race_range_global(P, v, v.mode, g0, g1, best, best_j, gqueue);
     }
   }
   block_argmax(best, best_j);
@@ -442,7 +601,7 @@ k_race(Params P) {
     // Every weight was 0 (rounding only): draw from p over the whole row.
     float b2 = 0.f;
     int j2 = kNoIndex;
-    if (v.z > 0.f) race_range_global(P, v, kRaceP, 0u, groups, b2, j2, queue);
+    if (v.z > 0.f) race_range_global(P, v, kRaceP, 0u, groups, b2, j2, gqueue);
     block_argmax(b2, j2);
     tok = (j2 == kNoIndex) ? 0 : j2;
     if (threadIdx.x == 0) atomicOr(P.status, SPEC_STATUS_EMPTY_RESIDUAL);
