@@ -116,8 +116,9 @@ def algorithmic_bytes(batch, num_accepted) -> dict:
     needed = int(np.minimum(num_accepted + 1, gam + 1).sum()) * V * esize
     if int(batch.get("flags", 0)) & 4:
         rows = needed
-    return dict(row_pass=rows, race_q=q_rows, small=small, total=rows + q_rows + small,
-                rows_to_first_rejection=needed, all_rows=R * V * esize)
+    return dict(row_pass=rows, race_q=q_rows, q_gathers=judged_q, small=small,
+                total=rows + q_rows + small, rows_to_first_rejection=needed,
+                all_rows=R * V * esize)
 
 
 class ClockSampler:
@@ -363,11 +364,14 @@ def main():
     achieved = bytes_["row_pass"] / (rows_avg * 1e-3) / 1e9
     step_gbs = bytes_["total"] / (ms_per_step * 1e-3) / 1e9
 
-    # End to end through the public API with host buffers.
+    # End to end through the public API with host buffers. draft_probs stays
+    # in page-locked host memory, which the library reads in place (only the
+    # gathered q(x) and the rows of rejected requests cross the host link);
+    # the other inputs are copied to the device every step.
     e2e = None
     if args.e2e_steps > 0:
         host = {}
-        for k in ("cu_num_draft", "draft_token_ids", "target_logits", "draft_probs",
+        for k in ("cu_num_draft", "draft_token_ids", "target_logits",
                   "temperature", "top_k", "top_p"):
             a = batch.get(k)
             if a is None:
@@ -376,11 +380,21 @@ def main():
                 a = np.ascontiguousarray(a).view(np.int16)
             host[k] = torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
         dst = {"cu_num_draft": db.cu_num_draft, "draft_token_ids": db.draft_token_ids,
-               "target_logits": db.target_logits, "draft_probs": db.draft_probs,
+               "target_logits": db.target_logits,
                "temperature": db.temperature, "top_k": db.top_k, "top_p": db.top_p}
+        hb = sv.DeviceBatch(cu_num_draft=db.cu_num_draft, draft_token_ids=db.draft_token_ids,
+                            target_logits=db.target_logits, draft_probs=None,
+                            temperature=db.temperature, top_k=db.top_k, top_p=db.top_p,
+                            seed=db.seed, request_base=db.request_base, flags=db.flags,
+                            out_tokens=db.out_tokens, num_accepted=db.num_accepted,
+                            N=db.N, V=db.V)
+        q_read = 0
+        if batch["draft_probs"] is not None:
+            hb.draft_probs = torch.from_numpy(batch["draft_probs"]).pin_memory()
+            q_read = bytes_["race_q"] + bytes_["q_gathers"]
         out_tok = torch.empty(R, dtype=torch.int32).pin_memory()
         out_acc = torch.empty(B, dtype=torch.int32).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        h2d = sum(t.numel() * t.element_size() for t in host.values()) + q_read
         d2h = out_tok.numel() * 4 + out_acc.numel() * 4
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
@@ -391,15 +405,20 @@ def main():
             for k, t in host.items():
                 d = dst[k]
                 d.view(t.dtype).reshape(-1).copy_(t.reshape(-1), non_blocking=True)
-            ver.run(db, stream)
+            ver.run(hb, stream)
             out_tok.copy_(db.out_tokens, non_blocking=True)
             out_acc.copy_(db.num_accepted, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev) / args.e2e_steps
+        torch.cuda.synchronize(dev)
+        assert ver.status() == 0, "device status bits set (end-to-end calls)"
+        assert np.array_equal(out_acc.numpy(), n_acc), "end-to-end outcome differs"
         e2e = {"value": world * positions / (e2e_ms * 1e-3), "unit": "draft_positions/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e2e_ms}
+               "ms_per_step": e2e_ms,
+               "draft_probs": ("page-locked host memory read in place" if q_read
+                               else "none (one-hot draft)")}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -143,9 +143,15 @@ typedef struct {
                                   the gamma_r + 1 rows of request r are rows
                                   cu[r] + r .. cu[r+1] + r */
   spec_dtype logits_dtype;     /* SPEC_F32 or SPEC_BF16 */
-  const float* draft_probs;    /* [N x V] device fp32 (row cu[r] + i is q_i of
+  const float* draft_probs;    /* [N x V] fp32 (row cu[r] + i is q_i of
                                   request r), or NULL: one-hot greedy draft,
-                                  q_i(x_i) = 1 */
+                                  q_i(x_i) = 1. Device memory, or page-locked
+                                  host memory (cudaHostAlloc / registered),
+                                  which the kernels read in place: only the
+                                  gathered q_i(x_i) and the rows of rejected
+                                  requests cross the host link. Pageable host
+                                  memory: SPEC_ERR_INVALID_ARG. The memory
+                                  must not change until the call completes. */
   const float* temperature;    /* [B] device; 0 => argmax-match path; > 0 */
   const int* top_k;            /* [B] device or NULL; <= 0 or >= V => off */
   const float* top_p;          /* [B] device or NULL; >= 1 => off; in (0, 1] */

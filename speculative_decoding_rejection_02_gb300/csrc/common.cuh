@@ -92,6 +92,7 @@ struct Params {
   const void* logits;
   int bf16;  // 1: bf16 logits, 0: fp32
   const float* q;
+  int q_host;  // 1: q is page-locked host memory (read with plain loads)
   const float* temp;
   const int* top_k;
   const float* top_p;

@@ -510,11 +510,14 @@ k_race(Params P) {
                                 (qbytes % 16 == 0)));
     s_staged = ok ? 1 : 0;
     if (ok) {
+      // Draft probabilities in host memory are staged by the threads below
+      // with 16-byte plain loads; the bulk copies take device memory only.
+      const bool q_bulk = resid && !P.q_host;
       mbar_init(&bar, 1);
       fence_mbar_init();
-      mbar_arrive_expect_tx(&bar, lbytes + qbytes);
+      mbar_arrive_expect_tx(&bar, lbytes + (q_bulk ? qbytes : 0u));
       bulk_load(lbuf, lsrc, lbytes, &bar);
-      if (resid) bulk_load(qbuf, qsrc, qbytes, &bar);
+      if (q_bulk) bulk_load(qbuf, qsrc, qbytes, &bar);
     }
     // The best so far (seeded by the accept scan, raised by other slices
     // as they finish), read once while the copies fly: the whole block must
@@ -525,6 +528,26 @@ k_race(Params P) {
   __syncthreads();
   const unsigned long long lb = s_lb;
   const bool staged = s_staged != 0;
+  if (staged && resid && P.q_host) {
+    // n / 4 16-byte vectors (n is a multiple of 4 here); all loads of a
+    // thread are issued before its stores.
+    constexpr int kVec = kRaceSlice / 4 / kRaceThreads;
+    const uint4* src = reinterpret_cast<const uint4*>(qsrc);
+    uint4* dst = reinterpret_cast<uint4*>(qbuf);
+    const int nv = n / 4;
+    uint4 t4[kVec];
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const int i = (int)threadIdx.x + k * kRaceThreads;
+      if (i < nv) t4[k] = ldg_stream(src + i);
+    }
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const int i = (int)threadIdx.x + k * kRaceThreads;
+      if (i < nv) dst[i] = t4[k];
+    }
+    __syncthreads();
+  }
   if (staged) {
     // Every thread waits for the copies (bounded); all agree on the outcome.
     if (!__syncthreads_and(mbar_wait(&bar, 0) ? 1 : 0)) {

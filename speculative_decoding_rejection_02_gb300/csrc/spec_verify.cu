@@ -99,6 +99,27 @@ int check_batch(const spec_verify_config* cfg, const spec_verify_batch* b, bool 
   return SPEC_OK;
 }
 
+// Where draft_probs lives: device (or managed) memory, or page-locked host
+// memory that the device reads in place (its device alias is used; the race
+// then reads those rows with plain loads). Pageable host memory is rejected.
+int resolve_q(sv::Params& P) {
+  P.q_host = 0;
+  if (!P.q) return SPEC_OK;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, P.q) != cudaSuccess) {
+    cudaGetLastError();
+    return SPEC_ERR_INVALID_ARG;
+  }
+  if (a.type == cudaMemoryTypeHost) {
+    if (!a.devicePointer) return SPEC_ERR_INVALID_ARG;
+    P.q = static_cast<const float*>(a.devicePointer);
+    P.q_host = 1;
+  } else if (a.type == cudaMemoryTypeUnregistered) {
+    return SPEC_ERR_INVALID_ARG;
+  }
+  return SPEC_OK;
+}
+
 // The kernel parameters of a call: the batch and the handle's workspace.
 sv::Params make_params(spec_verify_handle* h, const spec_verify_batch* b, bool greedy) {
   sv::Params P;
@@ -111,6 +132,7 @@ sv::Params make_params(spec_verify_handle* h, const spec_verify_batch* b, bool g
   P.logits = b->target_logits;
   P.bf16 = (b->logits_dtype == SPEC_BF16) ? 1 : 0;
   P.q = greedy ? nullptr : b->draft_probs;
+  P.q_host = 0;
   P.temp = b->temperature;
   P.top_k = greedy ? nullptr : b->top_k;
   P.top_p = greedy ? nullptr : b->top_p;
@@ -161,6 +183,8 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   if (cudaSetDevice(h->cfg.device) != cudaSuccess) return SPEC_ERR_CUDA;
 
   sv::Params P = make_params(h, b, greedy);
+  rc = resolve_q(P);
+  if (rc != SPEC_OK) return rc;
   const long long R = (long long)b->N + b->B;
   const bool match = !greedy && (P.flags & SPEC_FLAG_SAMPLER_MATCH);
   // Races: one per request (its k* row), or one per row under sampler-match.
@@ -449,6 +473,8 @@ static int shard_setup(spec_verify_handle* h, const spec_verify_batch* b, const 
     return SPEC_ERR_INVALID_ARG;
   if (cudaSetDevice(h->cfg.device) != cudaSuccess) return SPEC_ERR_CUDA;
   P = make_params(h, b, false);
+  rc = resolve_q(P);
+  if (rc != SPEC_OK) return rc;
   P.shard = 1;
   P.v0 = (int)sh->v0;
   P.Vg = sh->V_global;

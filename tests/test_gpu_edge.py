@@ -301,3 +301,46 @@ def test_masked_races_repeat_exactly():
     for _ in range(16):
         gpu = run_gpu(b)
         assert_parity(compare(b, gpu, ref))
+
+
+@pytest.mark.parametrize("name,B,V", [("c2", 8, 32000), ("c3", 24, 20008), ("c3", 24, 20011),
+                                      ("c5", 40, 20008)])
+def test_draft_probs_in_page_locked_host_memory(name, B, V):
+    """draft_probs left in page-locked host memory is read in place: the same
+    outputs as with the rows on the device, and parity with the oracle."""
+    import torch
+
+    import speculative_decoding_rejection_02_gb300 as sv
+    batch = synth.make(name, B=B, V=V)
+    R = batch["target_logits"].shape[0]
+    ver = sv.Verifier(max_batch=B, max_rows=R, max_vocab=V)
+    on_dev = sv.upload(batch, "cuda:0")
+    ver.run(on_dev)
+    on_host = sv.upload(batch, "cuda:0")
+    on_host.draft_probs = torch.from_numpy(batch["draft_probs"]).pin_memory()
+    ver.run(on_host)
+    torch.cuda.synchronize()
+    assert ver.status() == 0
+    assert torch.equal(on_dev.num_accepted, on_host.num_accepted)
+    assert torch.equal(on_dev.out_tokens, on_host.out_tokens)
+    assert torch.equal(on_dev.p_at_draft, on_host.p_at_draft)
+    gpu = dict(out_tokens=on_host.out_tokens.cpu().numpy(),
+               num_accepted=on_host.num_accepted.cpu().numpy(),
+               p_at_draft=on_host.p_at_draft.cpu().numpy(), status=0)
+    assert_parity(compare(batch, gpu, oracle.verify(batch)))
+    ver.close()
+
+
+def test_pageable_draft_probs_are_rejected():
+    import torch
+
+    import speculative_decoding_rejection_02_gb300 as sv
+    batch = synth.make("c2", B=2, V=64)
+    R = batch["target_logits"].shape[0]
+    ver = sv.Verifier(max_batch=2, max_rows=R, max_vocab=64)
+    db = sv.upload(batch, "cuda:0")
+    db.draft_probs = torch.from_numpy(batch["draft_probs"])  # not page-locked
+    with pytest.raises(sv.SpecVerifyError) as err:
+        ver.run(db)
+    assert err.value.code == -1
+    ver.close()
