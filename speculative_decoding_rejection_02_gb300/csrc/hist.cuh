@@ -14,17 +14,18 @@
 // While the row streams, each thread drops an element unless it lies at or
 // above (its own running max) - D; every running max is at most m, so every
 // element at or above m - D is counted. A counted element adds 1 to the
-// counter of its value: one 32-bit counter per bf16 value of magnitude in
-// [2^-16, 2^8) (24 binades x 128 values per sign, 24 KB), plus one merged
-// counter per sign for the magnitudes below 2^-16, which also sums the
-// weights 2^(l c) of its members. A counted value of magnitude 2^8 or more
-// (or +inf) sends the row to the exact slow path.
+// counter of its value: per sign, one 32-bit counter per bf16 magnitude in
+// [2^-16, 2^8) (3072 values), one for all smaller magnitudes (taken at value
+// 0) and one for 2^8 and above (+inf included), which sends the row to the
+// exact slow path. The counter of a bf16 word's two values comes from a few
+// packed 16-bit operations (magnitude clamp, sign offset), one predicated
+// shared-memory add each.
 //
 // At the row's end the consumers turn counts into masses n 2^(v c - m c),
 // scan the values from the largest down and read off the top-k and top-p
 // thresholds, Z over the kept set and the kept set itself: exact for every
 // value, one read of the row, no sort, no per-element exp beyond the row
-// sum. The row goes to the slow path when a threshold falls on a merged
+// sum. The row goes to the slow path when a threshold falls on a tiny-value
 // counter or outside the window (top-k with fewer than k tokens in it), or
 // when the row holds NaN or +inf.
 #pragma once
@@ -35,27 +36,37 @@ namespace sv {
 
 constexpr unsigned kPendingSlow = 0x80000000u;  // row left to the exact slow path
 
-constexpr int kWinELo = 111;                 // biased exponent of 2^-16
-constexpr int kWinBinades = 24;              // magnitudes 2^-16 .. 2^8
-constexpr int kWinHalf = kWinBinades * 128;  // single-value counters per sign
-constexpr int kWinFine = 2 * kWinHalf;       // 6144
-// Items in increasing value order: negative values (most negative first),
-// the merged negative and positive counters, positive values.
-constexpr int kWinItems = kWinFine + 2;
-constexpr int kWinTinyNeg = kWinHalf;
-constexpr int kWinTinyPos = kWinHalf + 1;
+// Counter layout: per sign kWinSide slots, slot d of a magnitude in bits
+// being clamp(mag, kWinMagLo, kWinMagHi) - kWinMagLo: 0 for |v| < 2^-16, 1 ..
+// 3072 for the single values of [2^-16, 2^8), 3073 for |v| >= 2^8. Positive
+// values use slots d, negative ones kWinSide + d.
+constexpr int kWinSide = 3074;
+constexpr int kWinSlots = 2 * kWinSide;      // 6148
+constexpr uint32_t kWinMagLo = 0x377Fu;      // the largest bf16 magnitude below 2^-16
+constexpr uint32_t kWinMagHi = 0x4380u;      // 2^8
+// Items: the slots in increasing value order. Items 0 .. kWinSide-1 are the
+// negative side (item 0 the huge negatives, kWinSide-1 the tiny ones), then
+// the positive side (tiny first, huge last).
+constexpr int kWinItems = kWinSlots;
+constexpr int kWinHugeNeg = 0;
+constexpr int kWinTinyNeg = kWinSide - 1;
+constexpr int kWinTinyPos = kWinSide;
+constexpr int kWinHugePos = kWinSlots - 1;
 constexpr float kWinTopKWidth = 30.f;  // top-k window, in units of 1 / c
 constexpr float kWinTinyNegLow = -1.52587890625e-05f;  // -2^-16
 
+static_assert(kWinSlots == SPEC_SHARD_HIST_INTS, "the sharded histogram rows hold the slots");
+
 struct WinHist {
-  unsigned cnt[kWinItems];  // counter of fine item i at cnt[i] (the two merged
-                            // items keep theirs below)
-  unsigned tiny_cnt[2];     // merged counters: [0] negative, [1] positive
-  float tiny_w[2];          // their sums of 2^(l c)
-  unsigned out_of_range;    // set when a counted value has magnitude >= 2^8
-  unsigned pad[1];
+  unsigned cnt[kWinSlots];  // by slot
+  float tiny_w[2];          // sums of 2^(l c) of the counted tiny values: [0] negative, [1] positive
+  unsigned pad[2];
 };
 static_assert(sizeof(WinHist) % 16 == 0, "cleared with 16-byte stores");
+
+__device__ __forceinline__ int win_slot_of_item(int i) {
+  return i < kWinSide ? kWinSlots - 1 - i : i - kWinSide;
+}
 
 // Window half-width D (logit units) of a filtered row; c > 0.
 __device__ __forceinline__ float win_delta(float c, int tk, float tp, int V) {
@@ -63,27 +74,6 @@ __device__ __forceinline__ float win_delta(float c, int tk, float tp, int V) {
   if (tp < 1.f) d = (log2f((float)V / (1.f - tp)) + 1.f) / c;
   if (tk > 0 && tk < V) d = fmaxf(d, kWinTopKWidth / c);
   return d;
-}
-
-// Item (and counter) index of a bf16 value of magnitude in [2^-16, 2^8);
-// `fine` tells whether the magnitude is in that range.
-__device__ __forceinline__ int win_slot(uint32_t bits, bool& fine) {
-  const int idx = (int)(bits & 0x7FFFu) - kWinELo * 128;
-  fine = (unsigned)idx < (unsigned)kWinHalf;
-  return (bits & 0x8000u) ? (kWinHalf - 1 - idx) : (kWinHalf + 2 + idx);
-}
-
-// Count an element outside the single-value range (merged counter, or the
-// out-of-range flag for magnitudes >= 2^8 and +inf).
-__device__ __forceinline__ void win_add_rare(WinHist* h, uint32_t bits, float l, float c) {
-  const int e = (int)((bits & 0x7FFFu) >> 7);
-  const uint32_t pos = ((bits >> 15) & 1u) ^ 1u;
-  if (e < kWinELo) {
-    atomicAdd(&h->tiny_cnt[pos], 1u);
-    atomicAdd(&h->tiny_w[pos], ex2(l * c));
-  } else {
-    h->out_of_range = 1u;
-  }
 }
 
 // Shared-memory add of 1 to the counter at byte address `addr`, issued as
@@ -98,45 +88,43 @@ __device__ __forceinline__ void red_add1_if(uint32_t addr, bool on) {
 }
 
 // Count the elements of 4 words of packed bf16 pairs that lie at or above
-// the floor `flo` (-inf never does). The common case is one predicated
-// shared-memory add per element; the rare out-of-range ones are redone by
-// the warp's lanes that hold any.
+// the floor `flo` (-inf never does): per word, the two slots from packed
+// 16-bit operations, then one predicated shared-memory add per element. The
+// rare tiny magnitudes (below 2^-16) also add their weight 2^(l c) to the
+// side's sum, on a path the warp takes only when some lane holds one.
 __device__ __forceinline__ void win_count(WinHist* h, const uint32_t w[4], float flo, float c) {
-  const uint32_t base = smem_addr(h->cnt);
-  bool rare = false;
+  // byte address of slot 0, less the clamp offset folded in
+  const uint32_t base = smem_addr(h->cnt) - 4u * kWinMagLo;
+  uint32_t all_fine = 0x00010001u;  // a half drops to 0 once a tiny magnitude shows up
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    const uint32_t b0 = w[t] & 0xFFFFu, b1 = w[t] >> 16;
+    uint32_t d2, t2;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d2) : "r"(w[t] & 0x7FFF7FFFu), "r"(0x377F377Fu));
+    asm("min.u16x2 %0, %1, %2;" : "=r"(d2) : "r"(d2), "r"(0x43804380u));
+    asm("min.u16x2 %0, %1, %2;" : "=r"(t2) : "r"(d2 - 0x377F377Fu), "r"(all_fine));
+    all_fine = t2;
+    // + kWinSide per negative half (no carry: every half stays below 2^16)
+    const uint32_t s2 = d2 + ((w[t] >> 15) & 0x00010001u) * (uint32_t)kWinSide;
     const float l0 = __uint_as_float(w[t] << 16), l1 = __uint_as_float(w[t] & 0xFFFF0000u);
-    bool f0, f1;
-    const int k0 = win_slot(b0, f0), k1 = win_slot(b1, f1);
-    const bool c0 = l0 >= flo, c1 = l1 >= flo;
-    red_add1_if(base + 4u * (uint32_t)k0, c0 && f0);
-    red_add1_if(base + 4u * (uint32_t)k1, c1 && f1);
-    rare |= (c0 && !f0) || (c1 && !f1);
+    red_add1_if(base + 4u * (s2 & 0xFFFFu), l0 >= flo);
+    red_add1_if(base + 4u * (s2 >> 16), l1 >= flo);
   }
-  if (__any_sync(0xFFFFFFFFu, rare) && rare) {
+  const bool tiny = all_fine != 0x00010001u;
+  if (__any_sync(0xFFFFFFFFu, tiny) && tiny) {
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const uint32_t b0 = w[t] & 0xFFFFu, b1 = w[t] >> 16;
-      const float l0 = __uint_as_float(w[t] << 16), l1 = __uint_as_float(w[t] & 0xFFFF0000u);
-      bool f0, f1;
-      win_slot(b0, f0);
-      win_slot(b1, f1);
-      if (l0 >= flo && !f0) win_add_rare(h, b0, l0, c);
-      if (l1 >= flo && !f1) win_add_rare(h, b1, l1, c);
+    for (int t = 0; t < 8; ++t) {
+      const uint32_t b = (t & 1) ? (w[t >> 1] >> 16) : (w[t >> 1] & 0xFFFFu);
+      const float l = __uint_as_float(b << 16);
+      if ((b & 0x7FFFu) <= kWinMagLo && l >= flo)
+        atomicAdd(&h->tiny_w[(b >> 15) ? 0 : 1], ex2(l * c));
     }
   }
 }
 
-// Value of fine item i (not a merged one).
+// Value of fine item i (not a tiny or huge one).
 __device__ __forceinline__ float win_value(int i) {
-  if (i < kWinHalf) {
-    const uint32_t a = (uint32_t)(kWinHalf - 1 - i) + kWinELo * 128u;
-    return __uint_as_float((0x8000u | a) << 16);
-  }
-  const uint32_t a = (uint32_t)(i - kWinHalf - 2) + kWinELo * 128u;
-  return __uint_as_float(a << 16);
+  if (i < kWinSide) return __uint_as_float((0x8000u | (kWinMagLo + (uint32_t)(kWinSide - 1 - i))) << 16);
+  return __uint_as_float((kWinMagLo + (uint32_t)(i - kWinSide)) << 16);
 }
 
 // Sum of v over consumer threads with a larger index (exclusive suffix sum).
@@ -181,70 +169,57 @@ struct HistResult {
 // Add this CTA's window histogram into a global one and clear it (the
 // threads 0 .. nt-1 of the caller's group, tid among them).
 __device__ __forceinline__ void win_flush(WinHist* h, WinHist* g, int tid, int nt) {
-  for (int i = tid; i < kWinItems; i += nt) {
+  for (int i = tid; i < kWinSlots; i += nt) {
     const unsigned v = h->cnt[i];
     if (v) {
       atomicAdd(&g->cnt[i], v);
       h->cnt[i] = 0u;
     }
   }
-  if (tid == 0) {
-    for (int k = 0; k < 2; ++k) {
-      if (h->tiny_cnt[k]) {
-        atomicAdd(&g->tiny_cnt[k], h->tiny_cnt[k]);
-        atomicAdd(&g->tiny_w[k], h->tiny_w[k]);
-      }
-      h->tiny_cnt[k] = 0u;
-      h->tiny_w[k] = 0.f;
-    }
-    if (h->out_of_range) atomicOr(&g->out_of_range, 1u);
-    h->out_of_range = 0u;
+  if (tid < 2) {
+    if (h->tiny_w[tid] != 0.f) atomicAdd(&g->tiny_w[tid], h->tiny_w[tid]);
+    h->tiny_w[tid] = 0.f;
   }
 }
 
 // Move a global window histogram into this CTA's (which is clear) and clear
 // the global one.
 __device__ __forceinline__ void win_take(WinHist* h, WinHist* g, int tid, int nt) {
-  for (int i = tid; i < kWinItems; i += nt) {
+  for (int i = tid; i < kWinSlots; i += nt) {
     const unsigned v = __ldcg(&g->cnt[i]);
     if (v) {
       h->cnt[i] = v;
       g->cnt[i] = 0u;
     }
   }
-  if (tid == 0) {
-    for (int k = 0; k < 2; ++k) {
-      h->tiny_cnt[k] = __ldcg(&g->tiny_cnt[k]);
-      h->tiny_w[k] = __ldcg(&g->tiny_w[k]);
-      g->tiny_cnt[k] = 0u;
-      g->tiny_w[k] = 0.f;
-    }
-    h->out_of_range = __ldcg(&g->out_of_range);
-    g->out_of_range = 0u;
+  if (tid < 2) {
+    h->tiny_w[tid] = __ldcg(&g->tiny_w[tid]);
+    g->tiny_w[tid] = 0.f;
   }
 }
 
 // Row-end processing of the window histogram by the kWarps consumer warps
 // (all call it): m the row max, c = log2(e) / T, zfull the sum of
 // 2^(l c - m c) over the whole row, lo = m - D the window floor. Thread t
-// owns a run of consecutive items (kWinFine / threads fine ones; the merged
-// two go to the threads on either side of the sign change), and higher
-// threads hold larger values. Each thread reads its items' counts once,
-// clears them, and works from registers; items not wholly inside the window
-// (values below lo, not all counted) read as empty, so a threshold never
-// lands on them. Clears the histogram.
+// owns a run of consecutive items (each side's kWinSide items over half the
+// threads, the two ends of each side one extra), and higher threads hold
+// larger values. Each thread reads its items' counts once, clears them, and
+// works from registers; items not wholly inside the window (values below
+// lo, not all counted) read as empty, so a threshold never lands on them. A
+// counted huge value leaves the row to the slow path. Clears the histogram.
 template <int kWarps>
 __device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, float lo, int tk,
                                  float tp, int V, int tid, float* fscr, int* iscr) {
   constexpr int kThreads = kWarps * 32;
-  constexpr int kPer = kWinFine / kThreads;
   constexpr int kHalfT = kThreads / 2;
-  constexpr int kMax = kPer + 1;  // items of the two threads at the sign change
-  static_assert(kPer * kThreads == kWinFine, "fine items split evenly over the threads");
-  static_assert(kPer * kHalfT == kWinHalf, "the sign change falls between two threads");
+  constexpr int kPer = (kWinSide - 2) / kHalfT;
+  constexpr int kMax = kPer + 1;  // items of a side's first and last thread
+  static_assert(kPer * kHalfT + 2 == kWinSide, "each side splits evenly over half the threads");
   __shared__ int s_item;
-  const int i0 = tid < kHalfT ? tid * kPer : tid * kPer + 2 - (tid == kHalfT ? 1 : 0);
-  const int ni = (tid == kHalfT - 1 || tid == kHalfT) ? kMax : kPer;
+  const int side = tid < kHalfT ? 0 : 1;
+  const int u = tid - side * kHalfT;
+  const int i0 = side * kWinSide + u * kPer + (u > 0 ? 1 : 0);
+  const int ni = (u == 0 || u == kHalfT - 1) ? kMax : kPer;
   const float mc = m * c;
   const bool topk_on = (tk > 0 && tk < V);
   const bool topp_on = (tp < 1.f);
@@ -254,25 +229,29 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, floa
   unsigned cn[kMax];
   float ms[kMax];
   unsigned my_cnt = 0;
+  bool huge = false;
 #pragma unroll
   for (int k = 0; k < kMax; ++k) {
     const int i = i0 + k;
     cn[k] = 0u;
     ms[k] = 0.f;
     if (k < ni) {
-      unsigned n;
+      const int sl = win_slot_of_item(i);
+      const unsigned n = h->cnt[sl];
+      h->cnt[sl] = 0u;
       float w;
       bool whole;
-      if (i == kWinTinyNeg || i == kWinTinyPos) {
-        const int s = i - kWinTinyNeg;
-        n = h->tiny_cnt[s];
-        w = h->tiny_w[s] * emc;
-        h->tiny_cnt[s] = 0u;
-        h->tiny_w[s] = 0.f;
-        whole = (s == 0) ? (lo <= kWinTinyNegLow) : (lo <= 0.f);
+      if (i == kWinHugeNeg || i == kWinHugePos) {
+        huge |= (n != 0u);
+        w = 0.f;
+        whole = false;
+      } else if (i == kWinTinyNeg || i == kWinTinyPos) {
+        // magnitudes below 2^-16: the sum of their weights
+        const int sd = (i == kWinTinyNeg) ? 0 : 1;
+        w = h->tiny_w[sd] * emc;  // each side's sum has one reader, its owner
+        h->tiny_w[sd] = 0.f;
+        whole = (i == kWinTinyNeg) ? (lo <= kWinTinyNegLow) : (lo <= 0.f);
       } else {
-        n = h->cnt[i];
-        h->cnt[i] = 0u;
         const float v = win_value(i);
         w = n ? (float)n * ex2(fmaf(v, c, -mc)) : 0.f;
         whole = v >= lo;
@@ -355,12 +334,11 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, floa
     if (!pending && !(topk_on && ip == ik) && !(z >= thr)) pending = 1;
   }
 
-  const unsigned oor = h->out_of_range;
-  named_sync(1, kThreads);
-  if (tid == 0) h->out_of_range = 0u;
+  const int any_huge = consumer_reduce<int, kWarps>(huge ? 1 : 0, iscr, tid,
+                                                    [](int a, int b) { return a | b; });
 
   HistResult res;
-  res.pending = (pending || oor != 0u) ? 1 : 0;
+  res.pending = (pending || any_huge) ? 1 : 0;
   res.theta = (!res.pending && ikeep >= 0) ? win_value(ikeep) : -INFINITY;
   res.z = z;
   return res;

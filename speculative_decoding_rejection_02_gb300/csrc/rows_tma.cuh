@@ -552,23 +552,13 @@ k_rows_tma(Params P, long long R) {
         if (lane == 0) red_s[warp] = part;
         if (FILT && M.cls == kFiltered) {
           int* hout = P.sh_hist + M.row * (long long)SPEC_SHARD_HIST_INTS;
-          for (int i = tid; i < kWinItems; i += kTmaConsumers) {
-            if (i != kWinTinyNeg && i != kWinTinyPos) {
-              hout[i] = (int)hist->cnt[i];
-              hist->cnt[i] = 0u;
-            }
+          for (int i = tid; i < kWinSlots; i += kTmaConsumers) {
+            hout[i] = (int)hist->cnt[i];
+            hist->cnt[i] = 0u;
           }
-          named_sync(1, kTmaConsumers);
-          if (tid == 0) {
-            hout[kWinTinyNeg] = (int)hist->tiny_cnt[0];
-            hout[kWinTinyPos] = (int)hist->tiny_cnt[1];
-            hout[kWinItems] = (int)hist->out_of_range;
-            hout[kWinItems + 1] = 0;
-            P.sh_hist_w[2 * M.row] = hist->tiny_w[0];
-            P.sh_hist_w[2 * M.row + 1] = hist->tiny_w[1];
-            hist->tiny_cnt[0] = hist->tiny_cnt[1] = 0u;
-            hist->tiny_w[0] = hist->tiny_w[1] = 0.f;
-            hist->out_of_range = 0u;
+          if (tid < 2) {
+            P.sh_hist_w[2 * M.row + tid] = hist->tiny_w[tid];
+            hist->tiny_w[tid] = 0.f;
           }
         }
         named_sync(1, kTmaConsumers);

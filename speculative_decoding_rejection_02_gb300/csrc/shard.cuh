@@ -86,15 +86,8 @@ k_shard_finish(Params P) {
   }
   WinHist* h = reinterpret_cast<WinHist*>(shard_smem);
   const int* hin = P.sh_hist + row * (long long)SPEC_SHARD_HIST_INTS;
-  for (int i = tid; i < kWinItems; i += kShardFinishThreads)
-    h->cnt[i] = (i == kWinTinyNeg || i == kWinTinyPos) ? 0u : (unsigned)hin[i];
-  if (tid == 0) {
-    h->tiny_cnt[0] = (unsigned)hin[kWinTinyNeg];
-    h->tiny_cnt[1] = (unsigned)hin[kWinTinyPos];
-    h->tiny_w[0] = P.sh_hist_w[2 * row];
-    h->tiny_w[1] = P.sh_hist_w[2 * row + 1];
-    h->out_of_range = hin[kWinItems] != 0 ? 1u : 0u;
-  }
+  for (int i = tid; i < kWinSlots; i += kShardFinishThreads) h->cnt[i] = (unsigned)hin[i];
+  if (tid < 2) h->tiny_w[tid] = P.sh_hist_w[2 * row + tid];
   __syncthreads();
   const int tk = P.top_k ? __ldg(P.top_k + r) : 0;
   const float tp = P.top_p ? __ldg(P.top_p + r) : 1.f;
