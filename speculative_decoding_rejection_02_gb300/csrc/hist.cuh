@@ -76,14 +76,14 @@ __device__ __forceinline__ float win_delta(float c, int tk, float tp, int V) {
   return d;
 }
 
-// Shared-memory add of 1 to the counter at byte address `addr`, issued as
-// one predicated instruction (no branch around it).
-__device__ __forceinline__ void red_add1_if(uint32_t addr, bool on) {
+// Shared-memory add of 1 to the counter at byte address `addr` when
+// l >= flo: one compare and one predicated add.
+__device__ __forceinline__ void red_add1_if_ge(uint32_t addr, float l, float flo) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
+      "setp.ge.f32 p, %1, %2;\n\t"
       "@p red.shared.add.u32 [%0], 1;\n\t}" ::"r"(addr),
-      "r"((uint32_t)on)
+      "f"(l), "f"(flo)
       : "memory");
 }
 
@@ -106,8 +106,8 @@ __device__ __forceinline__ void win_count(WinHist* h, const uint32_t w[4], float
     // + kWinSide per negative half (no carry: every half stays below 2^16)
     const uint32_t s2 = d2 + ((w[t] >> 15) & 0x00010001u) * (uint32_t)kWinSide;
     const float l0 = __uint_as_float(w[t] << 16), l1 = __uint_as_float(w[t] & 0xFFFF0000u);
-    red_add1_if(base + 4u * (s2 & 0xFFFFu), l0 >= flo);
-    red_add1_if(base + 4u * (s2 >> 16), l1 >= flo);
+    red_add1_if_ge(base + 4u * (s2 & 0xFFFFu), l0, flo);
+    red_add1_if_ge(base + 4u * (s2 >> 16), l1, flo);
   }
   const bool tiny = all_fine != 0x00010001u;
   if (__any_sync(0xFFFFFFFFu, tiny) && tiny) {
