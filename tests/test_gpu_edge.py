@@ -214,6 +214,39 @@ def test_window_histogram_cases(case):
     assert gpu["status"] & ~np.uint32(0x8) == 0
 
 
+@pytest.mark.parametrize("case", ["tiny_kept", "tiny_boundary"])
+def test_window_histogram_tiny_magnitudes(case):
+    """Rows whose counted values include many magnitudes below 2^-16 (and
+    exact zeros of both signs), at temperatures where their weights differ
+    visibly from one another: their exact weight sums must reach Z and the
+    kept mass whether the top-p boundary lies above them ("tiny_kept") or
+    among them ("tiny_boundary", left to the exact slow kernel)."""
+    rng = np.random.default_rng(["tiny_kept", "tiny_boundary"].index(case) + 301)
+    V, B = 4096, 24
+    g = rng.integers(0, 4, size=B)
+    N = int(g.sum())
+    logits = rng.normal(0, 6e-6, size=(N + B, V))
+    logits[rng.random((N + B, V)) < 0.1] = 0.0
+    logits[rng.random((N + B, V)) < 0.05] = -0.0
+    if case == "tiny_kept":
+        # a few heavier tokens put the boundary above the tiny values, or
+        # keep all of them when top_p is high
+        hot = rng.integers(0, V, size=(N + B, 30))
+        for r in range(N + B):
+            logits[r, hot[r]] = rng.uniform(0.0005, 0.004, size=30)
+        temps = rng.choice([0.0005, 0.001], size=B)
+        tp = rng.choice([0.3, 0.9, 0.9999], size=B)
+    else:
+        temps = rng.choice([0.00002, 0.0001], size=B)
+        tp = rng.choice([0.5, 0.9], size=B)
+    q = rng.random((N, V)) ** 2
+    q /= q.sum(1, keepdims=True)
+    ids = np.array([rng.choice(V, p=q[n]) for n in range(N)], np.int32)
+    b = make_batch(logits, g, ids, temps, q, None, tp, dtype="bf16", seed=29)
+    gpu, _ = check(b)
+    assert gpu["status"] & ~np.uint32(0x8) == 0
+
+
 def test_bounded_wait_times_out_and_the_context_survives():
     """A wait that cannot be satisfied ends with SPEC_STATUS_TIMEOUT instead
     of hanging: a test-only handle flag leaves the early-exit work queue
