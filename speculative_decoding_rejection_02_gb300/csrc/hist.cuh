@@ -216,6 +216,7 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, floa
   constexpr int kMax = kPer + 1;  // items of a side's first and last thread
   static_assert(kPer * kHalfT + 2 == kWinSide, "each side splits evenly over half the threads");
   __shared__ int s_item;
+  __shared__ int s_huge[2];  // written every row by the huge items' owners
   const int side = tid < kHalfT ? 0 : 1;
   const int u = tid - side * kHalfT;
   const int i0 = side * kWinSide + u * kPer + (u > 0 ? 1 : 0);
@@ -263,6 +264,10 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, floa
       }
     }
   }
+  // Only the first and the last thread own a huge item; the barriers below
+  // publish their flags.
+  if (tid == 0) s_huge[0] = huge ? 1 : 0;
+  if (tid == kThreads - 1) s_huge[1] = huge ? 1 : 0;
   auto merged = [](int i) { return i == kWinTinyNeg || i == kWinTinyPos; };
   int pending = (zfull == zfull && m < INFINITY) ? 0 : 1;  // NaN or +inf in the row
 
@@ -334,8 +339,8 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, floa
     if (!pending && !(topk_on && ip == ik) && !(z >= thr)) pending = 1;
   }
 
-  const int any_huge = consumer_reduce<int, kWarps>(huge ? 1 : 0, iscr, tid,
-                                                    [](int a, int b) { return a | b; });
+  if (!topk_on && !topp_on) named_sync(1, kThreads);  // (filtered rows have one of them)
+  const int any_huge = s_huge[0] | s_huge[1];
 
   HistResult res;
   res.pending = (pending || any_huge) ? 1 : 0;
