@@ -95,21 +95,22 @@ __device__ __forceinline__ void red_add1_if_ge(uint32_t addr, float l, float flo
 __device__ __forceinline__ void win_count(WinHist* h, const uint32_t w[4], float flo, float c) {
   // byte address of slot 0, less the clamp offset folded in
   const uint32_t base = smem_addr(h->cnt) - 4u * kWinMagLo;
-  uint32_t all_fine = 0x00010001u;  // a half drops to 0 once a tiny magnitude shows up
+  uint32_t fine = 0x80008000u;  // a half's top bit drops once a tiny magnitude shows up
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    uint32_t d2, t2;
-    asm("max.u16x2 %0, %1, %2;" : "=r"(d2) : "r"(w[t] & 0x7FFF7FFFu), "r"(0x377F377Fu));
+    const uint32_t mag2 = w[t] & 0x7FFF7FFFu;
+    uint32_t d2;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d2) : "r"(mag2), "r"(0x377F377Fu));
     asm("min.u16x2 %0, %1, %2;" : "=r"(d2) : "r"(d2), "r"(0x43804380u));
-    asm("min.u16x2 %0, %1, %2;" : "=r"(t2) : "r"(d2 - 0x377F377Fu), "r"(all_fine));
-    all_fine = t2;
+    fine &= (w[t] | 0x80008000u) - 0x37803780u;  // (mag | 2^15) - 2^-16's bits, no borrow
     // + kWinSide per negative half (no carry: every half stays below 2^16)
     const uint32_t s2 = d2 + ((w[t] >> 15) & 0x00010001u) * (uint32_t)kWinSide;
     const float l0 = __uint_as_float(w[t] << 16), l1 = __uint_as_float(w[t] & 0xFFFF0000u);
     red_add1_if_ge(base + 4u * (s2 & 0xFFFFu), l0, flo);
     red_add1_if_ge(base + 4u * (s2 >> 16), l1, flo);
   }
-  const bool tiny = all_fine != 0x00010001u;
+  // Tiny magnitudes also add their weights (huge ones need nothing here).
+  const bool tiny = (fine & 0x80008000u) != 0x80008000u;
   if (__any_sync(0xFFFFFFFFu, tiny) && tiny) {
 #pragma unroll
     for (int t = 0; t < 8; ++t) {

@@ -393,7 +393,8 @@ k_rows_tma(Params P, long long R) {
   // Running state of the current row: max, its lowest index, fl(max * c),
   // and the sum of 2^(l c - fl(max c)) over this thread's elements.
   float vmax = -INFINITY, vmc = 0.f, s = 0.f;
-  int imax = kNoIndex;
+  int imax = kNoIndex;  // first element of the vector holding vmax (kNoIndex: none)
+  uint4 mvec = make_uint4(0u, 0u, 0u, 0u);  // that vector
   for (;;) {
     int landed = 1;
     if (lane == 0) landed = mbar_wait(&full[stage], phase) ? 1 : 0;
@@ -417,39 +418,50 @@ k_rows_tma(Params P, long long R) {
       v[k] = idx < nvec ? buf[idx] : make_uint4(pad, pad, pad, pad);
     }
     float m32;
+    // per-vector maxima (bf16: packed pairs), then the stage max
+    uint32_t vm[kTmaVecPerThread];
     if (BF16) {
-      __nv_bfloat162 h = u32_as_bf162(v[0].x);
 #pragma unroll
       for (int k = 0; k < kTmaVecPerThread; ++k) {
-        h = __hmax2(h, u32_as_bf162(v[k].x));
-        h = __hmax2(h, u32_as_bf162(v[k].y));
-        h = __hmax2(h, u32_as_bf162(v[k].z));
-        h = __hmax2(h, u32_as_bf162(v[k].w));
+        const __nv_bfloat162 h = __hmax2(__hmax2(u32_as_bf162(v[k].x), u32_as_bf162(v[k].y)),
+                                         __hmax2(u32_as_bf162(v[k].z), u32_as_bf162(v[k].w)));
+        memcpy(&vm[k], &h, sizeof h);
       }
+      __nv_bfloat162 h = u32_as_bf162(vm[0]);
+#pragma unroll
+      for (int k = 1; k < kTmaVecPerThread; ++k) h = __hmax2(h, u32_as_bf162(vm[k]));
       m32 = fmaxf(__low2float(h), __high2float(h));
     } else {
-      m32 = __uint_as_float(v[0].x);
 #pragma unroll
       for (int k = 0; k < kTmaVecPerThread; ++k)
-        m32 = fmaxf(fmaxf(m32, fmaxf(__uint_as_float(v[k].x), __uint_as_float(v[k].y))),
-                    fmaxf(__uint_as_float(v[k].z), __uint_as_float(v[k].w)));
+        vm[k] = __float_as_uint(
+            fmaxf(fmaxf(__uint_as_float(v[k].x), __uint_as_float(v[k].y)),
+                  fmaxf(__uint_as_float(v[k].z), __uint_as_float(v[k].w))));
+      m32 = __uint_as_float(vm[0]);
+#pragma unroll
+      for (int k = 1; k < kTmaVecPerThread; ++k) m32 = fmaxf(m32, __uint_as_float(vm[k]));
     }
     if (m32 > vmax || (imax == kNoIndex && m32 > -INFINITY)) {
-      // New running max (rare after the first stages): rescale, locate it.
+      // New running max: rescale, and remember the vector that holds it.
       const float nmc = m32 * M.c;
       if (soft && vmax > -INFINITY) s *= ex2(vmc - nmc);
-      int at = kNoIndex;
+      // The lowest index holding it: the first vector whose max it is, then
+      // the first element of that vector.
+      int kk = kTmaVecPerThread - 1;
 #pragma unroll
-      for (int k = kTmaVecPerThread - 1; k >= 0; --k) {
-        float f[8];
-        unpack_chunk(v[k], BF16, f);
-#pragma unroll
-        for (int e = epc - 1; e >= 0; --e)
-          if (f[e] == m32) at = M.j0 + (tid + k * kTmaConsumers) * epc + e;
+      for (int k = kTmaVecPerThread - 2; k >= 0; --k) {
+        const float mk = BF16 ? fmaxf(bf16_lo(vm[k]), bf16_hi(vm[k])) : __uint_as_float(vm[k]);
+        if (mk == m32) kk = k;
       }
+      uint4 vk = v[kTmaVecPerThread - 1];
+#pragma unroll
+      for (int k = kTmaVecPerThread - 2; k >= 0; --k)
+        if (k == kk) vk = v[k];
+      // Keep that vector; its element is found once, at the row's end.
       vmax = m32;
       vmc = nmc;
-      imax = at;
+      imax = M.j0 + (tid + kk * kTmaConsumers) * epc;
+      mvec = vk;
     }
     if (soft && vmax > -INFINITY) {
       const unsigned long long c2 = f2_pack(M.c, M.c);
@@ -524,7 +536,14 @@ k_rows_tma(Params P, long long R) {
     }
     if (M.last) {
       float m = vmax;
-      int a = imax;
+      int a = kNoIndex;
+      if (imax != kNoIndex) {
+        float f[8];
+        unpack_chunk(mvec, BF16, f);
+#pragma unroll
+        for (int e = epc - 1; e >= 0; --e)
+          if (f[e] == vmax) a = imax + e;
+      }
       warp_argmax(m, a);
       if (lane == 0) {
         red_m[warp] = m;
