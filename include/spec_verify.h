@@ -323,7 +323,8 @@ typedef struct {
   int* hist;           /* [(N+B) x SPEC_SHARD_HIST_INTS] window histogram counts of
                           top-k / top-p rows (NULL when the batch has no top_k and
                           no top_p) */
-  float* hist_w;       /* [(N+B) x 2] weights of its two merged counters (NULL as hist) */
+  float* hist_w;       /* [(N+B) x 2] sums of 2^(l c) of the counted values below 2^-16
+                          in magnitude, negative then positive (NULL as hist) */
   unsigned long long* best;    /* [B] race winner of the local columns, (score bits
                                   << 32) | (0xFFFFFFFF - global index); 0: none */
   unsigned long long* best_p;  /* [B] the race on p for requests whose combined best
