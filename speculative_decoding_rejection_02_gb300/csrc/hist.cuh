@@ -76,23 +76,37 @@ __device__ __forceinline__ float win_delta(float c, int tk, float tp, int V) {
   return d;
 }
 
-// Shared-memory add of 1 to the counter at byte address `addr` when
-// l >= flo: one compare and one predicated add.
-__device__ __forceinline__ void red_add1_if_ge(uint32_t addr, float l, float flo) {
+// The window floor as a pair of bf16 values: the largest bf16 at or below
+// f (a lower floor only counts more), never -inf (so -inf logits and the
+// padding are never counted), in both halves.
+__device__ __forceinline__ uint32_t win_floor2(float f) {
+  const uint32_t b = __float_as_uint(f);
+  uint32_t t = b >> 16;                              // toward zero
+  if ((b & 0x80000000u) && (b & 0xFFFFu)) t += 1u;   // negative: one step further down
+  if (t == 0xFF80u) t = 0xFF7Fu;                     // -inf: the lowest finite bf16
+  return t | (t << 16);
+}
+
+// Shared-memory adds of 1 to the counters at byte addresses a0 and a1 for
+// the low and high bf16 of w that are at or above the packed floor f2: one
+// packed compare, two predicated adds.
+__device__ __forceinline__ void red_add2_if_ge(uint32_t a0, uint32_t a1, uint32_t w, uint32_t f2) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ge.f32 p, %1, %2;\n\t"
-      "@p red.shared.add.u32 [%0], 1;\n\t}" ::"r"(addr),
-      "f"(l), "f"(flo)
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ge.bf16x2 p|q, %2, %3;\n\t"
+      "@p red.shared.add.u32 [%0], 1;\n\t"
+      "@q red.shared.add.u32 [%1], 1;\n\t}" ::"r"(a0),
+      "r"(a1), "r"(w), "r"(f2)
       : "memory");
 }
 
 // Count the elements of 4 words of packed bf16 pairs that lie at or above
-// the floor `flo` (-inf never does): per word, the two slots from packed
-// 16-bit operations, then one predicated shared-memory add per element. The
-// rare tiny magnitudes (below 2^-16) also add their weight 2^(l c) to the
-// side's sum, on a path the warp takes only when some lane holds one.
-__device__ __forceinline__ void win_count(WinHist* h, const uint32_t w[4], float flo, float c) {
+// the packed floor f2 (win_floor2): per word, the two slots from packed
+// 16-bit operations, one packed compare and one predicated shared-memory add
+// per element. The rare tiny magnitudes (below 2^-16) also add their weight
+// 2^(l c) to the side's sum, on a path the warp takes only when some lane
+// holds one.
+__device__ __forceinline__ void win_count(WinHist* h, const uint32_t w[4], uint32_t f2, float c) {
   // byte address of slot 0, less the clamp offset folded in
   const uint32_t base = smem_addr(h->cnt) - 4u * kWinMagLo;
   uint32_t fine = 0x80008000u;  // a half's top bit drops once a tiny magnitude shows up
@@ -105,13 +119,13 @@ __device__ __forceinline__ void win_count(WinHist* h, const uint32_t w[4], float
     fine &= (w[t] | 0x80008000u) - 0x37803780u;  // (mag | 2^15) - 2^-16's bits, no borrow
     // + kWinSide per negative half (no carry: every half stays below 2^16)
     const uint32_t s2 = d2 + ((w[t] >> 15) & 0x00010001u) * (uint32_t)kWinSide;
-    const float l0 = __uint_as_float(w[t] << 16), l1 = __uint_as_float(w[t] & 0xFFFF0000u);
-    red_add1_if_ge(base + 4u * (s2 & 0xFFFFu), l0, flo);
-    red_add1_if_ge(base + 4u * (s2 >> 16), l1, flo);
+    red_add2_if_ge(base + 4u * (s2 & 0xFFFFu), base + 4u * (s2 >> 16), w[t], f2);
   }
-  // Tiny magnitudes also add their weights (huge ones need nothing here).
+  // Tiny magnitudes also add their weights (huge ones need nothing here),
+  // under the same floor as their counts.
   const bool tiny = (fine & 0x80008000u) != 0x80008000u;
   if (__any_sync(0xFFFFFFFFu, tiny) && tiny) {
+    const float flo = __uint_as_float(f2 << 16);
 #pragma unroll
     for (int t = 0; t < 8; ++t) {
       const uint32_t b = (t & 1) ? (w[t >> 1] >> 16) : (w[t >> 1] & 0xFFFFu);

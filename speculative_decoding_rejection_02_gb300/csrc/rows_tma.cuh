@@ -499,11 +499,11 @@ k_rows_tma(Params P, long long R) {
     if (FILT && M.cls == kFiltered) {
       // Count the elements at or above this thread's window floor (its
       // running max minus D; -inf and the padding never count).
-      const float flo = fmaxf(vmax - M.delta, -3.402823466e38f);
+      const uint32_t flo2 = win_floor2(fmaxf(vmax - M.delta, -3.402823466e38f));
 #pragma unroll
       for (int k = 0; k < kTmaVecPerThread; ++k) {
         const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-        win_count(hist, w, flo, M.c);
+        win_count(hist, w, flo2, M.c);
       }
     }
     {
