@@ -103,31 +103,37 @@ __device__ __forceinline__ void red_add2_if_ge(uint32_t a0, uint32_t a1, uint32_
 // Count the elements of 4 words of packed bf16 pairs that lie at or above
 // the packed floor f2 (win_floor2): per word, the two slots from packed
 // 16-bit operations, one packed compare and one predicated shared-memory add
-// per element. The rare tiny magnitudes (below 2^-16) also add their weight
-// 2^(l c) to the side's sum, on a path the warp takes only when some lane
-// holds one.
-__device__ __forceinline__ void win_count(WinHist* h, const uint32_t w[4], uint32_t f2, float c) {
+// per element. mn2 keeps the smallest magnitudes seen (per half), for
+// win_tiny.
+__device__ __forceinline__ void win_count(WinHist* h, const uint32_t w[4], uint32_t f2,
+                                          uint32_t& mn2) {
   // byte address of slot 0, less the clamp offset folded in
   const uint32_t base = smem_addr(h->cnt) - 4u * kWinMagLo;
-  uint32_t fine = 0x80008000u;  // a half's top bit drops once a tiny magnitude shows up
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     const uint32_t mag2 = w[t] & 0x7FFF7FFFu;
     uint32_t d2;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(mn2) : "r"(mn2), "r"(mag2));
     asm("max.u16x2 %0, %1, %2;" : "=r"(d2) : "r"(mag2), "r"(0x377F377Fu));
     asm("min.u16x2 %0, %1, %2;" : "=r"(d2) : "r"(d2), "r"(0x43804380u));
-    fine &= (w[t] | 0x80008000u) - 0x37803780u;  // (mag | 2^15) - 2^-16's bits, no borrow
     // + kWinSide per negative half (no carry: every half stays below 2^16)
     const uint32_t s2 = d2 + ((w[t] >> 15) & 0x00010001u) * (uint32_t)kWinSide;
     red_add2_if_ge(base + 4u * (s2 & 0xFFFFu), base + 4u * (s2 >> 16), w[t], f2);
   }
-  // Tiny magnitudes also add their weights (huge ones need nothing here),
-  // under the same floor as their counts.
-  const bool tiny = (fine & 0x80008000u) != 0x80008000u;
+}
+
+// After win_count over a thread's words of a stage (smallest magnitudes
+// mn2): the rare tiny magnitudes (below 2^-16) that were counted also add
+// their weight 2^(l c) to their side's sum, on a path the warp takes only
+// when some lane holds one. Huge ones need nothing here.
+template <int kWords>
+__device__ __forceinline__ void win_tiny(WinHist* h, const uint32_t (&w)[kWords], uint32_t f2,
+                                         uint32_t mn2, float c) {
+  const bool tiny = min(mn2 & 0xFFFFu, mn2 >> 16) <= kWinMagLo;
   if (__any_sync(0xFFFFFFFFu, tiny) && tiny) {
-    const float flo = __uint_as_float(f2 << 16);
+    const float flo = __uint_as_float(f2 << 16);  // the floor the counts used
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
+    for (int t = 0; t < 2 * kWords; ++t) {
       const uint32_t b = (t & 1) ? (w[t >> 1] >> 16) : (w[t >> 1] & 0xFFFFu);
       const float l = __uint_as_float(b << 16);
       if ((b & 0x7FFFu) <= kWinMagLo && l >= flo)

@@ -500,11 +500,18 @@ k_rows_tma(Params P, long long R) {
       // Count the elements at or above this thread's window floor (its
       // running max minus D; -inf and the padding never count).
       const uint32_t flo2 = win_floor2(fmaxf(vmax - M.delta, -3.402823466e38f));
+      uint32_t words[4 * kTmaVecPerThread];
+      uint32_t mn2 = 0xFFFFFFFFu;
 #pragma unroll
       for (int k = 0; k < kTmaVecPerThread; ++k) {
         const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-        win_count(hist, w, flo2, M.c);
+        words[4 * k] = v[k].x;
+        words[4 * k + 1] = v[k].y;
+        words[4 * k + 2] = v[k].z;
+        words[4 * k + 3] = v[k].w;
+        win_count(hist, w, flo2, mn2);
       }
+      win_tiny(hist, words, flo2, mn2, M.c);
     }
     {
       // The draft token's logit, captured by the thread that holds it.
