@@ -56,6 +56,7 @@ constexpr float kWinTopKWidth = 30.f;  // top-k window, in units of 1 / c
 constexpr float kWinTinyNegLow = -1.52587890625e-05f;  // -2^-16
 
 static_assert(kWinSlots == SPEC_SHARD_HIST_INTS, "the sharded histogram rows hold the slots");
+static_assert(kWinSlots % 4 == 0, "the counters are cleared with 16-byte stores");
 
 struct WinHist {
   unsigned cnt[kWinSlots];  // by slot
@@ -227,7 +228,8 @@ __device__ __forceinline__ void win_take(WinHist* h, WinHist* g, int tid, int nt
 // larger values. Each thread reads its items' counts once, clears them, and
 // works from registers; items not wholly inside the window (values below
 // lo, not all counted) read as empty, so a threshold never lands on them. A
-// counted huge value leaves the row to the slow path. Clears the histogram.
+// counted huge value leaves the row to the slow path. Clears the histogram
+// (the caller's next barrier orders the clearing before later counts).
 template <int kWarps>
 __device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, float lo, int tk,
                                  float tp, int V, int tid, float* fscr, int* iscr) {
@@ -258,9 +260,7 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, floa
     cn[k] = 0u;
     ms[k] = 0.f;
     if (k < ni) {
-      const int sl = win_slot_of_item(i);
-      const unsigned n = h->cnt[sl];
-      h->cnt[sl] = 0u;
+      const unsigned n = h->cnt[win_slot_of_item(i)];
       float w;
       bool whole;
       if (i == kWinHugeNeg || i == kWinHugePos) {
@@ -362,6 +362,12 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, floa
 
   if (!topk_on && !topp_on) named_sync(1, kThreads);  // (filtered rows have one of them)
   const int any_huge = s_huge[0] | s_huge[1];
+  // Every count was read before the barriers above: clear the counters with
+  // 16-byte stores (the tiny weights were cleared by their readers).
+  {
+    uint4* hz = reinterpret_cast<uint4*>(h->cnt);
+    for (int i = tid; i < kWinSlots / 4; i += kThreads) hz[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
 
   HistResult res;
   res.pending = (pending || any_huge) ? 1 : 0;

@@ -412,10 +412,16 @@ k_rows_tma(Params P, long long R) {
     // missing ones read as -inf (no max, no mass).
     constexpr uint32_t pad = BF16 ? 0xFF80FF80u : 0xFF800000u;
     uint4 v[kTmaVecPerThread];
+    if (nvec == kTmaVecPerThread * kTmaConsumers) {
+      // a full stage (every stage but a row's or part's last)
 #pragma unroll
-    for (int k = 0; k < kTmaVecPerThread; ++k) {
-      const int idx = tid + k * kTmaConsumers;
-      v[k] = idx < nvec ? buf[idx] : make_uint4(pad, pad, pad, pad);
+      for (int k = 0; k < kTmaVecPerThread; ++k) v[k] = buf[tid + k * kTmaConsumers];
+    } else {
+#pragma unroll
+      for (int k = 0; k < kTmaVecPerThread; ++k) {
+        const int idx = tid + k * kTmaConsumers;
+        v[k] = idx < nvec ? buf[idx] : make_uint4(pad, pad, pad, pad);
+      }
     }
     float m32;
     // per-vector maxima (bf16: packed pairs), then the stage max
