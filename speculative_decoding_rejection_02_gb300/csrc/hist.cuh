@@ -12,14 +12,15 @@
 // is 30 / c wide (weights down to 2^-30 of the maximum's).
 //
 // While the row streams, each thread drops an element unless it lies at or
-// above (its own running max) - D; every running max is at most m, so every
-// element at or above m - D is counted. A counted element adds 1 to the
-// counter of its value: per sign, one 32-bit counter per bf16 magnitude in
-// [2^-16, 2^8) (3072 values), one for all smaller magnitudes (taken at value
-// 0) and one for 2^8 and above (+inf included), which sends the row to the
-// exact slow path. The counter of a bf16 word's two values comes from a few
-// packed 16-bit operations (magnitude clamp, sign offset), one predicated
-// shared-memory add each.
+// above its floor, (its own running max) - D rounded down to bf16; every
+// running max is at most m, so every element at or above m - D is counted. A
+// counted element adds 1 to the counter of its value: per sign, one 32-bit
+// counter per bf16 magnitude in [2^-16, 2^8) (3072 values), one for all
+// smaller magnitudes (whose exact weights 2^(l c) are summed beside it) and
+// one for 2^8 and above (+inf included), which sends the row to the exact
+// slow path. The counters of a bf16 word's two values come from a few packed
+// 16-bit operations (magnitude clamp, sign offset), one packed compare with
+// the floor and one predicated shared-memory add each.
 //
 // At the row's end the consumers turn counts into masses n 2^(v c - m c),
 // scan the values from the largest down and read off the top-k and top-p
