@@ -377,3 +377,27 @@ def test_pageable_draft_probs_are_rejected():
         ver.run(db)
     assert err.value.code == -1
     ver.close()
+
+
+def test_draft_probs_in_host_memory_under_early_exit():
+    """Early exit through its work queue (the row pass judges positions and
+    gathers q(x) itself) with draft_probs left in page-locked host memory:
+    the same outputs as with the rows on the device."""
+    import torch
+
+    import speculative_decoding_rejection_02_gb300 as sv
+    batch = synth.make("c5", B=40, V=20008)
+    batch["flags"] = sv.FLAG_EARLY_EXIT
+    R = batch["target_logits"].shape[0]
+    ver = sv.Verifier(max_batch=40, max_rows=R, max_vocab=20008,
+                      config_flags=sv.CONFIG_EARLY_QUEUE)
+    on_dev = sv.upload(batch, "cuda:0")
+    ver.run(on_dev)
+    on_host = sv.upload(batch, "cuda:0")
+    on_host.draft_probs = torch.from_numpy(batch["draft_probs"]).pin_memory()
+    ver.run(on_host)
+    torch.cuda.synchronize()
+    assert ver.status() == 0
+    assert torch.equal(on_dev.num_accepted, on_host.num_accepted)
+    assert torch.equal(on_dev.out_tokens, on_host.out_tokens)
+    ver.close()
