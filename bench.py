@@ -29,6 +29,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -40,6 +41,8 @@ if ROOT not in sys.path:
 import synth  # noqa: E402
 
 L2_BYTES = 129 * 2 ** 20
+METRIC = "verified draft positions/sec and achieved HBM GB/s (fraction of GB300 peak)"
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
 WORKLOADS = {
     "c2": "B=8 gamma=3 V=32000 fp32 logits N(0,2^2)+3 boosted tokens, probabilistic draft, T=1",
     "c3": ("B=64 gamma=5 V=128256 bf16 logits N(0,3^2)+Zipf(1.1), probabilistic draft, "
@@ -68,6 +71,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the c2/c3/c4 and early-exit timings beside the headline")
     return ap.parse_args()
 
 
@@ -134,6 +139,7 @@ class ClockSampler:
         self.proc = None
         self.out = None
         self.device = device_index
+        self.path = None
 
     def _gpu_id(self):
         try:
@@ -145,18 +151,14 @@ class ClockSampler:
 
     def start(self):
         try:
-            self.out = open(self._path(), "w")
+            fd, self.path = tempfile.mkstemp(prefix="spec_verify_clocks_", suffix=".csv")
+            self.out = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", self._gpu_id(), f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=self.out, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
-
-    def _path(self):
-        d = os.path.join(ROOT, "gpurun_out") if os.path.isdir(os.path.join(ROOT, "gpurun_out")) \
-            else "/tmp"
-        return os.path.join(d, f"clocks_{os.getpid()}.csv")
 
     def stop(self):
         if self.proc is None:
@@ -170,23 +172,109 @@ class ClockSampler:
         self.out.close()
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self._path()) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 8:
-                    continue
-                try:
-                    sm.append(float(parts[0]))
-                    mx.append(float(parts[1]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, parts[4:8]):
-                    if v.lower().startswith("active"):
-                        reasons.add(n)
+        with open(self.path) as f:
+            lines = f.readlines()
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
                 "reasons": sorted(reasons)}
+
+
+def timed_calls(ver, db, stream, dev, K, flush):
+    """K calls on `stream`, each bracketed by CUDA events on that stream and
+    split into phases by the library's phase events (row pass, accept scan,
+    race); the L2 flush buffer, if any, is rewritten before each call.
+    Returns per-call milliseconds and the phase averages."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    ph = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    for i in range(K):
+        if flush is not None:
+            flush.zero_()
+        ver.set_phase_events(ph[i])
+        ev[i][0].record(stream)
+        ver.run(db, stream)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    ver.set_phase_events(None)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    phases = {"rows": sum(p[0].elapsed_time(p[1]) for p in ph) / K,
+              "accept": sum(p[1].elapsed_time(p[2]) for p in ph) / K,
+              "race": sum(p[2].elapsed_time(p[3]) for p in ph) / K}
+    return step_ms, phases
+
+
+def flush_buffer(batch, dev):
+    """An L2-sized write between timed calls when the logits would fit in L2."""
+    import torch
+    if batch["target_logits"].nbytes < 2 * L2_BYTES:
+        return torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    return None
+
+
+def fractions(bytes_, ms_per_step, rows_ms, peak):
+    """Achieved GB/s of the row pass and of the whole call, against the
+    measured copy bandwidth and against the nominal HBM3e figure."""
+    rows_gbs = bytes_["row_pass"] / (rows_ms * 1e-3) / 1e9
+    call_gbs = bytes_["total"] / (ms_per_step * 1e-3) / 1e9
+    return {"rows_gbs": rows_gbs, "rows_frac": rows_gbs / peak,
+            "rows_frac_nominal": rows_gbs / NOMINAL_HBM_GBS,
+            "call_gbs": call_gbs, "call_frac": call_gbs / peak,
+            "call_frac_nominal": call_gbs / NOMINAL_HBM_GBS}
+
+
+def per_config_timings(sv, dev, stream, peak, main_batch, steps=30, warmup=5):
+    """The other target workloads timed on the same GPU and clocks as the
+    headline line: c2, c3 and c4 with the rejection rule, and the headline
+    batch with early exit. Device-timed like the headline (inputs resident)."""
+    import torch
+    out = {}
+    cases = [("c2", None, 0), ("c3", None, 0), ("c4", None, 0)]
+    if main_batch is not None:
+        cases.append((main_batch["name"] + " early-exit", main_batch, sv.FLAG_EARLY_EXIT))
+    for label, batch, flags in cases:
+        b = dict(batch) if batch is not None else synth.make(label)
+        b["flags"] = flags
+        R = b["target_logits"].shape[0]
+        ver = sv.Verifier(max_batch=b["B"], max_rows=R, max_vocab=b["V"], device=dev.index)
+        db = sv.upload(b, dev, with_p=False)
+        flush = flush_buffer(b, dev)
+        for _ in range(warmup):
+            ver.run(db, stream)
+        torch.cuda.synchronize(dev)
+        assert ver.status() == 0, f"device status bits set ({label})"
+        n_acc = db.num_accepted.cpu().numpy()
+        bytes_ = algorithmic_bytes(b, n_acc)
+        step_ms, phases = timed_calls(ver, db, stream, dev, steps, flush)
+        ms = sum(step_ms) / steps
+        N = int(b["cu_num_draft"][-1])
+        out[label] = {"workload": WORKLOADS.get(b["name"], b["name"]), "steps": steps,
+                      "ms_per_step": ms, "value": N / (ms * 1e-3), "unit": "draft_positions/s",
+                      "phases_ms": phases, "algorithmic_bytes_per_step": bytes_,
+                      "l2": ("inputs larger than L2" if flush is None
+                             else "L2 flushed between timed calls (512 MB write)"),
+                      **fractions(bytes_, ms, phases["rows"], peak)}
+        ver.close()
+        del db, flush
+        torch.cuda.empty_cache()
+    return out
 
 
 def measured_hbm_peak():
@@ -195,7 +283,7 @@ def measured_hbm_peak():
         with open(path) as f:
             return float(json.load(f)["hbm_gbs"]), "measured"
     except Exception:
-        return 6800.0, "fallback"
+        return 6800.0, "fallback (an earlier GB300 copy measurement)"
 
 
 def kernel_source_sha() -> str:
@@ -305,7 +393,7 @@ def run_reference(args, rank, world):
     dt = time.perf_counter() - t0
     v = pos / dt
     line = {
-        "impl": "reference", "metric": "verified draft positions/sec", "value": v,
+        "impl": "reference", "metric": METRIC, "value": v,
         "unit": "draft_positions/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -351,9 +439,7 @@ def main():
     db = sv.upload(batch, dev, with_p=False)
     stream = torch.cuda.current_stream(dev)
     in_bytes = sum(v for v in synth.batch_bytes(batch).values())
-    flush = None
-    if batch["target_logits"].nbytes < 2 * L2_BYTES:
-        flush = torch.empty(4 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush = flush_buffer(batch, dev)
 
     # Warm-up (also fixes the deterministic outcome used for the byte count).
     for _ in range(max(3, args.warmup)):
@@ -365,40 +451,26 @@ def main():
 
     # Timed region: K calls, per-call events and per-phase events.
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(K)]
-    ph = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     clocks = ClockSampler(local)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.3)
-    for i in range(K):
-        if flush is not None:
-            flush.zero_()
-        ver.set_phase_events(ph[i])
-        ev[i][0].record(stream)
-        ver.run(db, stream)
-        ev[i][1].record(stream)
-    torch.cuda.synchronize(dev)
+    step_ms, phases = timed_calls(ver, db, stream, dev, K, flush)
     clock_info = clocks.stop()
-    ver.set_phase_events(None)
     if world > 1:
         dist.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    rows_ms = [p[0].elapsed_time(p[1]) for p in ph]
-    accept_ms = [p[1].elapsed_time(p[2]) for p in ph]
-    race_ms = [p[2].elapsed_time(p[3]) for p in ph]
     total_ms = sum(step_ms)
     total_ms = max_over_ranks(total_ms, dev)
     ms_per_step = total_ms / K
     value = world * positions / (ms_per_step * 1e-3)
-    rows_avg = sum(rows_ms) / K
+    rows_avg = phases["rows"]
 
     peak, peak_kind = measured_hbm_peak()
-    achieved = bytes_["row_pass"] / (rows_avg * 1e-3) / 1e9
-    step_gbs = bytes_["total"] / (ms_per_step * 1e-3) / 1e9
+    fr = fractions(bytes_, ms_per_step, rows_avg, peak)
+    achieved = fr["rows_gbs"]
+    step_gbs = fr["call_gbs"]
 
     # End to end through the public API with host buffers. draft_probs stays
     # in page-locked host memory, which the library reads in place (only the
@@ -465,6 +537,11 @@ def main():
         cpu_all = {"value": rate, "unit": "draft_positions/s", "cores": thr, "kind": "oracle",
                    "sample": desc, "seconds": round(secs, 2)}
 
+    per_cfg = None
+    if (rank == 0 and world == 1 and args.B is None and not args.no_per_config
+            and args.config == "c5" and args.accept == "rejection" and not args.early_exit):
+        per_cfg = per_config_timings(sv, dev, stream, peak, batch)
+
     # row pass, accept scan, race; with top-k / top-p also the exact kernel
     # for the rows the row pass leaves unsettled
     filters = batch.get("top_k") is not None or batch.get("top_p") is not None
@@ -475,7 +552,7 @@ def main():
         launches_per_step = 3  # queue init, row pass, race
     if rank == 0:
         line = {
-            "metric": "verified draft positions/sec and achieved HBM GB/s (fraction of GB300 peak)",
+            "metric": METRIC,
             "value": value, "unit": "draft_positions/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
@@ -488,13 +565,16 @@ def main():
                        "early_exit": bool(args.early_exit),
                        "parallelism": f"replicas x{world}"},
             "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak,
+            "hbm_frac_nominal": fr["call_frac_nominal"],
             "algorithmic_bytes_per_step": bytes_,
-            "phases_ms": {"rows": rows_avg, "accept": sum(accept_ms) / K,
-                          "race": sum(race_ms) / K},
+            "phases_ms": phases,
             "roofline": {"bound": "hbm", "kernel": "target-row pass", "achieved": achieved,
                          "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS hbm_gbs)",
+                         "frac_nominal": fr["rows_frac_nominal"],
+                         "nominal_peak": NOMINAL_HBM_GBS,
                          "traffic": ncu_traffic(args.config)},
+            "per_config": per_cfg,
             "cpu_baseline": cpu,
             "cpu_baseline_all_cores": cpu_all,
             "e2e": e2e,

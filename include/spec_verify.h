@@ -233,10 +233,13 @@ int spec_verify_set_phase_events(spec_verify_handle* h, void* const* events, int
 
 /*
  * spec_verify_run_noalloc — spec_verify_run for callers that cannot allocate
- * device memory: code that runs inside a CUDA graph that is being captured
- * or replayed, inside a custom memory pool or allocator callback, or in a
- * process whose allocator is owned by another framework. It needs no handle
- * and calls no cudaMalloc, cudaFree or allocating library routine: its
+ * device memory: code running inside an allocator or memory-pool callback
+ * (allocating there would re-enter the allocator), a process whose device
+ * memory is all owned by another framework's caching allocator (a private
+ * cudaMalloc would sit outside its budget and its pool), and latency-bound
+ * loops that must not pay for cudaMalloc, which can synchronise the device.
+ * It needs no handle and calls no cudaMalloc, cudaFree or allocating library
+ * routine: its
  * scratch (row statistics, slice partials, race state) lives in one
  * file-scope device array of the library, SPEC_NOALLOC_SCRATCH_BYTES bytes
  * on every GPU that loads the library, held until the process exits.

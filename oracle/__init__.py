@@ -211,11 +211,17 @@ def _batch_struct(batch, keep):
     return b, B, int(cu[-1])
 
 
-def verify(batch, requests=None):
+def verify(batch, requests=None, threads: int = 1):
     """Run the oracle over a batch dict (see ``synth``) and return a dict of
     outputs and decision margins. ``requests`` restricts the work to a list of
     request indices (the other requests' slots keep their fill values:
-    tokens -2, counts -1, NaN margins)."""
+    tokens -2, counts -1, NaN margins).
+
+    ``threads`` > 1 splits the requests into that many disjoint sets (every
+    t-th request) and runs the unchanged single-threaded oracle on each set in
+    its own thread, all writing into the same output arrays: a request's
+    verification reads only the batch and writes only that request's slots,
+    so the result is the same as one thread's."""
     keep = []
     b, B, N = _batch_struct(batch, keep)
     R = N + B
@@ -230,11 +236,30 @@ def verify(batch, requests=None):
         "row_race_margin": np.full(R, np.nan),
     }
     o = _Outputs(**{k: _ptr(v) for k, v in out.items()})
-    if requests is None:
+    if requests is None and threads <= 1:
         rc = lib().or_verify(C.byref(b), C.byref(o))
     else:
-        reqs = np.ascontiguousarray(requests, dtype=np.int32)
-        rc = lib().or_verify_requests(C.byref(b), _ptr(reqs), reqs.size, C.byref(o))
+        reqs = np.ascontiguousarray(np.arange(B) if requests is None else requests,
+                                    dtype=np.int32)
+        L = lib()
+        if threads <= 1 or reqs.size < 2:
+            rc = L.or_verify_requests(C.byref(b), _ptr(reqs), reqs.size, C.byref(o))
+        else:
+            from concurrent.futures import ThreadPoolExecutor
+            parts = [np.ascontiguousarray(reqs[t::threads]) for t in range(threads)]
+            parts = [p for p in parts if p.size]
+            with ThreadPoolExecutor(len(parts)) as ex:
+                rcs = list(ex.map(lambda p: L.or_verify_requests(C.byref(b), _ptr(p), p.size,
+                                                                 C.byref(o)), parts))
+            rc = next((r for r in rcs if r != 0), 0)
     if rc != 0:
         raise ValueError(f"oracle verify failed ({rc})")
     return out
+
+
+def host_threads() -> int:
+    """Host cores this process may run on (for ``verify(threads=...)``)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1

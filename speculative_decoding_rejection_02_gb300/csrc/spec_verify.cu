@@ -210,22 +210,28 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
     const bool big = (long long)b->B >= 2ll * qblocks;
     if (!queue_ok || !(big || (h->cfg.flags & SPEC_CONFIG_EARLY_QUEUE))) P.early = 0;
   }
+  // Early exit: split each row into parts of about the target size (whole
+  // stages) when the workspace has room for it. The queue takes every row
+  // part plus one closing ticket per CTA; whole rows that still do not fit
+  // take the full pass instead.
+  int parts = 1;
+  long long part_bytes = (long long)b->V * esize;
   if (P.early) {
-    // Rows from the work queue, judged as they finish; no accept kernel.
-    // Split each row into parts of about the target size (whole stages),
-    // when the workspace has room for it.
     const long long row_bytes = (long long)b->V * esize;
     const long long stage = P.fast_filtered ? sv::tma_stage_bytes(true) : sv::tma_stage_bytes(false);
     const long long target = P.fast_filtered ? kPartTargetFiltered : kPartTarget;
-    int parts = (int)((row_bytes + target - 1) / target);
+    parts = (int)((row_bytes + target - 1) / target);
     parts = parts < 1 ? 1 : (parts > sv::kMaxParts ? sv::kMaxParts : parts);
-    long long part_bytes = ((row_bytes + parts - 1) / parts + stage - 1) / stage * stage;
+    part_bytes = ((row_bytes + parts - 1) / parts + stage - 1) / stage * stage;
     parts = (int)((row_bytes + part_bytes - 1) / part_bytes);
-    // The queue takes every row part plus one closing ticket per CTA.
     const long long tickets = (long long)(P.fast_filtered ? h->filt_blocks : h->tma_blocks);
     if (!h->part_stats || R * parts + tickets > h->q_cap) parts = 1;
+    if (R + tickets > h->q_cap) P.early = 0;
+  }
+  if (P.early) {
+    // Rows from the work queue, judged as they finish; no accept kernel.
     P.parts = parts;
-    P.part_bytes = parts > 1 ? part_bytes : row_bytes;
+    P.part_bytes = parts > 1 ? part_bytes : (long long)b->V * esize;
     if (cudaMemsetAsync(h->queue_ctl, 0, kQueueCtl * sizeof(unsigned), stream) != cudaSuccess ||
         cudaMemsetAsync(h->queue_ready, 0, (size_t)h->q_cap * sizeof(unsigned), stream) !=
             cudaSuccess)

@@ -22,3 +22,13 @@ def golden_lines(name):
             line = line.strip()
             if line and not line.startswith("#"):
                 yield line.split()
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Print the session's GPU-vs-oracle parity totals (decisions and excused
+    decisions per workload and acceptance rule), when any comparison ran."""
+    parity = sys.modules.get("parity")
+    if parity is None or not getattr(parity, "TALLY", None):
+        return
+    for line in parity.tally_lines():
+        terminalreporter.write_line(line)

@@ -8,10 +8,102 @@
   acceptance the decision at a position is the race drawn on its row.
 * p at the draft tokens: relative 1e-5 for fp32 logits, 2e-3 for bf16 (rows
   whose top-p boundary margin is below 1e-5 are skipped).
+
+Excused decisions are tallied per workload over the whole session
+(``TALLY``); the rule that they stay below 1e-4 of all decisions is asserted
+on those totals, with no allowance of one per test, by the test module that
+runs after the parity tests (``test_zy_parity_tally.py``), and the totals are
+printed at the end of the run.
 """
+import functools
+
 import numpy as np
 
 MARGIN = 1e-5
+EXCUSED_FRACTION = 1e-4
+
+# workload -> acceptance rule -> size -> running totals of the comparisons
+TALLY = {}
+
+
+def _mode(batch):
+    f = int(batch.get("flags", 0))
+    if f & 2:
+        return "sampler-match"
+    if f & 4:
+        return "early-exit"
+    if f & 1:
+        return "naive"
+    return "rejection"
+
+
+def _workload(batch):
+    name = str(batch.get("name", "edge"))
+    return "c1" if name.startswith("toy") else name
+
+
+def _size(batch):
+    import synth
+    cfg = synth.CONFIGS.get(batch.get("name"))
+    if cfg is None:
+        return "full" if str(batch.get("name", "")).startswith("toy") else "custom"
+    return "full" if (batch["B"] == cfg["B"] and batch["V"] == cfg["V"]) else "scaled"
+
+
+def _record(batch, rep):
+    key = (_workload(batch), _mode(batch), _size(batch))
+    t = TALLY.setdefault(key, dict(calls=0, requests=0, decisions=0, excused=0, p_checked=0,
+                                   p_max_rel=0.0))
+    t["calls"] += 1
+    for k in ("requests", "decisions", "excused", "p_checked"):
+        t[k] += rep[k]
+    t["p_max_rel"] = max(t["p_max_rel"], rep["p_max_rel"])
+
+
+def totals_by_workload():
+    """Per workload: decisions and excused decisions over every comparison of
+    the session (all acceptance rules and sizes)."""
+    out = {}
+    for (w, _, _), t in TALLY.items():
+        o = out.setdefault(w, dict(decisions=0, excused=0, requests=0, p_max_rel=0.0))
+        o["decisions"] += t["decisions"]
+        o["excused"] += t["excused"]
+        o["requests"] += t["requests"]
+        o["p_max_rel"] = max(o["p_max_rel"], t["p_max_rel"])
+    return out
+
+
+def tally_lines():
+    lines = ["parity tally (GPU vs oracle): workload / rule / size: requests, decisions, "
+             "excused, largest p(x) rel. error"]
+    for key in sorted(TALLY):
+        t = TALLY[key]
+        lines.append(f"  {key[0]:3s} {key[1]:13s} {key[2]:6s} {t['requests']:>8d} req "
+                     f"{t['decisions']:>9d} dec {t['excused']:>3d} exc  p {t['p_max_rel']:.2e}")
+    for w, t in sorted(totals_by_workload().items()):
+        lines.append(f"  {w:3s} all: {t['decisions']} decisions, {t['excused']} excused "
+                     f"(bound {EXCUSED_FRACTION:g} x decisions = "
+                     f"{EXCUSED_FRACTION * t['decisions']:.2f})")
+    return lines
+
+
+@functools.lru_cache(maxsize=None)
+def _full(name):
+    import synth
+    return synth.make(name)
+
+
+def full_batch(name):
+    """The full-size workload (generated once per session; a shallow copy, so
+    that a test may set flags or replace arrays without touching the cache)."""
+    return dict(_full(name))
+
+
+def oracle_all(batch, requests=None):
+    """The oracle over every request (or the given ones), on every host core:
+    the unchanged single-threaded oracle on disjoint request sets."""
+    import oracle
+    return oracle.verify(batch, requests=requests, threads=oracle.host_threads())
 
 
 def run_gpu(batch, greedy=False, device="cuda:0", verifier=None):
@@ -86,14 +178,16 @@ def compare(batch, gpu, ref, requests=None, check_p=True):
                     rep["p_max_rel"] = max(rep["p_max_rel"], rel)
                 if err > rtol * abs(po) + 1e-30:
                     rep["p_bad"].append((r, i, po, pg))
+    _record(batch, rep)
     return rep
 
 
-def assert_parity(rep, max_excused_frac=1e-4):
+def assert_parity(rep):
+    """Every difference excused and every p(x) within tolerance. The excused
+    decisions themselves are bounded on the session's totals per workload
+    (``totals_by_workload``), not per call."""
     assert not rep["unexcused"], rep["unexcused"][:5]
     assert not rep["p_bad"], rep["p_bad"][:5]
-    allowed = max(1, int(max_excused_frac * rep["decisions"]))
-    assert rep["excused"] <= allowed, rep
 
 
 def check_structure(batch, gpu):

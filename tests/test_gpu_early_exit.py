@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import synth
-from parity import assert_parity, check_structure, compare, run_gpu
+from parity import assert_parity, check_structure, compare, full_batch, oracle_all, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -81,15 +81,19 @@ def test_same_round_as_the_full_pass(name, schedule):
                            rtol=1e-5, atol=0)
 
 
-@pytest.mark.parametrize("name,n_sample", [("c4", 12), ("c5", 16)])
-def test_full_size_sampled(name, n_sample):
-    b = _early(synth.make(name))
-    gpu = run_gpu(b)  # the library's own choice of schedule
+@pytest.mark.parametrize("name,schedule", [
+    ("c3", "auto"), ("c4", "auto"), ("c5", "auto"),  # the library's own choice
+    ("c3", "queue"), ("c4", "queue"),                # the work queue at full size
+])
+def test_full_size_every_request(name, schedule):
+    b = _early(full_batch(name))
+    gpu = run_gpu(b) if schedule == "auto" else _run(b, schedule)
     assert gpu["status"] == 0
     check_structure(b, gpu)
-    reqs = np.sort(np.random.default_rng(11).choice(b["B"], size=n_sample, replace=False))
-    ref = oracle.verify(b, requests=reqs)
-    assert_parity(compare(b, gpu, ref, requests=reqs))
+    rep = compare(b, gpu, oracle_all(b))
+    assert rep["requests"] == b["B"]
+    assert_parity(rep)
+    _unread_are_nan(b, gpu)
 
 
 @pytest.mark.parametrize("schedule", SCHEDULES)

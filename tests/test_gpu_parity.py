@@ -1,12 +1,11 @@
-"""GPU verifier vs the CPU oracle, through the C ABI, on the five workloads
-(scaled variants in full, the full sizes on sampled requests plus
-size-independent properties)."""
+"""GPU verifier vs the CPU oracle, through the C ABI, on the five workloads:
+scaled variants and the full sizes, every request of each."""
 import numpy as np
 import pytest
 
 import oracle
 import synth
-from parity import assert_parity, check_structure, compare, run_gpu
+from parity import assert_parity, check_structure, compare, full_batch, oracle_all, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -55,18 +54,20 @@ def test_scaled_workloads(name, B, V):
     assert_parity(compare(b, gpu, ref))
 
 
-@pytest.mark.parametrize("name,n_sample", [("c3", 18), ("c4", 10), ("c5", 16)])
-def test_full_size_sampled(name, n_sample):
-    b = synth.make(name)
+@pytest.mark.parametrize("name", ["c3", "c4", "c5"])
+def test_full_size_every_request(name):
+    """The full workload, every request against the oracle (run on every host
+    core), and every temperature-0 request against numpy's argmax."""
+    b = full_batch(name)
     gpu = run_gpu(b)
     assert gpu["status"] == 0
     check_structure(b, gpu)
-    rng = np.random.default_rng(7)
-    reqs = np.sort(rng.choice(b["B"], size=n_sample, replace=False))
-    ref = oracle.verify(b, requests=reqs)
-    assert_parity(compare(b, gpu, ref, requests=reqs))
-    # temperature-0 requests, every one of them: the emitted tokens are the
-    # target argmax at each emitted position (argmax decoding)
+    ref = oracle_all(b)
+    rep = compare(b, gpu, ref)
+    assert rep["requests"] == b["B"]
+    assert_parity(rep)
+    # temperature-0 requests: the emitted tokens are the target argmax at each
+    # emitted position (argmax decoding)
     cu = b["cu_num_draft"]
     logits = b["target_logits"]
     for r in np.nonzero(b["temperature"] == 0)[0]:

@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import synth
-from parity import assert_parity, check_structure, compare, run_gpu
+from parity import assert_parity, check_structure, compare, full_batch, oracle_all, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -55,14 +55,15 @@ def test_scaled_workloads(name, B, V):
     assert rep["requests"] > 0
 
 
-def test_full_size_c4_sampled():
-    b = _sm(synth.make("c4"))
+@pytest.mark.parametrize("name", ["c3", "c4", "c5"])
+def test_full_size_every_request(name):
+    b = _sm(full_batch(name))
     gpu = run_gpu(b)
     assert gpu["status"] == 0
     check_structure(b, gpu)
-    reqs = np.sort(np.random.default_rng(8).choice(b["B"], size=10, replace=False))
-    ref = oracle.verify(b, requests=reqs)
-    assert_parity(compare(b, gpu, ref, requests=reqs))
+    rep = compare(b, gpu, oracle_all(b))
+    assert rep["requests"] == b["B"]
+    assert_parity(rep)
 
 
 def test_top_k_one_equals_greedy_entry_point():

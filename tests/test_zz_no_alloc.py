@@ -1,10 +1,14 @@
 """spec_verify_run_noalloc: the verification entry point for callers that
-cannot allocate device memory (graph capture or replay, allocator callbacks,
-processes whose allocator belongs to another framework). Its scratch is a
-fixed device array inside the library, so this test checks, through the C
+cannot allocate device memory (code inside an allocator or memory-pool
+callback, processes whose device memory belongs to another framework's
+caching allocator, loops that must not pay for a cudaMalloc). Its scratch is
+a fixed device array inside the library, so this test checks, through the C
 ABI, that it returns exactly what spec_verify_run returns on the same batch,
 on two calls in a row (the second call finds the array holding the first
-call's contents), and that it refuses batches beyond its stated limits.
+call's contents), on every part of the array: plain rows, misaligned rows,
+aligned bf16 rows with top-k / top-p (the window histogram and its list of
+unsettled rows) and early exit through the work queue; that it agrees with
+the oracle; and that it refuses batches beyond its stated limits.
 """
 import ctypes as C
 
@@ -12,8 +16,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 import speculative_decoding_rejection_02_gb300 as sv
+from parity import assert_parity, check_structure, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -44,15 +50,27 @@ def _run_noalloc(batch):
     return db.out_tokens.cpu().numpy(), db.num_accepted.cpu().numpy(), db.p_at_draft.cpu().numpy()
 
 
-@pytest.mark.parametrize("name,B,V", [("c5", 40, 65536), ("c3", 27, 30011), ("c2", 8, 32000)])
-def test_noalloc_matches_handle_entry_point(name, B, V):
+@pytest.mark.parametrize("name,B,V,early", [
+    ("c5", 40, 65536, False),   # bf16 rows through the bulk-copy row pass
+    ("c3", 27, 30011, False),   # misaligned rows: slice partials, exact filter kernel
+    ("c3", 27, 30008, False),   # aligned bf16 rows with top-k / top-p: window histogram
+    ("c2", 8, 32000, False),    # fp32 rows
+    ("c5", 700, 4096, True),    # early exit through the work queue (B >= 2 x row-pass CTAs)
+    ("c3", 640, 4000, True),    # early exit with filtered rows through the work queue
+])
+def test_noalloc_matches_handle_entry_point(name, B, V, early):
     batch = synth.make(name, B=B, V=V)
+    if early:
+        batch["flags"] = sv.FLAG_EARLY_EXIT
     ref_tok, ref_acc, ref_p = _run_handle(batch)
     for _ in range(2):  # two calls in a row share the array
         tok, acc, p = _run_noalloc(batch)
         assert np.array_equal(tok, ref_tok)
         assert np.array_equal(acc, ref_acc)
         np.testing.assert_allclose(p, ref_p, rtol=1e-6, atol=0)
+    gpu = dict(out_tokens=tok, num_accepted=acc, p_at_draft=p, status=0)
+    check_structure(batch, gpu)
+    assert_parity(compare(batch, gpu, oracle.verify(batch, threads=oracle.host_threads())))
 
 
 def test_noalloc_rejects_batches_beyond_its_limits():
