@@ -94,6 +94,8 @@ __device__ __forceinline__ void enqueue_match_races(const Params& P, int r, int 
 
 __global__ void __launch_bounds__(kAcceptWarps * 32)
 k_accept(Params P) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * kAcceptWarps + (threadIdx.x >> 5);
   if (r >= P.B) return;
@@ -251,6 +253,7 @@ k_accept(Params P) {
 // writes num_accepted. Other requests were finished by k_accept.
 __global__ void __launch_bounds__(kAcceptWarps * 32)
 k_match(Params P) {
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int r = blockIdx.x * kAcceptWarps + (threadIdx.x >> 5);
   if (r >= P.B) return;

@@ -76,6 +76,8 @@ __device__ __forceinline__ void request_done(const Params& P) {
 // Validate every request's offsets and queue the parts of its row 0 (one
 // thread per request). Invalid requests end here, as in k_accept.
 __global__ void k_early_init(Params P) {
+  pdl_wait();
+  pdl_trigger();
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= P.B) return;
   const int c0 = __ldg(P.cu + r), c1 = __ldg(P.cu + r + 1);

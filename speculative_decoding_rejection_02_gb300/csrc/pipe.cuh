@@ -118,6 +118,16 @@ __device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsig
   return d;
 }
 
+// Programmatic dependent launch (the kernels of one call are chained with
+// it): wait until the previous kernel of the stream has completed and its
+// writes are visible (returns at once when this kernel was launched without
+// a programmatic dependency), and allow the next kernel of the stream to be
+// launched (its blocks then wait in pdl_wait for this whole grid).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier over the first `threads` threads of the block (id 1..15).
 __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");

@@ -468,6 +468,7 @@ __device__ __forceinline__ void race_dispatch(bool bf16, bool has_q, bool theta,
 
 __global__ void __launch_bounds__(kRaceThreads, 4)
 k_race(Params P) {
+  pdl_wait();
   extern __shared__ __align__(128) unsigned char race_smem[];
   __shared__ int s_last;
   __shared__ unsigned long long s_packed;

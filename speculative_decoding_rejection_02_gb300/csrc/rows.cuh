@@ -14,6 +14,7 @@
 //    for top-k, probability mass for top-p), re-reading the row each step.
 #pragma once
 #include "common.cuh"
+#include "pipe.cuh"
 
 namespace sv {
 
@@ -60,7 +61,7 @@ __device__ void finish_row_x(const Params& P, long long row, int cls, float m, i
     if (cls == kArgmaxOnly) {
       p_x = (x == argmax) ? 1.f : 0.f;
     } else if (st == 0) {
-      p_x = (lx >= theta) ? exp2f(fmaf(lx, c, -(m * c))) / z : 0.f;
+      p_x = (lx >= theta) ? exp2f(fmaf(lx, c, -__fmul_rn(m, c))) / z : 0.f;
     }
   }
   RowStats s;
@@ -108,6 +109,8 @@ __device__ __forceinline__ bool locate_row(const Params& P, long long row, int& 
 
 __global__ void __launch_bounds__(kStreamThreads)
 k_rows_stream(Params P) {
+  pdl_wait();
+  pdl_trigger();
   const int spr = P.slices_per_row;
   const long long row = (long long)blockIdx.x / spr;
   const int slice = (int)(blockIdx.x % spr);
@@ -381,6 +384,8 @@ __device__ void filtered_row(const Params& P, long long row) {
 // the blocks share out the rows that pass listed as unsettled.
 __global__ void __launch_bounds__(kFilterThreads)
 k_rows_filtered(Params P) {
+  pdl_wait();
+  pdl_trigger();
   if (!P.fast_filtered) {
     filtered_row(P, blockIdx.x);
     return;

@@ -199,6 +199,8 @@ struct ConsumerGroup {
 template <bool BF16, bool FILT, bool EARLY = false, bool SHARD = false>
 __global__ void __launch_bounds__(kTmaThreads, 2)
 k_rows_tma(Params P, long long R) {
+  pdl_wait();
+  pdl_trigger();
   static_assert(!FILT || BF16, "the histogram path is for bf16 rows");
   constexpr int kTmaStageBytes = tma_stage_bytes(FILT);
   constexpr int kTmaVecPerThread = tma_vec_per_thread(FILT);
@@ -449,8 +451,10 @@ k_rows_tma(Params P, long long R) {
     }
     if (m32 > vmax || (imax == kNoIndex && m32 > -INFINITY)) {
       // New running max: rescale, and remember the vector that holds it.
-      const float nmc = m32 * M.c;
-      if (soft && vmax > -INFINITY) s *= ex2(vmc - nmc);
+      // (every product and sum of Z with its own rounding: no instantiation
+      // of this kernel may fuse them, so all give the same statistics)
+      const float nmc = __fmul_rn(m32, M.c);
+      if (soft && vmax > -INFINITY) s = __fmul_rn(s, ex2(__fsub_rn(vmc, nmc)));
       // The lowest index holding it: the first vector whose max it is, then
       // the first element of that vector.
       int kk = kTmaVecPerThread - 1;
@@ -500,7 +504,7 @@ k_rows_tma(Params P, long long R) {
       float a0, a1, a2, a3;
       f2_unpack(acc0, a0, a1);
       f2_unpack(acc1, a2, a3);
-      s += (a0 + a1) + (a2 + a3);
+      s = __fadd_rn(s, __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3)));
     }
     if (FILT && M.cls == kFiltered) {
       // Count the elements at or above this thread's window floor (its
@@ -577,9 +581,9 @@ k_rows_tma(Params P, long long R) {
       a = bc_i;
       if constexpr (SHARD) {
         // Local statistics of this rank's columns (global indices).
-        const float mc = m * M.c;
+        const float mc = __fmul_rn(m, M.c);
         float part = 0.f;
-        if (soft && vmax > -INFINITY && m > -INFINITY) part = s * ex2(vmc - mc);
+        if (soft && vmax > -INFINITY && m > -INFINITY) part = __fmul_rn(s, ex2(__fsub_rn(vmc, mc)));
         part = warp_sum(part);
         if (lane == 0) red_s[warp] = part;
         if (FILT && M.cls == kFiltered) {
@@ -617,9 +621,9 @@ k_rows_tma(Params P, long long R) {
         // End of one part of the row: publish the part's statistics (and add
         // its window histogram to the request's global one). The CTA that
         // ends the row's last part merges them and judges the position.
-        const float mc = m * M.c;
+        const float mc = __fmul_rn(m, M.c);
         float part = 0.f;
-        if (soft && vmax > -INFINITY && m > -INFINITY) part = s * ex2(vmc - mc);
+        if (soft && vmax > -INFINITY && m > -INFINITY) part = __fmul_rn(s, ex2(__fsub_rn(vmc, mc)));
         part = warp_sum(part);
         if (lane == 0) red_s[warp] = part;
         WinHist* ghist = reinterpret_cast<WinHist*>(P.part_hist) + M.r;
@@ -682,9 +686,9 @@ k_rows_tma(Params P, long long R) {
         }
       }
       if (FILT && M.cls == kFiltered) {
-        const float mc = m * M.c;
+        const float mc = __fmul_rn(m, M.c);
         float part = 0.f;
-        if (vmax > -INFINITY && m > -INFINITY) part = s * ex2(vmc - mc);
+        if (vmax > -INFINITY && m > -INFINITY) part = __fmul_rn(s, ex2(__fsub_rn(vmc, mc)));
         if (!(EARLY && P.parts > 1)) part = warp_sum(part);
         float zfull = zmerged;
         if (!(EARLY && P.parts > 1)) {
@@ -724,11 +728,11 @@ k_rows_tma(Params P, long long R) {
         imax = kNoIndex;
         continue;
       }
-      const float mc = m * M.c;
+      const float mc = __fmul_rn(m, M.c);
       const bool merged_row = EARLY && P.parts > 1;
       float part = 0.f;
       if (!merged_row) {
-        if (soft && vmax > -INFINITY && m > -INFINITY) part = s * ex2(vmc - mc);
+        if (soft && vmax > -INFINITY && m > -INFINITY) part = __fmul_rn(s, ex2(__fsub_rn(vmc, mc)));
         part = warp_sum(part);
         if (lane == 0) red_s[warp] = part;
         named_sync(1, kTmaConsumers);

@@ -77,6 +77,28 @@ constexpr size_t kQueueSpare = 1024;
 constexpr long long kPartTarget = 512 * 1024;
 constexpr long long kPartTargetFiltered = 128 * 1024;
 
+// Launch a kernel that depends on the previous one in the stream with
+// programmatic dependent launch: it may be launched while that kernel runs
+// (after its pdl_trigger) and waits in pdl_wait for its completion, so the
+// launch latency between the kernels of one call overlaps the previous
+// kernel's tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                         cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 int check_batch(const spec_verify_config* cfg, const spec_verify_batch* b, bool greedy) {
   if (!cfg || !b) return SPEC_ERR_INVALID_ARG;
   if (b->B < 0 || b->N < 0 || b->V < 1) return SPEC_ERR_INVALID_ARG;
@@ -246,20 +268,20 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
     const long long items = (long long)b->B * parts;  // in flight at most
     const int grid = items < blocks ? (int)items : blocks;
     if (P.fast_filtered)
-      sv::k_rows_tma<true, true, true><<<grid, sv::kTmaThreads, sv::kTmaFiltSmemBytes, stream>>>(
-          P, R);
+      launch_after(sv::k_rows_tma<true, true, true>, grid, sv::kTmaThreads, sv::kTmaFiltSmemBytes,
+                   stream, P, R);
     else if (P.bf16)
-      sv::k_rows_tma<true, false, true><<<grid, sv::kTmaThreads, sv::kTmaSmemBytes, stream>>>(
-          P, R);
+      launch_after(sv::k_rows_tma<true, false, true>, grid, sv::kTmaThreads, sv::kTmaSmemBytes,
+                   stream, P, R);
     else
-      sv::k_rows_tma<false, false, true><<<grid, sv::kTmaThreads, sv::kTmaSmemBytes, stream>>>(
-          P, R);
+      launch_after(sv::k_rows_tma<false, false, true>, grid, sv::kTmaThreads, sv::kTmaSmemBytes,
+                   stream, P, R);
     if (timed) {
       cudaEventRecord(h->phase[1], stream);
       cudaEventRecord(h->phase[2], stream);
     }
-    sv::k_race<<<(unsigned)(races * P.race_slices), sv::kRaceThreads,
-                 sv::race_smem_bytes(P.bf16 ? 2 : 4, P.q != nullptr), stream>>>(P);
+    launch_after(sv::k_race, (unsigned)(races * P.race_slices), sv::kRaceThreads,
+                 sv::race_smem_bytes(P.bf16 ? 2 : 4, P.q != nullptr), stream, P);
     if (timed) cudaEventRecord(h->phase[3], stream);
     if (cudaPeekAtLastError() != cudaSuccess) {
       cudaGetLastError();
@@ -287,18 +309,18 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
     // Every filtered row (one block each), or only the listed ones.
     const long long cap = 2ll * h->sm_count;
     const long long sgrid = P.fast_filtered ? (R < cap ? R : cap) : R;
-    sv::k_rows_filtered<<<(unsigned)sgrid, sv::kFilterThreads, 0, stream>>>(P);
+    launch_after(sv::k_rows_filtered, (unsigned)sgrid, sv::kFilterThreads, 0, stream, P);
   }
   if (timed) cudaEventRecord(h->phase[1], stream);
-  sv::k_accept<<<(b->B + sv::kAcceptWarps - 1) / sv::kAcceptWarps, sv::kAcceptWarps * 32, 0,
-                 stream>>>(P);
+  launch_after(sv::k_accept, (unsigned)((b->B + sv::kAcceptWarps - 1) / sv::kAcceptWarps),
+               sv::kAcceptWarps * 32, 0, stream, P);
   if (timed) cudaEventRecord(h->phase[2], stream);
   if (!greedy) {
-    sv::k_race<<<(unsigned)(races * P.race_slices), sv::kRaceThreads,
-                 sv::race_smem_bytes(P.bf16 ? 2 : 4, P.q != nullptr), stream>>>(P);
+    launch_after(sv::k_race, (unsigned)(races * P.race_slices), sv::kRaceThreads,
+                 sv::race_smem_bytes(P.bf16 ? 2 : 4, P.q != nullptr), stream, P);
     if (match)
-      sv::k_match<<<(b->B + sv::kAcceptWarps - 1) / sv::kAcceptWarps, sv::kAcceptWarps * 32, 0,
-                    stream>>>(P);
+      launch_after(sv::k_match, (unsigned)((b->B + sv::kAcceptWarps - 1) / sv::kAcceptWarps),
+                   sv::kAcceptWarps * 32, 0, stream, P);
   }
   if (timed) cudaEventRecord(h->phase[3], stream);
   if (cudaPeekAtLastError() != cudaSuccess) {
