@@ -130,6 +130,7 @@ struct Params {
   void* part_hist;          // [max_batch] WinHist: merged window histograms
   int slices_per_row;
   int race_slices;
+  int race_slice_n;          // entries per race task (a power of two, at most race_slice())
   // Vocab-sharded calls: the local columns are global v0 .. v0 + V - 1.
   int v0;                    // 0 otherwise
   int Vg;                    // the full vocabulary (V otherwise)

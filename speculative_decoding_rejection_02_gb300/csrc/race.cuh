@@ -38,6 +38,8 @@ constexpr int kRaceThreads = 256;
 constexpr int kRaceSlice = 8192;
 constexpr int kRaceSliceNoQ = 16384;
 __host__ __device__ constexpr int race_slice(bool has_q) { return has_q ? kRaceSlice : kRaceSliceNoQ; }
+// Calls with too few races to fill the GPU halve the slice down to this.
+constexpr int kRaceSliceMin = 1024;
 constexpr int kRaceGroups = 4;    // groups of 4 entries per thread per batch
 // Above 1 / E_min, E_min = -ln(1 - 2^-24) ~ 5.96e-8 the smallest E a race
 // uniform can give: no entry scores more than w * kInvEMin.
@@ -491,7 +493,7 @@ k_race(Params P) {
                                task.inv_z, task.theta, task.z);
   const int V = P.V;
   const uint32_t groups = (uint32_t)((V + 3) / 4);
-  const int slice_n = race_slice(P.q != nullptr);
+  const int slice_n = P.race_slice_n;
   const uint32_t g0 = (uint32_t)slice * (uint32_t)(slice_n / 4);
   const uint32_t g1 = min(groups, g0 + (uint32_t)(slice_n / 4));
   const int j0 = (int)(g0 * 4u);

@@ -191,6 +191,7 @@ sv::Params make_params(spec_verify_handle* h, const spec_verify_batch* b, bool g
   const int slice = P.bf16 ? sv::kSliceBf16 : sv::kSliceF32;
   P.slices_per_row = (b->V + slice - 1) / slice;
   const int rslice = sv::race_slice(P.q != nullptr);
+  P.race_slice_n = rslice;
   P.race_slices = (b->V + rslice - 1) / rslice;
   P.v0 = 0;
   P.Vg = b->V;
@@ -211,6 +212,12 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   const bool match = !greedy && (P.flags & SPEC_FLAG_SAMPLER_MATCH);
   // Races: one per request (its k* row), or one per row under sampler-match.
   const long long races = match ? R : (long long)b->B;
+  // Too few race tasks to give every SM two: smaller slices (the race of a
+  // small batch is latency-bound, so more CTAs finish it sooner).
+  while (P.race_slice_n > sv::kRaceSliceMin && races * P.race_slices < 2ll * h->sm_count) {
+    P.race_slice_n /= 2;
+    P.race_slices = (b->V + P.race_slice_n - 1) / P.race_slice_n;
+  }
   if (R * P.slices_per_row > 0x7FFFFFFFll || races * P.race_slices > 0x7FFFFFFFll)
     return SPEC_ERR_CAPACITY;
   const bool timed = h->n_phase >= 4;
