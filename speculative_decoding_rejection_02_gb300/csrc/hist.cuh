@@ -11,16 +11,18 @@
 // the top-p boundary lies inside the window [m - D, m]. For top-k the window
 // is 30 / c wide (weights down to 2^-30 of the maximum's).
 //
-// While the row streams, each thread drops an element unless it lies at or
-// above its floor, (its own running max) - D rounded down to bf16; every
-// running max is at most m, so every element at or above m - D is counted. A
+// While the row streams, each thread counts every element of a full stage
+// and, in a row's last (partial, padded) stage, only those at or above its
+// floor, (its own running max) - D rounded down to bf16; every running max
+// is at most m, so every element at or above m - D is counted. A
 // counted element adds 1 to the counter of its value: per sign, one 32-bit
 // counter per bf16 magnitude in [2^-16, 2^8) (3072 values), one for all
 // smaller magnitudes (whose exact weights 2^(l c) are summed beside it) and
-// one for 2^8 and above (+inf included), which sends the row to the exact
-// slow path. The counters of a bf16 word's two values come from a few packed
-// 16-bit operations (magnitude clamp, sign offset), one packed compare with
-// the floor and one predicated shared-memory add each.
+// one for 2^8 and above (+inf and -inf included), which sends the row to the
+// exact slow path when it can matter (positive, or a window reaching -2^8).
+// The counters of a bf16 word's two values come from a few packed 16-bit
+// operations (magnitude clamp, sign offset) and one shared-memory add each
+// (predicated by a packed compare with the floor in the last stage only).
 //
 // At the row's end the consumers turn counts into masses n 2^(v c - m c),
 // scan the values from the largest down and read off the top-k and top-p
@@ -123,6 +125,33 @@ __device__ __forceinline__ void win_count(WinHist* h, const uint32_t w[4], uint3
     red_add2_if_ge(base + 4u * (s2 & 0xFFFFu), base + 4u * (s2 >> 16), w[t], f2);
   }
 }
+
+// Count every element of 4 words (a full stage: no padding in it) with the
+// slots of win_count and no compare: an unpredicated add costs far less
+// than the packed compare and two predicated adds. Elements below the
+// window land in counters the row end does not read (items below its
+// floor); -inf and magnitudes of 2^8 and above land in the huge counters,
+// of which the negative one matters only to a window reaching -2^8.
+__device__ __forceinline__ void win_count_all(WinHist* h, const uint32_t w[4], uint32_t& mn2) {
+  const uint32_t base = smem_addr(h->cnt) - 4u * kWinMagLo;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t mag2 = w[t] & 0x7FFF7FFFu;
+    uint32_t d2;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(mn2) : "r"(mn2), "r"(mag2));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d2) : "r"(mag2), "r"(0x377F377Fu));
+    asm("min.u16x2 %0, %1, %2;" : "=r"(d2) : "r"(d2), "r"(0x43804380u));
+    const uint32_t s2 = d2 + ((w[t] >> 15) & 0x00010001u) * (uint32_t)kWinSide;
+    asm volatile("red.shared.add.u32 [%0], 1;\n\tred.shared.add.u32 [%1], 1;" ::"r"(
+                     base + 4u * (s2 & 0xFFFFu)),
+                 "r"(base + 4u * (s2 >> 16))
+                 : "memory");
+  }
+}
+
+// The packed floor below every finite value: win_tiny's floor for the
+// elements win_count_all counts.
+constexpr uint32_t kWinFloorAll2 = 0xFF7FFF7Fu;
 
 // After win_count over a thread's words of a stage (smallest magnitudes
 // mn2): the rare tiny magnitudes (below 2^-16) that were counted also add
@@ -265,7 +294,11 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, floa
       float w;
       bool whole;
       if (i == kWinHugeNeg || i == kWinHugePos) {
-        huge |= (n != 0u);
+        // Counted values of magnitude 2^8 and above: +inf, NaN or a huge
+        // positive value (then the row's max), or huge negatives and -inf,
+        // which lie below a window floor above -2^8 and matter only to a
+        // window reaching it.
+        huge |= (n != 0u) && (i == kWinHugePos || !(lo > -256.f));
         w = 0.f;
         whole = false;
       } else if (i == kWinTinyNeg || i == kWinTinyPos) {

@@ -507,9 +507,12 @@ k_rows_tma(Params P, long long R) {
       s = __fadd_rn(s, __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3)));
     }
     if (FILT && M.cls == kFiltered) {
-      // Count the elements at or above this thread's window floor (its
-      // running max minus D; -inf and the padding never count).
-      const uint32_t flo2 = win_floor2(fmaxf(vmax - M.delta, -3.402823466e38f));
+      // Count every element of a full stage; in the row's last (padded)
+      // stage only those at or above this thread's window floor (its
+      // running max minus D; -inf and the padding never count there).
+      const bool full_stage = (nvec == kTmaVecPerThread * kTmaConsumers);
+      const uint32_t flo2 =
+          full_stage ? kWinFloorAll2 : win_floor2(fmaxf(vmax - M.delta, -3.402823466e38f));
       uint32_t words[4 * kTmaVecPerThread];
       uint32_t mn2 = 0xFFFFFFFFu;
 #pragma unroll
@@ -519,7 +522,8 @@ k_rows_tma(Params P, long long R) {
         words[4 * k + 1] = v[k].y;
         words[4 * k + 2] = v[k].z;
         words[4 * k + 3] = v[k].w;
-        win_count(hist, w, flo2, mn2);
+        if (full_stage) win_count_all(hist, w, mn2);
+        else win_count(hist, w, flo2, mn2);
       }
       win_tiny(hist, words, flo2, mn2, M.c);
     }
