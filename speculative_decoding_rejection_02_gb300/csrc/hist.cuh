@@ -1,36 +1,26 @@
-// Exact top-k / top-p on bf16 rows from a window histogram of values.
+// Exact top-k / top-p on bf16 rows from a histogram of values.
 //
 // A bf16 logit takes one of 65536 values, so the tempered, filtered
 // distribution of a row (velog "vLLM 커널은 이 규칙을 어떻게 옮겼나":
 // temperature, top-k and top-p applied before the judgement) is fixed by how
-// many tokens hold each value. Only values near the row maximum m can decide
-// the thresholds. For top-p, the tokens below m - D with
-//   D = (log2(V / (1 - top_p)) + 1) / c,   c = log2(e) / T,
-// weigh less than (1 - top_p) / 2 in units of the maximum's weight, and
-// Z >= 1 in those units, so the mass at or above m - D exceeds top_p Z and
-// the top-p boundary lies inside the window [m - D, m]. For top-k the window
-// is 30 / c wide (weights down to 2^-30 of the maximum's).
+// many tokens hold each value. While the row streams, every element adds 1
+// to the counter of its value: per sign, one 32-bit counter per bf16
+// magnitude in [2^-16, 2^8) (3072 values), one for all smaller magnitudes
+// (whose exact weights 2^(l c), c = log2(e) / T, are summed beside it) and
+// one for 2^8 and above (+inf and -inf included). The counters of a bf16
+// word's two values come from a few packed 16-bit operations (magnitude
+// clamp, sign offset) and one unpredicated shared-memory add each; the -inf
+// padding of a stage that the row does not fill is taken out of the
+// negative huge counter again.
 //
-// While the row streams, each thread counts every element of a full stage
-// and, in a row's last (partial, padded) stage, only those at or above its
-// floor, (its own running max) - D rounded down to bf16; every running max
-// is at most m, so every element at or above m - D is counted. A
-// counted element adds 1 to the counter of its value: per sign, one 32-bit
-// counter per bf16 magnitude in [2^-16, 2^8) (3072 values), one for all
-// smaller magnitudes (whose exact weights 2^(l c) are summed beside it) and
-// one for 2^8 and above (+inf and -inf included), which sends the row to the
-// exact slow path when it can matter (positive, or a window reaching -2^8).
-// The counters of a bf16 word's two values come from a few packed 16-bit
-// operations (magnitude clamp, sign offset) and one shared-memory add each
-// (predicated by a packed compare with the floor in the last stage only).
-//
-// At the row's end the consumers turn counts into masses n 2^(v c - m c),
-// scan the values from the largest down and read off the top-k and top-p
+// At the row's end the consumers turn counts into masses n 2^(v c - m c)
+// (m the row max): their sum is Z, no per-element exponential is needed.
+// Scanning the values from the largest down gives the top-k and top-p
 // thresholds, Z over the kept set and the kept set itself: exact for every
-// value, one read of the row, no sort, no per-element exp beyond the row
-// sum. The row goes to the slow path when a threshold falls on a tiny-value
-// counter or outside the window (top-k with fewer than k tokens in it), or
-// when the row holds NaN or +inf.
+// value, one read of the row, no sort. The row goes to the exact slow path
+// when a threshold falls on the tiny-value counter, when the row holds NaN,
+// +inf or a value of 2^8 and above, or when huge negative values could
+// weigh in Z ((m + 2^8) c < 50).
 #pragma once
 #include "common.cuh"
 #include "pipe.cuh"
@@ -55,15 +45,13 @@ constexpr int kWinHugeNeg = 0;
 constexpr int kWinTinyNeg = kWinSide - 1;
 constexpr int kWinTinyPos = kWinSide;
 constexpr int kWinHugePos = kWinSlots - 1;
-constexpr float kWinTopKWidth = 30.f;  // top-k window, in units of 1 / c
-constexpr float kWinTinyNegLow = -1.52587890625e-05f;  // -2^-16
 
 static_assert(kWinSlots == SPEC_SHARD_HIST_INTS, "the sharded histogram rows hold the slots");
 static_assert(kWinSlots % 4 == 0, "the counters are cleared with 16-byte stores");
 
 struct WinHist {
   unsigned cnt[kWinSlots];  // by slot
-  float tiny_w[2];          // sums of 2^(l c) of the counted tiny values: [0] negative, [1] positive
+  float tiny_w[2];          // sums of 2^(l c) of the tiny values: [0] negative, [1] positive
   unsigned pad[2];
 };
 static_assert(sizeof(WinHist) % 16 == 0, "cleared with 16-byte stores");
@@ -72,45 +60,13 @@ __device__ __forceinline__ int win_slot_of_item(int i) {
   return i < kWinSide ? kWinSlots - 1 - i : i - kWinSide;
 }
 
-// Window half-width D (logit units) of a filtered row; c > 0.
-__device__ __forceinline__ float win_delta(float c, int tk, float tp, int V) {
-  float d = 0.f;
-  if (tp < 1.f) d = (log2f((float)V / (1.f - tp)) + 1.f) / c;
-  if (tk > 0 && tk < V) d = fmaxf(d, kWinTopKWidth / c);
-  return d;
-}
-
-// The window floor as a pair of bf16 values: the largest bf16 at or below
-// f (a lower floor only counts more), never -inf (so -inf logits and the
-// padding are never counted), in both halves.
-__device__ __forceinline__ uint32_t win_floor2(float f) {
-  const uint32_t b = __float_as_uint(f);
-  uint32_t t = b >> 16;                              // toward zero
-  if ((b & 0x80000000u) && (b & 0xFFFFu)) t += 1u;   // negative: one step further down
-  if (t == 0xFF80u) t = 0xFF7Fu;                     // -inf: the lowest finite bf16
-  return t | (t << 16);
-}
-
-// Shared-memory adds of 1 to the counters at byte addresses a0 and a1 for
-// the low and high bf16 of w that are at or above the packed floor f2: one
-// packed compare, two predicated adds.
-__device__ __forceinline__ void red_add2_if_ge(uint32_t a0, uint32_t a1, uint32_t w, uint32_t f2) {
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ge.bf16x2 p|q, %2, %3;\n\t"
-      "@p red.shared.add.u32 [%0], 1;\n\t"
-      "@q red.shared.add.u32 [%1], 1;\n\t}" ::"r"(a0),
-      "r"(a1), "r"(w), "r"(f2)
-      : "memory");
-}
-
-// Count the elements of 4 words of packed bf16 pairs that lie at or above
-// the packed floor f2 (win_floor2): per word, the two slots from packed
-// 16-bit operations, one packed compare and one predicated shared-memory add
-// per element. mn2 keeps the smallest magnitudes seen (per half), for
-// win_tiny.
-__device__ __forceinline__ void win_count(WinHist* h, const uint32_t w[4], uint32_t f2,
-                                          uint32_t& mn2) {
+// Count every element of 4 words of packed bf16 pairs: per word, the two
+// slots from packed 16-bit operations and one shared-memory add per element
+// (unpredicated: a packed compare and predicated adds cost about ten more
+// instructions per word). mn2 / mx2 keep the smallest / largest magnitudes
+// seen (per half), for win_tiny / win_nan.
+__device__ __forceinline__ void win_count_all(WinHist* h, const uint32_t w[4], uint32_t& mn2,
+                                              uint32_t& mx2) {
   // byte address of slot 0, less the clamp offset folded in
   const uint32_t base = smem_addr(h->cnt) - 4u * kWinMagLo;
 #pragma unroll
@@ -118,29 +74,10 @@ __device__ __forceinline__ void win_count(WinHist* h, const uint32_t w[4], uint3
     const uint32_t mag2 = w[t] & 0x7FFF7FFFu;
     uint32_t d2;
     asm("min.u16x2 %0, %1, %2;" : "=r"(mn2) : "r"(mn2), "r"(mag2));
+    asm("max.u16x2 %0, %1, %2;" : "=r"(mx2) : "r"(mx2), "r"(mag2));
     asm("max.u16x2 %0, %1, %2;" : "=r"(d2) : "r"(mag2), "r"(0x377F377Fu));
     asm("min.u16x2 %0, %1, %2;" : "=r"(d2) : "r"(d2), "r"(0x43804380u));
     // + kWinSide per negative half (no carry: every half stays below 2^16)
-    const uint32_t s2 = d2 + ((w[t] >> 15) & 0x00010001u) * (uint32_t)kWinSide;
-    red_add2_if_ge(base + 4u * (s2 & 0xFFFFu), base + 4u * (s2 >> 16), w[t], f2);
-  }
-}
-
-// Count every element of 4 words (a full stage: no padding in it) with the
-// slots of win_count and no compare: an unpredicated add costs far less
-// than the packed compare and two predicated adds. Elements below the
-// window land in counters the row end does not read (items below its
-// floor); -inf and magnitudes of 2^8 and above land in the huge counters,
-// of which the negative one matters only to a window reaching -2^8.
-__device__ __forceinline__ void win_count_all(WinHist* h, const uint32_t w[4], uint32_t& mn2) {
-  const uint32_t base = smem_addr(h->cnt) - 4u * kWinMagLo;
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const uint32_t mag2 = w[t] & 0x7FFF7FFFu;
-    uint32_t d2;
-    asm("min.u16x2 %0, %1, %2;" : "=r"(mn2) : "r"(mn2), "r"(mag2));
-    asm("max.u16x2 %0, %1, %2;" : "=r"(d2) : "r"(mag2), "r"(0x377F377Fu));
-    asm("min.u16x2 %0, %1, %2;" : "=r"(d2) : "r"(d2), "r"(0x43804380u));
     const uint32_t s2 = d2 + ((w[t] >> 15) & 0x00010001u) * (uint32_t)kWinSide;
     asm volatile("red.shared.add.u32 [%0], 1;\n\tred.shared.add.u32 [%1], 1;" ::"r"(
                      base + 4u * (s2 & 0xFFFFu)),
@@ -149,26 +86,34 @@ __device__ __forceinline__ void win_count_all(WinHist* h, const uint32_t w[4], u
   }
 }
 
-// The packed floor below every finite value: win_tiny's floor for the
-// elements win_count_all counts.
-constexpr uint32_t kWinFloorAll2 = 0xFF7FFF7Fu;
+// A NaN among a thread's counted elements (largest magnitudes mx2 above
+// that of infinity) makes the positive tiny-value weight sum NaN, so the
+// row's Z is NaN at its end (also after the histograms of several parts or
+// ranks are summed).
+__device__ __forceinline__ void win_nan(WinHist* h, uint32_t mx2) {
+  if (max(mx2 & 0xFFFFu, mx2 >> 16) > 0x7F80u) atomicAdd(&h->tiny_w[1], __int_as_float(0x7FC00000));
+}
 
-// After win_count over a thread's words of a stage (smallest magnitudes
-// mn2): the rare tiny magnitudes (below 2^-16) that were counted also add
-// their weight 2^(l c) to their side's sum, on a path the warp takes only
-// when some lane holds one. Huge ones need nothing here.
+// Elements of a stage holding n (bf16) elements, whole 16-byte vectors:
+// the padding that win_count_all counted as -inf (negative huge counter).
+__device__ __forceinline__ unsigned win_pad(int n, int stage_elems) {
+  return (unsigned)(stage_elems - n);
+}
+
+// After win_count_all over a thread's words of a stage (smallest magnitudes
+// mn2): the rare tiny magnitudes (below 2^-16) also add their weight
+// 2^(l c) to their side's sum, on a path the warp takes only when some lane
+// holds one. Huge ones need nothing here.
 template <int kWords>
-__device__ __forceinline__ void win_tiny(WinHist* h, const uint32_t (&w)[kWords], uint32_t f2,
-                                         uint32_t mn2, float c) {
+__device__ __forceinline__ void win_tiny(WinHist* h, const uint32_t (&w)[kWords], uint32_t mn2,
+                                         float c) {
   const bool tiny = min(mn2 & 0xFFFFu, mn2 >> 16) <= kWinMagLo;
   if (__any_sync(0xFFFFFFFFu, tiny) && tiny) {
-    const float flo = __uint_as_float(f2 << 16);  // the floor the counts used
 #pragma unroll
     for (int t = 0; t < 2 * kWords; ++t) {
       const uint32_t b = (t & 1) ? (w[t >> 1] >> 16) : (w[t >> 1] & 0xFFFFu);
       const float l = __uint_as_float(b << 16);
-      if ((b & 0x7FFFu) <= kWinMagLo && l >= flo)
-        atomicAdd(&h->tiny_w[(b >> 15) ? 0 : 1], ex2(l * c));
+      if ((b & 0x7FFFu) <= kWinMagLo) atomicAdd(&h->tiny_w[(b >> 15) ? 0 : 1], ex2(l * c));
     }
   }
 }
@@ -215,6 +160,7 @@ __device__ __forceinline__ T consumer_reduce(T v, T* scratch, int tid, Op op) {
 struct HistResult {
   float theta;  // keep iff logit >= theta
   float z;      // sum over kept of 2^(l c - m c)
+  float zall;   // sum over the whole row (NaN: a NaN in the row)
   int pending;  // 1: leave the row to the exact slow path
 };
 
@@ -250,19 +196,18 @@ __device__ __forceinline__ void win_take(WinHist* h, WinHist* g, int tid, int nt
   }
 }
 
-// Row-end processing of the window histogram by the kWarps consumer warps
-// (all call it): m the row max, c = log2(e) / T, zfull the sum of
-// 2^(l c - m c) over the whole row, lo = m - D the window floor. Thread t
-// owns a run of consecutive items (each side's kWinSide items over half the
-// threads, the two ends of each side one extra), and higher threads hold
-// larger values. Each thread reads its items' counts once, clears them, and
-// works from registers; items not wholly inside the window (values below
-// lo, not all counted) read as empty, so a threshold never lands on them. A
-// counted huge value leaves the row to the slow path. Clears the histogram
-// (the caller's next barrier orders the clearing before later counts).
+// Row-end processing of the histogram by the kWarps consumer warps (all
+// call it): m the row max, c = log2(e) / T. Thread t owns a run of
+// consecutive items (each side's kWinSide items over half the threads, the
+// two ends of each side one extra), and higher threads hold larger values.
+// Each thread reads its items' counts once, clears them, and works from
+// registers: the masses, their sum Z, the top-k item, Z_k, the top-p item and
+// Z over the kept set. A huge value that can matter leaves the row to the
+// slow path. Clears the histogram (the caller's next barrier orders the
+// clearing before later counts).
 template <int kWarps>
-__device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, float lo, int tk,
-                                 float tp, int V, int tid, float* fscr, int* iscr) {
+__device__ HistResult win_finish(WinHist* h, float m, float c, int tk, float tp, int V, int tid,
+                                 float* fscr, int* iscr) {
   constexpr int kThreads = kWarps * 32;
   constexpr int kHalfT = kThreads / 2;
   constexpr int kPer = (kWinSide - 2) / kHalfT;
@@ -294,11 +239,12 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, floa
       float w;
       bool whole;
       if (i == kWinHugeNeg || i == kWinHugePos) {
-        // Counted values of magnitude 2^8 and above: +inf, NaN or a huge
-        // positive value (then the row's max), or huge negatives and -inf,
-        // which lie below a window floor above -2^8 and matter only to a
-        // window reaching it.
-        huge |= (n != 0u) && (i == kWinHugePos || !(lo > -256.f));
+        // Values of magnitude 2^8 and above: +inf, NaN or a huge positive
+        // value (then the row's max) send the row to the exact path; huge
+        // negatives and -inf weigh less than 2^-50 of the max each once
+        // (m + 2^8) c >= 50 (out of Z, which then moves by < 2^-32), and
+        // need the exact path below that.
+        huge |= (n != 0u) && (i == kWinHugePos || !((m + 256.f) * c >= 50.f));
         w = 0.f;
         whole = false;
       } else if (i == kWinTinyNeg || i == kWinTinyPos) {
@@ -306,11 +252,11 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, floa
         const int sd = (i == kWinTinyNeg) ? 0 : 1;
         w = h->tiny_w[sd] * emc;  // each side's sum has one reader, its owner
         h->tiny_w[sd] = 0.f;
-        whole = (i == kWinTinyNeg) ? (lo <= kWinTinyNegLow) : (lo <= 0.f);
+        whole = true;
       } else {
         const float v = win_value(i);
         w = n ? (float)n * ex2(fmaf(v, c, -mc)) : 0.f;
-        whole = v >= lo;
+        whole = true;
       }
       if (whole) {
         cn[k] = n;
@@ -324,6 +270,12 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, floa
   if (tid == 0) s_huge[0] = huge ? 1 : 0;
   if (tid == kThreads - 1) s_huge[1] = huge ? 1 : 0;
   auto merged = [](int i) { return i == kWinTinyNeg || i == kWinTinyPos; };
+  // Z over the whole row from the counts (every value was counted).
+  float my_all = 0.f;
+#pragma unroll
+  for (int k = 0; k < kMax; ++k) my_all += ms[k];
+  const float zfull =
+      consumer_reduce<float, kWarps>(my_all, fscr, tid, [](float a, float b) { return a + b; });
   int pending = (zfull == zfull && m < INFINITY) ? 0 : 1;  // NaN or +inf in the row
 
   // top-k: the item holding the k-th largest value (counts from the top).
@@ -407,6 +359,7 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, float zfull, floa
   res.pending = (pending || any_huge) ? 1 : 0;
   res.theta = (!res.pending && ikeep >= 0) ? win_value(ikeep) : -INFINITY;
   res.z = z;
+  res.zall = zfull;
   return res;
 }
 

@@ -46,7 +46,6 @@ struct StageMeta {
   int last;  // 1 on the row's last stage
   int tk;    // top-k of the row's request (filtered rows)
   float tp;  // top-p of the row's request (filtered rows)
-  float delta;  // window half-width of the row's histogram (filtered rows)
   int r;        // request of the row
   int pos;      // position of the row within its request (0 .. gamma)
   int gamma;    // draft tokens of the request
@@ -242,7 +241,6 @@ k_rows_tma(Params P, long long R) {
         const int part = (int)(item & 7);
         const RowInfo cur = warp_row_info(P, row, true);
         const char* src = (const char*)P.logits + row * row_bytes;
-        const float delta = FILT ? win_delta(cur.c, cur.tk, cur.tp, P.Vg) : 0.f;
         const long long off0 = (long long)part * P.part_bytes;
         const long long off1 = min(off0 + P.part_bytes, row_bytes);
         const int nch = (int)((off1 - off0 + kTmaStageBytes - 1) / kTmaStageBytes);
@@ -267,7 +265,6 @@ k_rows_tma(Params P, long long R) {
             M.last = (ch == nch - 1) ? 1 : 0;
             M.tk = cur.tk;
             M.tp = cur.tp;
-            M.delta = delta;
             M.r = cur.r;
             M.pos = cur.pos;
             M.gamma = cur.gamma;
@@ -300,7 +297,6 @@ k_rows_tma(Params P, long long R) {
         long long nrow = row + gridDim.x;
         bool next_done = false;
         const char* src = (const char*)P.logits + row * row_bytes;
-        const float delta = FILT ? win_delta(cur.c, cur.tk, cur.tp, P.Vg) : 0.f;
         // the draft token as a local column (-1: another rank's)
         const int xl = SHARD ? ((cur.x >= P.v0 && cur.x - P.v0 < P.V) ? cur.x - P.v0 : -1)
                              : cur.x;
@@ -325,7 +321,6 @@ k_rows_tma(Params P, long long R) {
             M.last = (ch == nchunks - 1) ? 1 : 0;
             M.tk = cur.tk;
             M.tp = cur.tp;
-            M.delta = delta;
             mbar_arrive_expect_tx(&full[stage], bytes);
             bulk_load(ring + (size_t)stage * kTmaStageBytes, src + off, bytes, &full[stage]);
           }
@@ -408,8 +403,9 @@ k_rows_tma(Params P, long long R) {
     if (M.row < 0) break;
     const uint4* buf = reinterpret_cast<const uint4*>(ring + (size_t)stage * kTmaStageBytes);
     const int nvec = M.n / epc;
-    // The row sum Z runs on softmax rows and (for top-p) on filtered rows.
-    const bool soft = (M.cls == kSoftmax) || (FILT && M.cls == kFiltered);
+    // The row sum Z runs on softmax rows (top-k / top-p rows take theirs
+    // from the window histogram, which counts every element).
+    const bool soft = (M.cls == kSoftmax);
     // This thread's vectors of the stage, in increasing element order; the
     // missing ones read as -inf (no max, no mass).
     constexpr uint32_t pad = BF16 ? 0xFF80FF80u : 0xFF800000u;
@@ -507,14 +503,11 @@ k_rows_tma(Params P, long long R) {
       s = __fadd_rn(s, __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3)));
     }
     if (FILT && M.cls == kFiltered) {
-      // Count every element of a full stage; in the row's last (padded)
-      // stage only those at or above this thread's window floor (its
-      // running max minus D; -inf and the padding never count there).
-      const bool full_stage = (nvec == kTmaVecPerThread * kTmaConsumers);
-      const uint32_t flo2 =
-          full_stage ? kWinFloorAll2 : win_floor2(fmaxf(vmax - M.delta, -3.402823466e38f));
+      // Count every element into the window histogram. The padding of a
+      // row's (or part's) last stage is -inf and lands in the negative huge
+      // counter; thread 0 takes it out again.
       uint32_t words[4 * kTmaVecPerThread];
-      uint32_t mn2 = 0xFFFFFFFFu;
+      uint32_t mn2 = 0xFFFFFFFFu, mx2 = 0u;
 #pragma unroll
       for (int k = 0; k < kTmaVecPerThread; ++k) {
         const uint32_t w[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
@@ -522,10 +515,13 @@ k_rows_tma(Params P, long long R) {
         words[4 * k + 1] = v[k].y;
         words[4 * k + 2] = v[k].z;
         words[4 * k + 3] = v[k].w;
-        if (full_stage) win_count_all(hist, w, mn2);
-        else win_count(hist, w, flo2, mn2);
+        win_count_all(hist, w, mn2, mx2);
       }
-      win_tiny(hist, words, flo2, mn2, M.c);
+      win_tiny(hist, words, mn2, M.c);
+      win_nan(hist, mx2);
+      if (tid == 0 && nvec < kTmaVecPerThread * kTmaConsumers)
+        atomicSub(&hist->cnt[win_slot_of_item(kWinHugeNeg)],
+                  win_pad(M.n, kTmaVecPerThread * kTmaConsumers * epc));
     }
     {
       // The draft token's logit, captured by the thread that holds it.
@@ -690,18 +686,8 @@ k_rows_tma(Params P, long long R) {
         }
       }
       if (FILT && M.cls == kFiltered) {
-        const float mc = __fmul_rn(m, M.c);
-        float part = 0.f;
-        if (vmax > -INFINITY && m > -INFINITY) part = __fmul_rn(s, ex2(__fsub_rn(vmc, mc)));
-        if (!(EARLY && P.parts > 1)) part = warp_sum(part);
-        float zfull = zmerged;
-        if (!(EARLY && P.parts > 1)) {
-          if (lane == 0) red_s[warp] = part;
-          named_sync(1, kTmaConsumers);
-          for (int w = 0; w < kTmaConsumerWarps; ++w) zfull += red_s[w];
-        }
-        const HistResult hr = win_finish<kTmaConsumerWarps>(hist, m, M.c, zfull, m - M.delta,
-                                                            M.tk, M.tp, P.V, tid, fscr, iscr);
+        const HistResult hr =
+            win_finish<kTmaConsumerWarps>(hist, m, M.c, M.tk, M.tp, P.V, tid, fscr, iscr);
         const bool unsettled = hr.pending || !(m > -INFINITY);
         if (unsettled && EARLY) {
           // The judgement needs this row now: settle it exactly here.

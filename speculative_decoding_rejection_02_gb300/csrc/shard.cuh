@@ -91,11 +91,11 @@ k_shard_finish(Params P) {
   __syncthreads();
   const int tk = P.top_k ? __ldg(P.top_k + r) : 0;
   const float tp = P.top_p ? __ldg(P.top_p + r) : 1.f;
-  const float lo = m - win_delta(c, tk, tp, P.Vg);
-  const HistResult hr = win_finish<kShardFinishThreads / 32>(h, m, c, z, lo, tk, tp, P.Vg, tid,
-                                                             fscr, iscr);
+  const HistResult hr =
+      win_finish<kShardFinishThreads / 32>(h, m, c, tk, tp, P.Vg, tid, fscr, iscr);
   if (tid != 0) return;
-  if (hr.pending && m > -INFINITY && z == z && m < INFINITY) {
+  // (Z of a top-k / top-p row comes from its histogram: NaN if the row held one)
+  if (hr.pending && m > -INFINITY && hr.zall == hr.zall && m < INFINITY) {
     // The window cannot settle this row and no rank holds it whole.
     RowStats s;
     s.m = m;
@@ -111,7 +111,7 @@ k_shard_finish(Params P) {
     return;
   }
   // NaN or +inf anywhere in the row: a NaN Z makes finish_row_x report it.
-  const float zk = (z == z && m < INFINITY) ? hr.z : __int_as_float(0x7FC00000);
+  const float zk = (hr.zall == hr.zall && m < INFINITY) ? hr.z : __int_as_float(0x7FC00000);
   finish_row_x(P, row, cls, m, argmax, zk, hr.theta, c, x, lx);
 }
 
