@@ -144,6 +144,31 @@ __device__ __forceinline__ T suffix_exclusive(T v, T* scratch, int tid) {
   return above;
 }
 
+// suffix_exclusive, and the sum of v over all the consumer threads.
+template <typename T, int kWarps>
+__device__ __forceinline__ T suffix_exclusive_total(T v, T* scratch, int tid, T& total) {
+  const int lane = tid & 31, warp = tid >> 5;
+  T x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const T y = __shfl_down_sync(0xFFFFFFFFu, x, o);
+    if (lane + o < 32) x += y;
+  }
+  const T excl = x - v;
+  if (lane == 0) scratch[warp] = x;
+  named_sync(1, kWarps * 32);
+  T above = excl, all = T(0);
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const T sw = scratch[w];
+    all += sw;
+    if (w > warp) above += sw;
+  }
+  named_sync(1, kWarps * 32);
+  total = all;
+  return above;
+}
+
 template <typename T, int kWarps, typename Op>
 __device__ __forceinline__ T consumer_reduce(T v, T* scratch, int tid, Op op) {
   const int lane = tid & 31, warp = tid >> 5;
@@ -214,6 +239,7 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, int tk, float tp,
   constexpr int kMax = kPer + 1;  // items of a side's first and last thread
   static_assert(kPer * kHalfT + 2 == kWinSide, "each side splits evenly over half the threads");
   __shared__ int s_item;
+  __shared__ float s_z;
   __shared__ int s_huge[2];  // written every row by the huge items' owners
   const int side = tid < kHalfT ? 0 : 1;
   const int u = tid - side * kHalfT;
@@ -270,17 +296,17 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, int tk, float tp,
   if (tid == 0) s_huge[0] = huge ? 1 : 0;
   if (tid == kThreads - 1) s_huge[1] = huge ? 1 : 0;
   auto merged = [](int i) { return i == kWinTinyNeg || i == kWinTinyPos; };
-  // Z over the whole row from the counts (every value was counted).
-  float my_all = 0.f;
-#pragma unroll
-  for (int k = 0; k < kMax; ++k) my_all += ms[k];
-  const float zfull =
-      consumer_reduce<float, kWarps>(my_all, fscr, tid, [](float a, float b) { return a + b; });
-  int pending = (zfull == zfull && m < INFINITY) ? 0 : 1;  // NaN or +inf in the row
+  int pending = (m < INFINITY) ? 0 : 1;  // +inf in the row (NaN: through Z below)
 
   // top-k: the item holding the k-th largest value (counts from the top).
   int ik = -1;  // lowest item kept by top-k (-1: all)
+  float zfull = 0.f, zk = 0.f;
   if (topk_on) {
+    // Z over the whole row from the counts (every value was counted).
+    float my_all = 0.f;
+#pragma unroll
+    for (int k = 0; k < kMax; ++k) my_all += ms[k];
+    zfull = consumer_reduce<float, kWarps>(my_all, fscr, tid, [](float a, float b) { return a + b; });
     if (tid == 0) s_item = -1;
     const unsigned above = suffix_exclusive<unsigned, kWarps>(my_cnt, (unsigned*)iscr, tid);
     if (above < (unsigned)tk && above + my_cnt >= (unsigned)tk) {
@@ -297,54 +323,60 @@ __device__ HistResult win_finish(WinHist* h, float m, float c, int tk, float tp,
     }
     named_sync(1, kThreads);
     ik = s_item;
-    if (ik < 0 || merged(ik)) pending = 1;  // outside the window, or on a merged item
+    if (ik < 0 || merged(ik)) pending = 1;  // beyond the counted values, or on a merged item
   }
 
-  // Mass of this thread's items in the top-k set.
+  // Mass of this thread's items in the top-k set (all items without top-k).
   float my_mass = 0.f;
 #pragma unroll
   for (int k = 0; k < kMax; ++k)
     if (i0 + k >= ik) my_mass += ms[k];
-  float zk = zfull;
   if (topk_on)
     zk = consumer_reduce<float, kWarps>(my_mass, fscr, tid, [](float a, float b) { return a + b; });
 
   // top-p: keep value v iff the mass strictly above it (in the top-k set) is
   // < top_p Z_k: the kept values run from the top down to item ip, the
-  // lowest nonempty item whose mass above is below the bar.
+  // lowest nonempty item whose mass above is below the bar. One suffix scan
+  // gives each thread the mass above its items and (without top-k) Z_k;
+  // the thread owning ip reads Z over the kept set off its own scan.
   int ikeep = ik;
   float z = zk;
   if (topp_on) {
+    if (tid == 0) s_item = 0x7FFFFFFF;  // (ordered before the atomicMin by the scan's barrier)
+    float total;
+    const float above = suffix_exclusive_total<float, kWarps>(my_mass, fscr, tid, total);
+    if (!topk_on) zfull = zk = total;
     const float thr = tp * zk;
-    const float above = suffix_exclusive<float, kWarps>(my_mass, fscr, tid);
     int cand = 0x7FFFFFFF;
+    float zc = 0.f;  // the kept mass if cand is the boundary
     float run = above;
 #pragma unroll
     for (int k = kMax - 1; k >= 0; --k) {
       const int i = i0 + k;
       if (k < ni && i >= ik) {
-        if (cn[k] && run < thr) cand = i;
-        run += ms[k];
+        const float next = run + ms[k];
+        if (cn[k] && run < thr) {
+          cand = i;
+          zc = next;
+        }
+        run = next;
       }
     }
-    if (tid == 0) s_item = 0x7FFFFFFF;
-    named_sync(1, kThreads);
     if (cand != 0x7FFFFFFF) atomicMin(&s_item, cand);
     named_sync(1, kThreads);
     const int ip = s_item;
+    if (cand == ip && ip != 0x7FFFFFFF) s_z = zc;  // one owner
+    named_sync(1, kThreads);
     if (ip == 0x7FFFFFFF || merged(ip)) pending = 1;
     ikeep = ip;
-    float zpart = 0.f;
-#pragma unroll
-    for (int k = 0; k < kMax; ++k)
-      if (i0 + k >= ip) zpart += ms[k];
-    z = consumer_reduce<float, kWarps>(zpart, fscr, tid, [](float a, float b) { return a + b; });
+    z = (ip == 0x7FFFFFFF) ? zk : s_z;
     // The next value below ip has the kept mass z above it; it is dropped
-    // (wherever it lies, inside the window or not) iff z >= thr. Unless
-    // top-k ends the set at ip, a kept mass below the bar means the kept set
-    // might continue below the window.
+    // iff z >= thr. Unless top-k ends the set at ip, a kept mass below the
+    // bar means the set would continue into values that were not counted
+    // one by one.
     if (!pending && !(topk_on && ip == ik) && !(z >= thr)) pending = 1;
   }
+  if (!(zfull == zfull)) pending = 1;  // NaN in the row
 
   if (!topk_on && !topp_on) named_sync(1, kThreads);  // (filtered rows have one of them)
   const int any_huge = s_huge[0] | s_huge[1];
