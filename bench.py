@@ -66,6 +66,8 @@ def parse():
                          "target's sampler draws every position; drafts must equal it)")
     ap.add_argument("--early-exit", action="store_true",
                     help="stop reading a request's rows at its first rejection")
+    ap.add_argument("--resident", action="store_true",
+                    help="with --early-exit: hold each judged row in a thread-block cluster")
     ap.add_argument("--B", type=int, default=None,
                     help="resize the workload to B requests (profiling of small cases)")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -255,14 +257,17 @@ def per_config_timings(sv, dev, stream, peak, main_batch, steps=30, warmup=5):
     batch with early exit. Device-timed like the headline (inputs resident)."""
     import torch
     out = {}
-    cases = [("c2", None, 0), ("c3", None, 0), ("c4", None, 0)]
+    cases = [("c2", None, 0, 0), ("c3", None, 0, 0), ("c4", None, 0, 0)]
     if main_batch is not None:
-        cases.append((main_batch["name"] + " early-exit", main_batch, sv.FLAG_EARLY_EXIT))
-    for label, batch, flags in cases:
+        cases.append((main_batch["name"] + " early-exit", main_batch, sv.FLAG_EARLY_EXIT, 0))
+        cases.append((main_batch["name"] + " early-exit resident", main_batch, sv.FLAG_EARLY_EXIT,
+                      sv.CONFIG_EARLY_RESIDENT))
+    for label, batch, flags, cfg_flags in cases:
         b = dict(batch) if batch is not None else synth.make(label)
         b["flags"] = flags
         R = b["target_logits"].shape[0]
-        ver = sv.Verifier(max_batch=b["B"], max_rows=R, max_vocab=b["V"], device=dev.index)
+        ver = sv.Verifier(max_batch=b["B"], max_rows=R, max_vocab=b["V"], device=dev.index,
+                          config_flags=cfg_flags)
         db = sv.upload(b, dev, with_p=False)
         flush = flush_buffer(b, dev)
         for _ in range(warmup):
@@ -444,7 +449,8 @@ def main():
     R = N + B
     positions = N
 
-    ver = sv.Verifier(max_batch=B, max_rows=R, max_vocab=V, device=local)
+    ver = sv.Verifier(max_batch=B, max_rows=R, max_vocab=V, device=local,
+                      config_flags=sv.CONFIG_EARLY_RESIDENT if args.resident else 0)
     db = sv.upload(batch, dev, with_p=False)
     stream = torch.cuda.current_stream(dev)
     in_bytes = sum(v for v in synth.batch_bytes(batch).values())
@@ -559,6 +565,8 @@ def main():
         launches_per_step += 1  # k_match
     if args.early_exit:
         launches_per_step = 3  # queue init, row pass, race
+        if args.resident and not filters:
+            launches_per_step = 1  # the cluster kernel
     if rank == 0:
         line = {
             "metric": METRIC,
@@ -572,6 +580,7 @@ def main():
                               else "L2 flushed between timed calls (512 MB write)"),
                        "acceptance": args.accept,
                        "early_exit": bool(args.early_exit),
+                       "resident_rows": bool(args.early_exit and args.resident),
                        "parallelism": f"replicas x{world}"},
             "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak,
             "hbm_frac_nominal": fr["call_frac_nominal"],

@@ -100,12 +100,21 @@ extern "C" {
  * token and count is the one the full pass gives; the differences are that
  * an unusable row (NaN, +inf, all -inf) or an invalid draft token after the
  * stop does not void the request or set a status bit, and p_at_draft is NaN
- * at the positions after the stop. When the batch has enough requests to
- * keep every SM busy (B at least twice the row pass's resident CTAs) and its
- * rows are 16-byte aligned (bf16 if top_k / top_p are given), the rows are
- * read position by position and the rows after the stop are never read;
- * otherwise every row is read (faster for small batches) with the same
- * results. Cannot be combined with SPEC_FLAG_SAMPLER_MATCH. */
+ * at the positions after the stop. Schedules, all with the same results:
+ *  - when the batch has enough requests to keep every SM busy (B at least
+ *    twice the row pass's resident CTAs) and its rows are 16-byte aligned
+ *    (bf16 if top_k / top_p are given), the rows are read position by
+ *    position from a work queue and the rows after the stop are never read;
+ *    the token at the stop is drawn afterwards, reading that row again;
+ *  - otherwise every row is read (faster for small batches);
+ *  - on handles created with SPEC_CONFIG_EARLY_RESIDENT, batches without
+ *    top_k / top_p whose rows are 16-byte aligned and at most 8 x 64 KB,
+ *    with draft_probs (if given) in device memory and 16-byte aligned, are
+ *    verified one request per thread-block cluster that holds the judged
+ *    row in its shared memory: the rows up to the stop are read once each
+ *    and the token at the stop is drawn from the row held (the fewest HBM
+ *    bytes; slower than the work queue on a GPU the call has to itself).
+ * Cannot be combined with SPEC_FLAG_SAMPLER_MATCH. */
 #define SPEC_FLAG_EARLY_EXIT 0x4u
 
 typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
@@ -121,9 +130,17 @@ typedef struct {
 } spec_verify_config;
 
 /* Handle flags (spec_verify_config.flags). */
-#define SPEC_CONFIG_EARLY_QUEUE 0x2u       /* test only: early-exit calls read their rows
-                                              position by position whenever the rows
-                                              allow it, whatever the batch size */
+#define SPEC_CONFIG_EARLY_QUEUE 0x2u       /* test only: early-exit calls take the work
+                                              queue whenever the rows allow it, whatever
+                                              the batch size */
+#define SPEC_CONFIG_EARLY_FULL_PASS 0x4u   /* test only: early-exit calls read every row
+                                              and apply the early-exit semantics in the
+                                              accept scan, whatever the batch */
+#define SPEC_CONFIG_EARLY_RESIDENT 0x8u    /* early-exit calls whose batch allows it
+                                              keep each judged row resident in a
+                                              thread-block cluster (see
+                                              SPEC_FLAG_EARLY_EXIT); not with the two
+                                              flags above */
 #define SPEC_CONFIG_TEST_WAIT_TIMEOUT 0x1u /* test only (no counterpart on the pages):
                                               early-exit calls leave their work queue
                                               empty and its waits give up after a few

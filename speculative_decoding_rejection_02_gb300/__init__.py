@@ -37,6 +37,8 @@ FLAG_EARLY_EXIT = 0x4
 
 CONFIG_TEST_WAIT_TIMEOUT = 0x1  # test only: early-exit queue waits run out
 CONFIG_EARLY_QUEUE = 0x2        # test only: early exit always takes the work queue
+CONFIG_EARLY_FULL_PASS = 0x4    # test only: early exit always reads every row
+CONFIG_EARLY_RESIDENT = 0x8     # early exit keeps each judged row in a cluster's shared memory
 
 # The entry points declared in include/spec_verify.h.
 ENTRY_POINTS = (

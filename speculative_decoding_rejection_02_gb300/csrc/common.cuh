@@ -131,6 +131,7 @@ struct Params {
   int slices_per_row;
   int race_slices;
   int race_slice_n;          // entries per race task (a power of two, at most race_slice())
+  int res_part;              // early exit in clusters: elements of a row per CTA
   // Vocab-sharded calls: the local columns are global v0 .. v0 + V - 1.
   int v0;                    // 0 otherwise
   int Vg;                    // the full vocabulary (V otherwise)

@@ -13,6 +13,7 @@
 #include "common.cuh"
 #include "philox.cuh"
 #include "race.cuh"
+#include "resident.cuh"
 #include "rows.cuh"
 #include "rows_tma.cuh"
 #include "shard.cuh"
@@ -43,6 +44,7 @@ struct spec_verify_handle {
   int n_phase;
   int tma_blocks;   // resident CTAs of k_rows_tma<.., false> on the device
   int filt_blocks;  // resident CTAs of k_rows_tma<true, true>
+  int res_clusters[4];  // co-resident clusters of k_resident with 1, 2, 4, 8 CTAs
 };
 
 namespace {
@@ -64,6 +66,57 @@ bool set_row_pass_smem() {
          cudaFuncSetAttribute(sv::k_rows_tma<false, false, false, true>, a, plain) ==
              cudaSuccess &&
          cudaFuncSetAttribute(sv::k_rows_tma<true, true, false, true>, a, filt) == cudaSuccess;
+}
+
+// Early exit in clusters: the shared memory of k_resident and how many
+// clusters of 1, 2, 4 and 8 CTAs fit on the device at once (0: none).
+void resident_setup(int out[4]) {
+  for (int i = 0; i < 4; ++i) out[i] = 0;
+  const int smem = (int)sv::kResSmemBytes;
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  if (cudaFuncSetAttribute(sv::k_resident<true>, a, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(sv::k_resident<false>, a, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  for (int i = 0; i < 4; ++i) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(1u << i);
+    cfg.blockDim = dim3(sv::kResThreads);
+    cfg.dynamicSmemBytes = sv::kResSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1u << i;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, sv::k_resident<true>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    out[i] = n;
+  }
+}
+
+// Cluster size (1, 2, 4 or 8; 0: the batch cannot take the resident path)
+// for rows of V elements of esize bytes: the fewest CTAs whose parts fit,
+// doubled while the batch's requests all still run at once, so that small
+// batches spread each row over more SMs.
+int resident_cluster(const spec_verify_handle* h, int V, int esize, int B, int& part) {
+  int i = 0;
+  for (; i < 4; ++i) {
+    const int C = 1 << i;
+    const long long S = (((long long)V + C - 1) / C + 7) / 8 * 8;
+    if (S * esize <= sv::kResPartBytes && h->res_clusters[i] > 0) break;
+  }
+  if (i == 4) return 0;
+  while (i < 3 && h->res_clusters[i + 1] > 0 && (long long)B <= h->res_clusters[i + 1]) ++i;
+  const int C = 1 << i;
+  part = (int)((((long long)V + C - 1) / C + 7) / 8 * 8);
+  return C;
 }
 
 // Control words of the early-exit queue, and its slots beyond one per row
@@ -231,13 +284,58 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   P.fast_filtered = (rows_aligned && h->tma_blocks > 0 && h->filt_blocks > 0 && P.bf16 &&
                      filters) ? 1 : 0;
   if (P.early) {
+    // Handles created with SPEC_CONFIG_EARLY_RESIDENT, rows without top-k /
+    // top-p: each request in a cluster that keeps the judged row in shared
+    // memory (rows 16-byte aligned and at most 8 parts of 64 KB, draft
+    // probabilities in device memory and 16-byte aligned).
+    int part = 0;
+    const int C = ((h->cfg.flags & SPEC_CONFIG_EARLY_RESIDENT) && !filters && rows_aligned &&
+                   !P.q_host && !P.test_stall &&
+                   (!P.q || (reinterpret_cast<uintptr_t>(P.q) & 15) == 0))
+                      ? resident_cluster(h, b->V, esize, b->B, part)
+                      : 0;
+    if (C > 0) {
+      P.res_part = part;
+      const int fit = h->res_clusters[C == 1 ? 0 : C == 2 ? 1 : C == 4 ? 2 : 3];
+      const int ncl = b->B < fit ? b->B : fit;
+      if (cudaMemsetAsync(h->queue_ctl, 0, kQueueCtl * sizeof(unsigned), stream) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+      cudaLaunchConfig_t cfg;
+      std::memset(&cfg, 0, sizeof cfg);
+      cfg.gridDim = dim3((unsigned)(ncl * C));
+      cfg.blockDim = dim3(sv::kResThreads);
+      cfg.dynamicSmemBytes = sv::kResSmemBytes;
+      cfg.stream = stream;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = (unsigned)C;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      const cudaError_t e = P.bf16 ? cudaLaunchKernelEx(&cfg, sv::k_resident<true>, P)
+                                   : cudaLaunchKernelEx(&cfg, sv::k_resident<false>, P);
+      if (timed) {
+        // one kernel: its time is the rows phase
+        cudaEventRecord(h->phase[1], stream);
+        cudaEventRecord(h->phase[2], stream);
+        cudaEventRecord(h->phase[3], stream);
+      }
+      if (e != cudaSuccess || cudaPeekAtLastError() != cudaSuccess) {
+        cudaGetLastError();
+        return SPEC_ERR_CUDA;
+      }
+      return SPEC_OK;
+    }
     // The work queue pays off when the batch's requests can keep every SM
     // busy; otherwise (and for rows the bulk copies cannot take) the full
     // pass runs and the accept scan applies the same early-exit semantics.
     const int qblocks = P.fast_filtered ? h->filt_blocks : h->tma_blocks;
     const bool queue_ok = rows_aligned && h->tma_blocks > 0 && (!filters || P.fast_filtered);
     const bool big = (long long)b->B >= 2ll * qblocks;
-    if (!queue_ok || !(big || (h->cfg.flags & SPEC_CONFIG_EARLY_QUEUE))) P.early = 0;
+    if (!queue_ok || !(big || (h->cfg.flags & SPEC_CONFIG_EARLY_QUEUE)) ||
+        (h->cfg.flags & SPEC_CONFIG_EARLY_FULL_PASS))
+      P.early = 0;
   }
   // Early exit: split each row into parts of about the target size (whole
   // stages) when the workspace has room for it. The queue takes every row
@@ -351,7 +449,11 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   if (!cfg || cfg->max_batch < 1 || cfg->max_rows < 1 || cfg->max_vocab < 1)
     return SPEC_ERR_INVALID_ARG;
   if (cfg->max_rows < cfg->max_batch) return SPEC_ERR_INVALID_ARG;
-  if (cfg->flags & ~(SPEC_CONFIG_TEST_WAIT_TIMEOUT | SPEC_CONFIG_EARLY_QUEUE))
+  if (cfg->flags & ~(SPEC_CONFIG_TEST_WAIT_TIMEOUT | SPEC_CONFIG_EARLY_QUEUE |
+                     SPEC_CONFIG_EARLY_FULL_PASS | SPEC_CONFIG_EARLY_RESIDENT))
+    return SPEC_ERR_INVALID_ARG;
+  if ((cfg->flags & SPEC_CONFIG_EARLY_RESIDENT) &&
+      (cfg->flags & (SPEC_CONFIG_EARLY_QUEUE | SPEC_CONFIG_EARLY_FULL_PASS)))
     return SPEC_ERR_INVALID_ARG;
   if (cudaSetDevice(cfg->device) != cudaSuccess) return SPEC_ERR_CUDA;
   cudaDeviceProp prop;
@@ -379,6 +481,7 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   }
   h->tma_blocks = per_sm * prop.multiProcessorCount;
   h->filt_blocks = filt_per_sm * prop.multiProcessorCount;
+  resident_setup(h->res_clusters);
   if (cudaFuncSetAttribute(sv::k_race, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)sv::kRaceSmemMax) != cudaSuccess) {
     delete h;
@@ -670,6 +773,7 @@ struct NoallocDevice {
   int sm_count;
   int tma_blocks;
   int filt_blocks;
+  int res_clusters[4];
 };
 NoallocDevice g_na_dev[kNaMaxDevices];
 std::mutex g_na_mutex;
@@ -722,6 +826,7 @@ extern "C" int spec_verify_run_noalloc(const spec_verify_batch* b, void* stream,
         cudaGetLastError();
         return SPEC_ERR_CUDA;
       }
+      resident_setup(slot.res_clusters);
       slot.base = (char*)ptr;
       slot.sm_count = prop.multiProcessorCount;
       slot.tma_blocks = per_sm * prop.multiProcessorCount;
@@ -756,6 +861,7 @@ extern "C" int spec_verify_run_noalloc(const spec_verify_batch* b, void* stream,
   h.n_phase = 0;
   h.tma_blocks = nd.tma_blocks;
   h.filt_blocks = nd.filt_blocks;
+  for (int i = 0; i < 4; ++i) h.res_clusters[i] = nd.res_clusters[i];
   // The slice counters must start at zero: clear them (the array keeps the
   // previous call's contents).
   cudaStream_t s = (cudaStream_t)stream;

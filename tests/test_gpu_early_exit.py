@@ -1,9 +1,12 @@
 """Early-exit verification on the GPU (velog "드래프트가 제안하고 타깃이
 판정한다": the first rejection ends the round), through the C ABI, against
-the oracle under the same flag and against the GPU's own full pass. Both
+the oracle under the same flag and against the GPU's own full pass. Four
 schedules are run: rows read position by position through the work queue
-(forced with a test-only handle flag) and the full pass with early-exit
-judgement (what the library picks for small batches)."""
+and the full pass with early-exit judgement (each forced with a test-only
+handle flag), the library's own choice between those two, and the cluster
+kernel that keeps each judged row in shared memory and draws the token at
+the stop from it (a handle flag; batches with top-k / top-p fall back to the
+library's choice)."""
 import numpy as np
 import pytest
 
@@ -13,13 +16,14 @@ from parity import assert_parity, check_structure, compare, full_batch, oracle_a
 
 pytestmark = pytest.mark.gpu
 
-SCHEDULES = ["queue", "full"]
+SCHEDULES = ["queue", "full", "auto", "resident"]
 
 
 def _run(b, schedule, greedy=False):
     import speculative_decoding_rejection_02_gb300 as sv
     R = b["target_logits"].shape[0]
-    flags = sv.CONFIG_EARLY_QUEUE if schedule == "queue" else 0
+    flags = {"queue": sv.CONFIG_EARLY_QUEUE, "full": sv.CONFIG_EARLY_FULL_PASS,
+             "auto": 0, "resident": sv.CONFIG_EARLY_RESIDENT}[schedule]
     ver = sv.Verifier(max_batch=max(b["B"], 1), max_rows=max(R, 1), max_vocab=b["V"],
                       config_flags=flags)
     try:
@@ -84,6 +88,7 @@ def test_same_round_as_the_full_pass(name, schedule):
 @pytest.mark.parametrize("name,schedule", [
     ("c3", "auto"), ("c4", "auto"), ("c5", "auto"),  # the library's own choice
     ("c3", "queue"), ("c4", "queue"),                # the work queue at full size
+    ("c5", "resident"),                              # rows held in clusters
 ])
 def test_full_size_every_request(name, schedule):
     b = _early(full_batch(name))
@@ -146,3 +151,46 @@ def test_edge_rounds(schedule):
     assert gpu["status"] & 0x1
     assert_parity(compare(b, gpu, ref))
     assert gpu["num_accepted"][5] == 0 and np.all(gpu["out_tokens"][cu[5] + 5:cu[6] + 6] == -1)
+
+
+def test_resident_bad_offsets_end_their_requests():
+    """Cluster schedule: a request whose offsets are out of order is ended
+    with SPEC_STATUS_BAD_OFFSETS and no rows read; the call still ends."""
+    b = _early(synth.make("c5", B=12, V=4096))
+    cu = b["cu_num_draft"].copy()
+    cu[5], cu[6] = cu[6], cu[5]
+    b["cu_num_draft"] = cu
+    gpu = _run(b, "resident")
+    assert gpu["status"] & 0x10
+    assert gpu["num_accepted"][5] == 0
+
+
+@pytest.mark.parametrize("case", ["host_q", "top_p", "misaligned"])
+def test_resident_handle_falls_back_where_the_batch_needs_it(case):
+    """A handle asking for the cluster schedule still verifies batches that
+    schedule cannot take (draft_probs in page-locked host memory, top-p
+    rows, rows that are not 16-byte aligned), with the same results as a
+    default handle."""
+    import torch
+
+    import speculative_decoding_rejection_02_gb300 as sv
+    if case == "top_p":
+        b = _early(synth.make("c4", B=24, V=50000))
+    elif case == "misaligned":
+        b = _early(synth.make("c2", B=6, V=32001))
+    else:
+        b = _early(synth.make("c5", B=20, V=20008))
+    R = b["target_logits"].shape[0]
+    outs = []
+    for flags in (0, sv.CONFIG_EARLY_RESIDENT):
+        ver = sv.Verifier(max_batch=b["B"], max_rows=R, max_vocab=b["V"], config_flags=flags)
+        db = sv.upload(b, "cuda:0")
+        if case == "host_q":
+            db.draft_probs = torch.from_numpy(b["draft_probs"]).pin_memory()
+        ver.run(db)
+        torch.cuda.synchronize()
+        assert ver.status() == 0
+        outs.append((db.out_tokens.cpu().numpy(), db.num_accepted.cpu().numpy()))
+        ver.close()
+    assert np.array_equal(outs[0][0], outs[1][0])
+    assert np.array_equal(outs[0][1], outs[1][1])
