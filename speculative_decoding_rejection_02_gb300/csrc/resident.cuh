@@ -110,26 +110,25 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr)
                : "memory");
 }
-__device__ __forceinline__ bool mbar_test_acq_cluster(uint64_t* bar, uint32_t parity) {
+// Exchange waits: probes that may suspend the thread for up to
+// kClusterHintNs (the phase is completed by other CTAs' arrivals), at most
+// kClusterTries of them: about a second in all.
+constexpr uint32_t kClusterHintNs = 2000;
+constexpr uint32_t kClusterTries = 1u << 19;
+__device__ __forceinline__ bool mbar_try_acq_cluster(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_addr(bar)), "r"(parity)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(kClusterHintNs)
       : "memory");
   return ok != 0;
 }
-// Exchange waits poll (non-blocking tests with a short sleep between them)
-// instead of suspending: the phase is completed by other CTAs' arrivals.
-// At most kClusterPolls polls of at least ~0.1 us each: under a second.
-constexpr uint32_t kClusterPolls = 1u << 22;
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kClusterPolls; ++i) {
-    if (mbar_test_acq_cluster(bar, parity)) return true;
-    __nanosleep(64);
-  }
+  for (uint32_t i = 0; i < kClusterTries; ++i)
+    if (mbar_try_acq_cluster(bar, parity)) return true;
   return false;
 }
 // All threads of every CTA of the cluster (used once at the start and once
