@@ -300,10 +300,15 @@ def measured_hbm_peak():
         return 6800.0, "fallback (an earlier GB300 copy measurement)"
 
 
+# The sources the target-row pass (the dominant kernel) is built from.
+ROW_PASS_SOURCES = ("common.cuh", "pipe.cuh", "rows.cuh", "hist.cuh", "rows_tma.cuh")
+
+
 def kernel_source_sha() -> str:
+    """Hash of the row pass's sources: the key of its committed ncu traffic."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "speculative_decoding_rejection_02_gb300", "csrc")
-    for fn in sorted(os.listdir(d)):
+    for fn in ROW_PASS_SOURCES:
         with open(os.path.join(d, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
