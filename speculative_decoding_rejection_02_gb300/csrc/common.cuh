@@ -116,6 +116,8 @@ struct Params {
   unsigned* status;
   long long* pending_rows;  // filtered rows left to the exact slow kernel
   unsigned* pending_count;  // entries in pending_rows (race_count + 1)
+  unsigned* row_ticket;     // full row pass: rows after the first wave by ticket
+                            // (race_count + 2; null: by stride)
   // Early exit (SPEC_FLAG_EARLY_EXIT): the row pass's work queue.
   int early;
   int test_stall;           // 1: leave the early-exit queue empty, short waits (tests)

@@ -283,18 +283,31 @@ k_rows_tma(Params P, long long R) {
         if (!ok) break;
       }
     } else {
+      // Rows blockIdx.x, then either blockIdx.x + gridDim.x, + 2 gridDim.x,
+      // ... or, with a ticket counter, gridDim.x + the tickets this CTA
+      // takes in turn (CTAs whose rows were cheap take more of them).
+      auto next_row = [&](long long r0) -> long long {
+        if (!P.row_ticket) return r0 + gridDim.x;
+        unsigned t = 0;
+        if (lane == 0) t = atomicAdd(P.row_ticket, 1u);
+        return (long long)gridDim.x + __shfl_sync(0xFFFFFFFFu, t, 0);
+      };
       long long row = blockIdx.x;
       RowInfo cur;
       cur.cls = -1;
       while (row < R) {  // first row with work
         cur = warp_row_info(P, row, FILT);  // FILT: every row
         if (cur.cls >= 0) break;
-        row += gridDim.x;
+        row = next_row(row);
       }
+      // The next row is looked up while this one streams: at its first
+      // stage by stride, at its last with tickets (so that a ticket goes to
+      // the CTA about to be free).
+      const int look_at = P.row_ticket ? nchunks - 1 : 0;
       while (row < R && ok) {
         RowInfo next;
         next.cls = -1;
-        long long nrow = row + gridDim.x;
+        long long nrow = R;
         bool next_done = false;
         const char* src = (const char*)P.logits + row * row_bytes;
         // the draft token as a local column (-1: another rank's)
@@ -330,12 +343,12 @@ k_rows_tma(Params P, long long R) {
             stage = 0;
             phase ^= 1u;
           }
-          if (ch == 0) {
-            // Look the next row up while this one streams.
+          if (ch == look_at) {
+            nrow = next_row(row);
             while (nrow < R) {
               next = warp_row_info(P, nrow, FILT);
               if (next.cls >= 0) break;
-              nrow += gridDim.x;
+              nrow = next_row(nrow);
             }
             next_done = true;
           }

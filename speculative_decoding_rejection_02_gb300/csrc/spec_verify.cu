@@ -29,7 +29,7 @@ struct spec_verify_handle {
   unsigned long long* race_best;
   unsigned* race_counter;
   sv::RaceTask* race_list;
-  unsigned* race_count;  // [2]: races listed, rows left to the slow kernel
+  unsigned* race_count;  // [3]: races listed, rows left to the slow kernel, row tickets
   long long* pending_rows;
   long long* queue;      // early exit: [q_cap] items
   unsigned* queue_ready;  // [q_cap]
@@ -275,7 +275,7 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
     return SPEC_ERR_CAPACITY;
   const bool timed = h->n_phase >= 4;
   if (timed) cudaEventRecord(h->phase[0], stream);
-  if (!greedy && cudaMemsetAsync(h->race_count, 0, 2 * sizeof(unsigned), stream) != cudaSuccess)
+  if (!greedy && cudaMemsetAsync(h->race_count, 0, 3 * sizeof(unsigned), stream) != cudaSuccess)
     return SPEC_ERR_CUDA;
   const int esize = P.bf16 ? 2 : 4;
   const bool rows_aligned = (((long long)b->V * esize) % 16 == 0) &&
@@ -394,13 +394,18 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
     }
     return SPEC_OK;
   }
+  // Rows after the row pass's first wave go by ticket when there are any
+  // (the counter was cleared with the race counters; greedy calls keep the
+  // stride order).
   if (P.fast_filtered) {
     // One pass over every row; the filtered rows it cannot settle are listed.
     const long long fgrid = R < h->filt_blocks ? R : h->filt_blocks;
+    if (!greedy && R > fgrid) P.row_ticket = h->race_count + 2;
     sv::k_rows_tma<true, true><<<(unsigned)fgrid, sv::kTmaThreads, sv::kTmaFiltSmemBytes,
                                  stream>>>(P, R);
   } else if (rows_aligned && h->tma_blocks > 0) {
     const long long grid = R < h->tma_blocks ? R : h->tma_blocks;
+    if (!greedy && R > grid) P.row_ticket = h->race_count + 2;
     if (P.bf16)
       sv::k_rows_tma<true, false><<<(unsigned)grid, sv::kTmaThreads, sv::kTmaSmemBytes, stream>>>(
           P, R);
@@ -498,7 +503,7 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   const size_t sz_best = align_up(n_rows * sizeof(unsigned long long));
   const size_t sz_rccnt = align_up(n_rows * sizeof(unsigned));
   const size_t sz_list = align_up(n_rows * sizeof(sv::RaceTask));
-  const size_t sz_lcnt = align_up(2 * sizeof(unsigned));
+  const size_t sz_lcnt = align_up(3 * sizeof(unsigned));
   const size_t sz_pend = align_up(n_rows * sizeof(long long));
   const size_t qcap = n_rows * sv::kMaxParts + kQueueSpare;
   const size_t sz_queue = align_up(qcap * sizeof(long long));
@@ -756,7 +761,7 @@ constexpr size_t kNaOffBest = kNaOffRace + na_align(kNaBatch * sizeof(sv::RaceDe
 constexpr size_t kNaOffRccnt = kNaOffBest + na_align(kNaRows * sizeof(unsigned long long));
 constexpr size_t kNaOffList = kNaOffRccnt + na_align(kNaRows * sizeof(unsigned));
 constexpr size_t kNaOffLcnt = kNaOffList + na_align(kNaRows * sizeof(sv::RaceTask));
-constexpr size_t kNaOffPend = kNaOffLcnt + na_align(2 * sizeof(unsigned));
+constexpr size_t kNaOffPend = kNaOffLcnt + na_align(3 * sizeof(unsigned));
 // Early exit without row parts: one queue slot per row, plus the spare.
 constexpr size_t kNaQueueCap = kNaRows + kQueueSpare;
 constexpr size_t kNaOffQueue = kNaOffPend + na_align(kNaRows * sizeof(long long));

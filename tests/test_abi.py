@@ -107,6 +107,17 @@ def test_null_handle_and_bad_config(L):
     assert L.spec_verify_init(C.byref(h), C.byref(bad)) == -1
 
 
+def test_config_flags_checked_before_the_device(L):
+    """Unknown handle flags, and the cluster schedule combined with a forced
+    early-exit schedule, are rejected before any device is touched."""
+    h = C.c_void_p()
+    for flags in (0x100, sv.CONFIG_EARLY_RESIDENT | sv.CONFIG_EARLY_QUEUE,
+                  sv.CONFIG_EARLY_RESIDENT | sv.CONFIG_EARLY_FULL_PASS):
+        cfg = sv.Config(device=0, max_batch=4, max_rows=16, max_vocab=64, flags=flags)
+        assert L.spec_verify_init(C.byref(h), C.byref(cfg)) == -1
+        assert not h.value
+
+
 def test_init_without_gpu_fails_cleanly(L):
     import torch
     if torch.cuda.is_available():
