@@ -401,3 +401,20 @@ def test_draft_probs_in_host_memory_under_early_exit():
     assert torch.equal(on_dev.num_accepted, on_host.num_accepted)
     assert torch.equal(on_dev.out_tokens, on_host.out_tokens)
     ver.close()
+
+
+@pytest.mark.parametrize("V", [32000, 32001])
+def test_fp32_rows_with_top_k_and_top_p(V):
+    """fp32 target rows with top-k and top-p have no window histogram: the
+    exact kernel settles them by radix selection over 32-bit keys (four
+    8-bit digits), aligned and misaligned rows, ties included."""
+    b = synth.make("c2", B=24, V=V)
+    rng = np.random.default_rng(V)
+    logits = b["target_logits"].copy()
+    logits[::3] = np.round(logits[::3] * 2) / 2  # rows of tied values
+    b["target_logits"] = logits
+    b["top_k"] = rng.choice([0, 1, 7, 50, 3000], size=b["B"]).astype(np.int32)
+    b["top_p"] = rng.choice([1.0, 0.3, 0.9, 0.99], size=b["B"]).astype(np.float32)
+    b["temperature"] = rng.choice([0.0, 0.5, 1.0, 2.0], size=b["B"]).astype(np.float32)
+    gpu, _ = check(b)
+    assert gpu["status"] & ~np.uint32(0x8) == 0
