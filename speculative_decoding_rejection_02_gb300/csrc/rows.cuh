@@ -10,8 +10,9 @@
 //    registers and warp shuffles. The last CTA of a row (atomic counter)
 //    merges the slice partials and evaluates p at the row's draft token.
 //  * k_rows_filtered — rows with top-k and/or top-p. One CTA per row finds
-//    the thresholds exactly by bisection over order-preserving keys (counts
-//    for top-k, probability mass for top-p), re-reading the row each step.
+//    the thresholds exactly by an 8-ary search over order-preserving keys
+//    (counts for top-k, probability mass for top-p; seven thresholds per
+//    pass), re-reading the row each pass.
 #pragma once
 #include "common.cuh"
 #include "pipe.cuh"
@@ -289,10 +290,50 @@ __device__ __forceinline__ float key_threshold(uint32_t k, int bf16) {
   return key_float(k);
 }
 
+// The searches below test kSearchProbes thresholds per pass (an 8-ary
+// search over the keys): a pass reads the row once and reduces
+// kSearchProbes sums, so a 32-bit key space takes at most 11 passes.
+constexpr int kSearchProbes = 7;
+
+// The thresholds of one pass over the open interval (lo, hi), hi - lo >= 2:
+// non-decreasing, each strictly inside it.
+__device__ __forceinline__ void search_probes(long long lo, long long hi,
+                                              long long t[kSearchProbes]) {
+  const long long span = hi - lo;
+#pragma unroll
+  for (int i = 0; i < kSearchProbes; ++i) {
+    const long long step = span * (i + 1) / (kSearchProbes + 1);
+    t[i] = min(lo + (step > 0 ? step : 1), hi - 1);
+  }
+}
+
+// Sum of v[0..K-1] over the group, in a fixed order (every thread gets the
+// same K results); scr holds 32 x K values.
+template <int K, typename T, typename G>
+__device__ __forceinline__ void group_sum_k(const G& g, T (&v)[K], T* scr) {
+  const int lane = g.tid() & 31, warp = g.tid() >> 5;
+#pragma unroll
+  for (int k = 0; k < K; ++k) v[k] = warp_sum(v[k]);
+  if (lane == 0)
+#pragma unroll
+    for (int k = 0; k < K; ++k) scr[warp * K + k] = v[k];
+  g.sync();
+  const int nw = g.size() >> 5;
+#pragma unroll
+  for (int k = 0; k < K; ++k) {
+    T s = T(0);
+    for (int w = 0; w < nw; ++w) s += scr[w * K + k];
+    v[k] = s;
+  }
+  g.sync();
+}
+
 // One filtered row of request r, exactly, by a thread group G (all of its
 // threads call it; thread 0 writes the row's statistics).
 template <typename G>
 __device__ __noinline__ void filtered_row_stats(const Params& P, const G& g, long long row, int r) {
+  __shared__ float s_fsum[32 * kSearchProbes];
+  __shared__ int s_isum[32 * kSearchProbes];
   const int bf16 = P.bf16;
   const float c = kLog2e / __ldg(P.temp + r);
   const int tk = P.top_k ? __ldg(P.top_k + r) : 0;
@@ -325,11 +366,25 @@ __device__ __noinline__ void filtered_row_stats(const Params& P, const G& g, lon
   if (topk_on) {
     long long lo = 0, hi = key_space;  // count(key >= lo) >= k > count(key >= hi)
     while (hi - lo > 1) {
-      const long long mid = (lo + hi) >> 1;
-      int cnt = 0;
-      row_for_each(P, row, g.tid(), g.size(), [&](float v, int) { cnt += ((long long)elem_key(v, bf16) >= mid); });
-      cnt = g.sum(cnt);
-      if (cnt >= tk) lo = mid; else hi = mid;
+      long long t[kSearchProbes];
+      search_probes(lo, hi, t);
+      int cnt[kSearchProbes];
+#pragma unroll
+      for (int i = 0; i < kSearchProbes; ++i) cnt[i] = 0;
+      row_for_each(P, row, g.tid(), g.size(), [&](float v, int) {
+        const long long k = elem_key(v, bf16);
+#pragma unroll
+        for (int i = 0; i < kSearchProbes; ++i) cnt[i] += (k >= t[i]);
+      });
+      group_sum_k(g, cnt, s_isum);
+      long long nlo = lo, nhi = hi;
+#pragma unroll
+      for (int i = 0; i < kSearchProbes; ++i) {
+        if (nhi != hi) continue;
+        if (cnt[i] >= tk) nlo = t[i]; else nhi = t[i];
+      }
+      lo = nlo;
+      hi = nhi;
     }
     kk = lo;
   }
@@ -344,14 +399,28 @@ __device__ __noinline__ void filtered_row_stats(const Params& P, const G& g, lon
     const float thr = tp * zk;
     long long lo = kk - 1, hi = (long long)elem_key(m, bf16);  // A(lo) >= thr > A(hi)
     while (hi - lo > 1) {
-      const long long mid = (lo + hi) >> 1;
-      float a = 0.f;
+      long long t[kSearchProbes];
+      search_probes(lo, hi, t);
+      float a[kSearchProbes];
+#pragma unroll
+      for (int i = 0; i < kSearchProbes; ++i) a[i] = 0.f;
       row_for_each(P, row, g.tid(), g.size(), [&](float v, int) {
         const long long k = elem_key(v, bf16);
-        if (k > mid && k >= kk) a += exp2f(fmaf(v, c, -mc));
+        if (k >= kk) {
+          const float e = exp2f(fmaf(v, c, -mc));
+#pragma unroll
+          for (int i = 0; i < kSearchProbes; ++i) a[i] += (k > t[i]) ? e : 0.f;
+        }
       });
-      a = g.sum(a);
-      if (a < thr) hi = mid; else lo = mid;
+      group_sum_k(g, a, s_fsum);
+      long long nlo = lo, nhi = hi;
+#pragma unroll
+      for (int i = 0; i < kSearchProbes; ++i) {
+        if (nhi != hi) continue;
+        if (a[i] < thr) nhi = t[i]; else nlo = t[i];
+      }
+      lo = nlo;
+      hi = nhi;
     }
     kp = hi;
   }
@@ -382,7 +451,7 @@ __device__ void filtered_row(const Params& P, long long row) {
 
 // Without the streaming pass's histogram: block b settles row b. With it:
 // the blocks share out the rows that pass listed as unsettled.
-__global__ void __launch_bounds__(kFilterThreads)
+__global__ void __launch_bounds__(kFilterThreads, 2)
 k_rows_filtered(Params P) {
   pdl_wait();
   pdl_trigger();
