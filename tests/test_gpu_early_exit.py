@@ -194,3 +194,16 @@ def test_resident_handle_falls_back_where_the_batch_needs_it(case):
         ver.close()
     assert np.array_equal(outs[0][0], outs[1][0])
     assert np.array_equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_naive_control_under_early_exit(schedule):
+    """The negative control (a rejected position redrawn from p) combined
+    with early exit, under every schedule, against the oracle."""
+    b = _early(synth.make("c5", B=40, V=20008))
+    b["flags"] = int(b["flags"]) | oracle.FLAG_NAIVE
+    gpu = _run(b, schedule)
+    ref = oracle.verify(b)
+    assert gpu["status"] == 0
+    check_structure(b, gpu)
+    assert_parity(compare(b, gpu, ref))
