@@ -16,6 +16,7 @@
 #include "resident.cuh"
 #include "rows.cuh"
 #include "rows_tma.cuh"
+#include "select.cuh"
 #include "shard.cuh"
 
 struct spec_verify_handle {
@@ -55,7 +56,8 @@ size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 bool set_row_pass_smem() {
   const int plain = (int)sv::kTmaSmemBytes, filt = (int)sv::kTmaFiltSmemBytes;
   const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
-  return cudaFuncSetAttribute(sv::k_rows_tma<true, false>, a, plain) == cudaSuccess &&
+  return cudaFuncSetAttribute(sv::k_rows_select, a, (int)sv::kSelSmemBytes) == cudaSuccess &&
+         cudaFuncSetAttribute(sv::k_rows_tma<true, false>, a, plain) == cudaSuccess &&
          cudaFuncSetAttribute(sv::k_rows_tma<false, false>, a, plain) == cudaSuccess &&
          cudaFuncSetAttribute(sv::k_rows_tma<true, true>, a, filt) == cudaSuccess &&
          cudaFuncSetAttribute(sv::k_rows_tma<true, false, true>, a, plain) == cudaSuccess &&
@@ -416,10 +418,15 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
     sv::k_rows_stream<<<(unsigned)(R * P.slices_per_row), sv::kStreamThreads, 0, stream>>>(P);
   }
   if (filters) {
-    // Every filtered row (one block each), or only the listed ones.
+    // Every filtered row (one block each): fp32 rows settled from a histogram
+    // of their truncated values; bf16 rows the streaming pass could not take
+    // by the exact search. Or only the rows that pass listed.
     const long long cap = 2ll * h->sm_count;
     const long long sgrid = P.fast_filtered ? (R < cap ? R : cap) : R;
-    launch_after(sv::k_rows_filtered, (unsigned)sgrid, sv::kFilterThreads, 0, stream, P);
+    if (!P.fast_filtered && !P.bf16)
+      launch_after(sv::k_rows_select, (unsigned)R, sv::kSelThreads, sv::kSelSmemBytes, stream, P);
+    else
+      launch_after(sv::k_rows_filtered, (unsigned)sgrid, sv::kFilterThreads, 0, stream, P);
   }
   if (timed) cudaEventRecord(h->phase[1], stream);
   launch_after(sv::k_accept, (unsigned)((b->B + sv::kAcceptWarps - 1) / sv::kAcceptWarps),

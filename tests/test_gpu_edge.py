@@ -418,3 +418,20 @@ def test_fp32_rows_with_top_k_and_top_p(V):
     b["temperature"] = rng.choice([0.0, 0.5, 1.0, 2.0], size=b["B"]).astype(np.float32)
     gpu, _ = check(b)
     assert gpu["status"] & ~np.uint32(0x8) == 0
+
+
+@pytest.mark.parametrize("mode", ["top_p", "top_k", "both"])
+def test_fp32_single_filters_at_a_large_vocabulary(mode):
+    """fp32 rows at V = 151936 with top-p only, top-k only, or both: the
+    first two settled from the histogram of truncated values (wide candidate
+    ranges near the boundary), the third by the exact search."""
+    b = synth.make("c2", B=6, V=151936)
+    rng = np.random.default_rng(17)
+    B = b["B"]
+    b["temperature"] = rng.choice([0.5, 1.0, 2.0], size=B).astype(np.float32)
+    if mode in ("top_p", "both"):
+        b["top_p"] = rng.choice([0.3, 0.9, 0.99], size=B).astype(np.float32)
+    if mode in ("top_k", "both"):
+        b["top_k"] = rng.choice([1, 50, 20000], size=B).astype(np.int32)
+    gpu, _ = check(b)
+    assert gpu["status"] & ~np.uint32(0x8) == 0
