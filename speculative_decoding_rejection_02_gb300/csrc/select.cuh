@@ -1,7 +1,9 @@
-// Top-k / top-p rows of fp32 logits (velog "vLLM 커널은 이 규칙을 어떻게
-// 옮겼나": temperature, top-k and top-p applied before the judgement), settled
-// from a histogram of their bf16-truncated values instead of searching the
-// whole 32-bit key space.
+// Top-k / top-p rows the streaming pass does not take — fp32 logits, and bf16
+// rows whose length is not a multiple of 16 bytes — (velog "vLLM 커널은 이
+// 규칙을 어떻게 옮겼나": temperature, top-k and top-p applied before the
+// judgement), settled from a histogram of their bf16-truncated values
+// instead of searching the whole key space. For bf16 rows each bin holds one
+// value, so its mass bounds meet.
 //
 // One CTA per row:
 //  1. one pass over the row finds the max (lowest argmax), Z (online) and
@@ -184,12 +186,18 @@ __device__ bool select_row(const Params& P, long long row, int r, WinHist* hist,
   // of item i: count x e(low edge) and count x e(high edge, at most m), with
   // a margin for ex2's rounding.
   const int i0 = tid * kSelItemsPerThread;
+  // A fine item of a bf16 row holds a single value: both edges are that value.
+  const bool single = P.bf16 != 0;
   auto item_bounds = [&](int i, unsigned& cnt, float& lo_m, float& hi_m) {
     cnt = (i < kWinItems) ? hist->cnt[win_slot_of_item(i)] : 0u;
     lo_m = hi_m = 0.f;
     if (cnt) {
       float lo, hi;
       sel_item_range(i, lo, hi);
+      if (single && i != kWinHugeNeg && i != kWinTinyNeg && i != kWinTinyPos &&
+          i != kWinHugePos) {
+        if (i > kWinSide) hi = lo; else lo = hi;
+      }
       const float n = (float)cnt;
       lo_m = n * ex2(fmaf(lo, c, -mc)) * 0.999999f;
       hi_m = n * ex2(fmaf(fminf(hi, m), c, -mc)) * 1.000001f;
@@ -409,7 +417,8 @@ __device__ bool select_row(const Params& P, long long row, int r, WinHist* hist,
   return true;
 }
 
-// One block per row: the filtered rows of fp32 batches.
+// One block per row: the filtered rows of batches the streaming pass's
+// histogram does not take.
 __global__ void __launch_bounds__(kSelThreads, 2)
 k_rows_select(Params P) {
   pdl_wait();

@@ -418,12 +418,11 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
     sv::k_rows_stream<<<(unsigned)(R * P.slices_per_row), sv::kStreamThreads, 0, stream>>>(P);
   }
   if (filters) {
-    // Every filtered row (one block each): fp32 rows settled from a histogram
-    // of their truncated values; bf16 rows the streaming pass could not take
-    // by the exact search. Or only the rows that pass listed.
+    // Every filtered row (one block each), settled from a histogram of its
+    // truncated values; or only the rows the streaming pass listed.
     const long long cap = 2ll * h->sm_count;
     const long long sgrid = P.fast_filtered ? (R < cap ? R : cap) : R;
-    if (!P.fast_filtered && !P.bf16)
+    if (!P.fast_filtered)
       launch_after(sv::k_rows_select, (unsigned)R, sv::kSelThreads, sv::kSelSmemBytes, stream, P);
     else
       launch_after(sv::k_rows_filtered, (unsigned)sgrid, sv::kFilterThreads, 0, stream, P);
