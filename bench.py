@@ -70,6 +70,12 @@ def parse():
                     help="with --early-exit: hold each judged row in a thread-block cluster")
     ap.add_argument("--B", type=int, default=None,
                     help="resize the workload to B requests (profiling of small cases)")
+    ap.add_argument("--V", type=int, default=None,
+                    help="resize the workload's vocabulary (profiling of other row lengths)")
+    ap.add_argument("--top-p", type=float, default=None,
+                    help="set every request's top_p (profiling of the filtered-row paths)")
+    ap.add_argument("--top-k", type=int, default=None,
+                    help="set every request's top_k (profiling of the filtered-row paths)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -442,7 +448,11 @@ def main():
     if world > 1:
         dist.init_process_group("nccl", device_id=dev)
 
-    batch = synth.make(args.config, B=args.B)
+    batch = synth.make(args.config, B=args.B, V=args.V)
+    if args.top_p is not None:
+        batch["top_p"] = np.full(batch["B"], args.top_p, np.float32)
+    if args.top_k is not None:
+        batch["top_k"] = np.full(batch["B"], args.top_k, np.int32)
     B, V = batch["B"], batch["V"]
     batch["request_base"] = rank_request_base(rank, B)
     if args.accept == "sampler-match":
@@ -558,7 +568,8 @@ def main():
                    "sample": desc, "seconds": round(secs, 2)}
 
     per_cfg = None
-    if (rank == 0 and world == 1 and args.B is None and not args.no_per_config
+    if (rank == 0 and world == 1 and args.B is None and args.V is None and args.top_p is None
+            and args.top_k is None and not args.no_per_config
             and args.config == "c5" and args.accept == "rejection" and not args.early_exit):
         per_cfg = per_config_timings(sv, dev, stream, peak, batch)
 
@@ -585,6 +596,7 @@ def main():
                               else "L2 flushed between timed calls (512 MB write)"),
                        "acceptance": args.accept,
                        "early_exit": bool(args.early_exit),
+                       "top_p_all": args.top_p, "top_k_all": args.top_k,
                        "resident_rows": bool(args.early_exit and args.resident),
                        "parallelism": f"replicas x{world}"},
             "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak,
