@@ -240,7 +240,7 @@ k_rows_stream(Params P) {
 }
 
 // ---------------------------------------------------------------------------
-// Filtered rows: exact thresholds by bisection on order-preserving keys.
+// Filtered rows: exact thresholds by an 8-ary search on order-preserving keys.
 // ---------------------------------------------------------------------------
 constexpr int kFilterThreads = 512;
 

@@ -155,7 +155,7 @@ __device__ __forceinline__ PartStat load_part(const PartStat* p) {
 }
 
 // The kTmaConsumers consumer threads as a thread group (for the exact
-// filtered-row bisection inside the row pass); fs / is: one slot per warp.
+// filtered-row search inside the row pass); fs / is: one slot per warp.
 struct ConsumerGroup {
   float* fs;
   int* is;

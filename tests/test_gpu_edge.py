@@ -154,7 +154,7 @@ def test_temperature_zero_ignores_draft_probs():
 def test_filtered_rows_on_the_streaming_path(scale, V):
     """Aligned bf16 rows with top-k / top-p take the histogram path of the
     streaming pass; tiny logits (threshold near 0) and |l| >= 256 fall back
-    to the exact bisection kernel. Both must agree with the oracle."""
+    to the exact search. Both must agree with the oracle."""
     rng = np.random.default_rng(V + (7 if scale == "ties" else int(float(scale) * 100)))
     B = 36
     g = rng.integers(0, 5, size=B)
