@@ -435,3 +435,16 @@ def test_fp32_single_filters_at_a_large_vocabulary(mode):
         b["top_k"] = rng.choice([1, 50, 20000], size=B).astype(np.int32)
     gpu, _ = check(b)
     assert gpu["status"] & ~np.uint32(0x8) == 0
+
+
+def test_fp32_flat_rows_overflow_the_candidate_buffer():
+    """fp32 rows whose values all sit in a few bf16-truncated bins: the bins
+    around the top-p boundary hold more values than the select kernel's
+    buffer, so those rows take the exact search in the same block."""
+    b = synth.make("c2", B=4, V=60000)
+    rng = np.random.default_rng(23)
+    R = b["target_logits"].shape[0]
+    b["target_logits"] = (1.0 + rng.normal(0, 1e-3, size=(R, b["V"]))).astype(np.float32)
+    b["top_p"] = np.full(b["B"], 0.5, np.float32)
+    gpu, _ = check(b)
+    assert gpu["status"] & ~np.uint32(0x8) == 0
