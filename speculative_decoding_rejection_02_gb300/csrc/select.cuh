@@ -17,9 +17,10 @@
 //  3. a second look at the row (mostly from L2) sums the exact masses above
 //     the range and copies the values inside it to shared memory;
 //  4. an 8-ary search over the copied values settles the threshold.
-// Rows it cannot settle this way (NaN, +-inf or values of 2^8 and above,
-// top-k with top-p, more candidates than the buffer holds) are settled by
-// filtered_row_stats in the same CTA.
+// With top-k and top-p, top-k is settled first, then the whole top-k set is
+// copied and top-p is searched over it. Rows it cannot settle this way (NaN,
+// +-inf or values of 2^8 and above, more values to copy than the buffer
+// holds) are settled by filtered_row_stats in the same CTA.
 #pragma once
 #include "common.cuh"
 #include "hist.cuh"
@@ -132,6 +133,123 @@ __device__ __forceinline__ void sel_probes(long long lo, long long hi, long long
   }
 }
 
+// The smallest and largest key among the copied values (every thread gets
+// them); s_i holds 2 x kSelWarps ints.
+__device__ __forceinline__ void sel_key_range(const float* cand, int n, int* s_i, long long& kmin,
+                                              long long& kmax) {
+  const int tid = threadIdx.x;
+  int lo32 = INT_MAX, hi32 = INT_MIN;  // keys with the top bit flipped, as ints
+  for (int j = tid; j < n; j += kSelThreads) {
+    const int k = (int)(float_key(cand[j]) ^ 0x80000000u);
+    lo32 = min(lo32, k);
+    hi32 = max(hi32, k);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo32 = min(lo32, __shfl_xor_sync(0xFFFFFFFFu, lo32, o));
+    hi32 = max(hi32, __shfl_xor_sync(0xFFFFFFFFu, hi32, o));
+  }
+  const int warp = tid >> 5;
+  if ((tid & 31) == 0) {
+    s_i[warp * 2] = lo32;
+    s_i[warp * 2 + 1] = hi32;
+  }
+  __syncthreads();
+  lo32 = INT_MAX;
+  hi32 = INT_MIN;
+  for (int w = 0; w < kSelWarps; ++w) {
+    lo32 = min(lo32, s_i[w * 2]);
+    hi32 = max(hi32, s_i[w * 2 + 1]);
+  }
+  __syncthreads();
+  kmin = (long long)((uint32_t)lo32 ^ 0x80000000u);
+  kmax = (long long)((uint32_t)hi32 ^ 0x80000000u);
+}
+
+// Top-p among the copied values: the smallest key t with A(t) < thr, where
+// A(t) = a_hi + the copied mass with key > t; the caller guarantees
+// A(kmin - 1) >= thr > A(kmax).
+__device__ long long sel_search_topp(const float* cand, int n, float a_hi, float thr, float c,
+                                     float mc, float* s_f, int* s_i) {
+  long long kmin, kmax;
+  sel_key_range(cand, n, s_i, kmin, kmax);
+  long long lo = kmin - 1, hi = kmax;
+  while (hi - lo > 1) {
+    long long t[kSelProbes];
+    sel_probes(lo, hi, t);
+    float a[kSelProbes];
+#pragma unroll
+    for (int i = 0; i < kSelProbes; ++i) a[i] = 0.f;
+    for (int j = threadIdx.x; j < n; j += kSelThreads) {
+      const float v = cand[j];
+      const long long k = float_key(v);
+      const float e = exp2f(fmaf(v, c, -mc));
+#pragma unroll
+      for (int i = 0; i < kSelProbes; ++i) a[i] += (k > t[i]) ? e : 0.f;
+    }
+    sel_sum_k(a, s_f);
+    long long nlo = lo, nhi = hi;
+#pragma unroll
+    for (int i = 0; i < kSelProbes; ++i) {
+      if (nhi != hi) continue;
+      if (a_hi + a[i] < thr) nhi = t[i]; else nlo = t[i];
+    }
+    lo = nlo;
+    hi = nhi;
+  }
+  return hi;
+}
+
+// Top-k among the copied values: the largest key t with count(key >= t) >=
+// krem (1 <= krem <= n).
+__device__ long long sel_search_topk(const float* cand, int n, int krem, int* s_i) {
+  long long kmin, kmax;
+  sel_key_range(cand, n, s_i, kmin, kmax);
+  long long lo = kmin, hi = kmax + 1;
+  while (hi - lo > 1) {
+    long long t[kSelProbes];
+    sel_probes(lo, hi, t);
+    int cnt[kSelProbes];
+#pragma unroll
+    for (int i = 0; i < kSelProbes; ++i) cnt[i] = 0;
+    for (int j = threadIdx.x; j < n; j += kSelThreads) {
+      const long long k = float_key(cand[j]);
+#pragma unroll
+      for (int i = 0; i < kSelProbes; ++i) cnt[i] += (k >= t[i]);
+    }
+    sel_sum_k(cnt, s_i);
+    long long nlo = lo, nhi = hi;
+#pragma unroll
+    for (int i = 0; i < kSelProbes; ++i) {
+      if (nhi != hi) continue;
+      if (cnt[i] >= krem) nlo = t[i]; else nhi = t[i];
+    }
+    lo = nlo;
+    hi = nhi;
+  }
+  return lo;
+}
+
+// The copied mass with key >= keep, and the number of such values.
+__device__ void sel_kept(const float* cand, int n, long long keep, float c, float mc, float* s_f,
+                         int* s_i, float& mass, int& count) {
+  float z = 0.f;
+  int k = 0;
+  for (int j = threadIdx.x; j < n; j += kSelThreads) {
+    const float v = cand[j];
+    if ((long long)float_key(v) >= keep) {
+      z += exp2f(fmaf(v, c, -mc));
+      ++k;
+    }
+  }
+  float fv[1] = {z};
+  sel_sum_k<1>(fv, s_f);
+  int iv[1] = {k};
+  sel_sum_k<1>(iv, s_i);
+  mass = fv[0];
+  count = iv[0];
+}
+
 // Settle filtered row `row` of request r (the whole block calls it). Returns
 // false when the row needs filtered_row_stats.
 __device__ bool select_row(const Params& P, long long row, int r, WinHist* hist, float* cand) {
@@ -145,7 +263,7 @@ __device__ bool select_row(const Params& P, long long row, int r, WinHist* hist,
   const float tp = P.top_p ? __ldg(P.top_p + r) : 1.f;
   const bool topk_on = (tk > 0 && tk < V);
   const bool topp_on = (tp < 1.f);
-  if (topk_on == topp_on) return false;  // both (or neither): the general routine
+  if (!topk_on && !topp_on) return false;
 
   // ---- 1. max, lowest argmax, online Z, NaN, counts ----
   for (int i = tid; i < kWinSlots; i += kSelThreads) hist->cnt[i] = 0u;
@@ -231,13 +349,13 @@ __device__ bool select_row(const Params& P, long long row, int r, WinHist* hist,
       float ml, mh;
       item_bounds(i, cn, ml, mh);
       bool cand_item;
-      if (topp_on) {
+      if (topk_on) {
+        cand_item = (above_c < (unsigned)tk) && (above_c + cn >= (unsigned)tk);
+        if (cand_item) above_cnt_at = above_c;
+      } else {
         const bool kept = (above_h + mh < thr_lo);
         const bool dropped = (above_l >= thr_hi);
         cand_item = !kept && !dropped;
-      } else {
-        cand_item = (above_c < (unsigned)tk) && (above_c + cn >= (unsigned)tk);
-        if (cand_item) above_cnt_at = above_c;
       }
       if (cand_item) {
         lo_item = min(lo_item, i);
@@ -311,109 +429,57 @@ __device__ bool select_row(const Params& P, long long row, int r, WinHist* hist,
   if (n != (int)need) return false;
 
   // ---- 4. the threshold among the copied values (8-ary search on keys) ----
-  long long kmin = 0xFFFFFFFFll, kmax = 0;
-  for (int j = tid; j < n; j += kSelThreads) {
-    const long long k = float_key(cand[j]);
-    kmin = min(kmin, k);
-    kmax = max(kmax, k);
-  }
-  {
-    int lo32 = (int)(kmin ^ 0x80000000ll), hi32 = (int)(kmax ^ 0x80000000ll);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      lo32 = min(lo32, __shfl_xor_sync(0xFFFFFFFFu, lo32, o));
-      hi32 = max(hi32, __shfl_xor_sync(0xFFFFFFFFu, hi32, o));
-    }
-    const int warp = tid >> 5;
-    if ((tid & 31) == 0) {
-      s_i[warp * 2] = lo32;
-      s_i[warp * 2 + 1] = hi32;
-    }
-    __syncthreads();
-    lo32 = INT_MAX;
-    hi32 = INT_MIN;
-    for (int w = 0; w < kSelWarps; ++w) {
-      lo32 = min(lo32, s_i[w * 2]);
-      hi32 = max(hi32, s_i[w * 2 + 1]);
-    }
-    __syncthreads();
-    kmin = (long long)(uint32_t)(lo32 ^ (int)0x80000000);
-    kmax = (long long)(uint32_t)(hi32 ^ (int)0x80000000);
-  }
   long long keep;  // keep the elements whose key is >= keep
-  if (topp_on) {
-    // A(t) = a_hi + the copied mass with key > t: A(kmin - 1) >= thr > A(kmax)
-    // (Z from the first pass's online sum)
+  float z_kept = 0.f;
+  if (!topk_on) {
+    // (Z from the first pass's online sum) the range must hold the
+    // boundary: the mass above it below thr, with its own mass added at
+    // least thr (else the general routine)
     const float thr = tp * z1;
-    long long lo = kmin - 1, hi = kmax;
-    // the range must hold the boundary: the mass above it below thr, with
-    // its own mass added at least thr (else the general routine)
     if (!(a_hi < thr) || !(a_hi + a_mid >= thr)) return false;
-    while (hi - lo > 1) {
-      long long t[kSelProbes];
-      sel_probes(lo, hi, t);
-      float a[kSelProbes];
-#pragma unroll
-      for (int i = 0; i < kSelProbes; ++i) a[i] = 0.f;
-      for (int j = tid; j < n; j += kSelThreads) {
-        const float v = cand[j];
-        const long long k = float_key(v);
-        const float e = exp2f(fmaf(v, c, -mc));
-#pragma unroll
-        for (int i = 0; i < kSelProbes; ++i) a[i] += (k > t[i]) ? e : 0.f;
-      }
-      sel_sum_k(a, s_f);
-      long long nlo = lo, nhi = hi;
-#pragma unroll
-      for (int i = 0; i < kSelProbes; ++i) {
-        if (nhi != hi) continue;
-        if (a_hi + a[i] < thr) nhi = t[i]; else nlo = t[i];
-      }
-      lo = nlo;
-      hi = nhi;
-    }
-    keep = hi;
+    keep = sel_search_topp(cand, n, a_hi, thr, c, mc, s_f, s_i);
+    float mass;
+    int cnt;
+    sel_kept(cand, n, keep, c, mc, s_f, s_i, mass, cnt);
+    z_kept = a_hi + mass;
   } else {
-    // count(copied key >= t) >= k - above_k > count(copied key >= kmax + 1)
     const int krem = tk - (int)above_k;
     if (krem < 1 || krem > n) return false;
-    long long lo = kmin, hi = kmax + 1;
-    while (hi - lo > 1) {
-      long long t[kSelProbes];
-      sel_probes(lo, hi, t);
-      int cnt[kSelProbes];
-#pragma unroll
-      for (int i = 0; i < kSelProbes; ++i) cnt[i] = 0;
-      for (int j = tid; j < n; j += kSelThreads) {
-        const long long k = float_key(cand[j]);
-#pragma unroll
-        for (int i = 0; i < kSelProbes; ++i) cnt[i] += (k >= t[i]);
-      }
-      sel_sum_k(cnt, s_i);
-      long long nlo = lo, nhi = hi;
-#pragma unroll
-      for (int i = 0; i < kSelProbes; ++i) {
-        if (nhi != hi) continue;
-        if (cnt[i] >= krem) nlo = t[i]; else nhi = t[i];
-      }
-      lo = nlo;
-      hi = nhi;
+    keep = sel_search_topk(cand, n, krem, s_i);
+    float mass;
+    int cnt;
+    sel_kept(cand, n, keep, c, mc, s_f, s_i, mass, cnt);
+    z_kept = a_hi + mass;
+    if (topp_on) {
+      // Top-p over the top-k set, renormalised (Z_k = z_kept): copy the
+      // whole set (the values above the boundary bin and its kept ones)
+      // and search it with nothing above.
+      const int nk = (int)above_k + cnt;
+      if (nk > kSelCand) return false;
+      __syncthreads();
+      if (tid == 0) s_ncand = 0;
+      __syncthreads();
+      const long long kk = keep;
+      row_for_each(P, row, tid, kSelThreads, [&](float v, int) {
+        if ((long long)float_key(v) >= kk) {
+          const int at = atomicAdd(&s_ncand, 1);
+          if (at < kSelCand) cand[at] = v;
+        }
+      });
+      __syncthreads();
+      const int n2 = s_ncand;
+      __syncthreads();
+      if (n2 != nk) return false;
+      // Z_k summed over the copy itself, so that A(kmin - 1) = Z_k >= thr
+      // (top_p < 1) and A(kmax) = 0 < thr hold as the search sums them
+      sel_kept(cand, n2, 0, c, mc, s_f, s_i, mass, cnt);
+      const float thr = tp * mass;
+      keep = sel_search_topp(cand, n2, 0.f, thr, c, mc, s_f, s_i);
+      sel_kept(cand, n2, keep, c, mc, s_f, s_i, mass, cnt);
+      z_kept = mass;
     }
-    keep = lo;
   }
-  // Z over the kept set: the mass above the range and the kept copies.
-  float zk = 0.f;
-  for (int j = tid; j < n; j += kSelThreads) {
-    const float v = cand[j];
-    if ((long long)float_key(v) >= keep) zk += exp2f(fmaf(v, c, -mc));
-  }
-  {
-    float fv[1] = {zk};
-    sel_sum_k<1>(fv, s_f);
-    zk = fv[0];
-  }
-  if (tid == 0)
-    finish_row(P, row, r, kFiltered, m, am, a_hi + zk, key_float((uint32_t)keep), c);
+  if (tid == 0) finish_row(P, row, r, kFiltered, m, am, z_kept, key_float((uint32_t)keep), c);
   return true;
 }
 
