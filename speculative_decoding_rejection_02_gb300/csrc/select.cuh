@@ -124,6 +124,44 @@ __device__ __forceinline__ void sel_suffix_k(T (&v)[K], T (&total)[K], T* scr) {
   __syncthreads();
 }
 
+// Visit every element of a row, thread tid taking 16-byte chunks tid,
+// tid + 512, ... with four chunks' loads issued before any is used (the
+// looks at a row are bound by load latency otherwise); misaligned rows
+// element by element.
+template <typename F>
+__device__ __forceinline__ void sel_row_each(const Params& P, long long row, F&& f) {
+  const int V = P.V;
+  const int esize = P.bf16 ? 2 : 4;
+  const char* rowp = (const char*)P.logits + row * (long long)V * esize;
+  const int tid = threadIdx.x;
+  int jt = 0;
+  if ((reinterpret_cast<uintptr_t>(rowp) & 15) == 0) {
+    const int epc = 16 / esize;
+    const int nchunk = V / epc;
+    jt = nchunk * epc;
+    constexpr int kAhead = 4;
+    const uint4* src = (const uint4*)rowp;
+    int ch = tid;
+    for (; ch + (kAhead - 1) * kSelThreads < nchunk; ch += kAhead * kSelThreads) {
+      uint4 w[kAhead];
+#pragma unroll
+      for (int u = 0; u < kAhead; ++u) w[u] = __ldg(src + ch + u * kSelThreads);
+#pragma unroll
+      for (int u = 0; u < kAhead; ++u) {
+        float e[8];
+        unpack_chunk(w[u], P.bf16, e);
+        for (int t = 0; t < epc; ++t) f(e[t], (ch + u * kSelThreads) * epc + t);
+      }
+    }
+    for (; ch < nchunk; ch += kSelThreads) {
+      float e[8];
+      unpack_chunk(__ldg(src + ch), P.bf16, e);
+      for (int t = 0; t < epc; ++t) f(e[t], ch * epc + t);
+    }
+  }
+  for (int j = jt + tid; j < V; j += kSelThreads) f(load_logit(P, row, j), j);
+}
+
 __device__ __forceinline__ void sel_probes(long long lo, long long hi, long long t[kSelProbes]) {
   const long long span = hi - lo;
 #pragma unroll
@@ -270,7 +308,7 @@ __device__ bool select_row(const Params& P, long long row, int r, WinHist* hist,
   __syncthreads();
   float vmax = -INFINITY, vmc = 0.f, s = 0.f;
   int imax = kNoIndex, nan_seen = 0;
-  row_for_each(P, row, tid, kSelThreads, [&](float v, int j) {
+  sel_row_each(P, row, [&](float v, int j) {
     nan_seen |= (v != v);
     if (v > vmax || (imax == kNoIndex && v == v)) {
       const float nmc = __fmul_rn(v, c);
@@ -406,7 +444,7 @@ __device__ bool select_row(const Params& P, long long row, int r, WinHist* hist,
   if (tid == 0) s_ncand = 0;
   __syncthreads();
   float a_hi = 0.f, a_mid = 0.f;
-  row_for_each(P, row, tid, kSelThreads, [&](float v, int) {
+  sel_row_each(P, row, [&](float v, int) {
     const int it = sel_item(v);
     if (it >= lo_r) {
       const float e = exp2f(fmaf(v, c, -mc));
@@ -460,7 +498,7 @@ __device__ bool select_row(const Params& P, long long row, int r, WinHist* hist,
       if (tid == 0) s_ncand = 0;
       __syncthreads();
       const long long kk = keep;
-      row_for_each(P, row, tid, kSelThreads, [&](float v, int) {
+      sel_row_each(P, row, [&](float v, int) {
         if ((long long)float_key(v) >= kk) {
           const int at = atomicAdd(&s_ncand, 1);
           if (at < kSelCand) cand[at] = v;
