@@ -75,7 +75,6 @@ __device__ __forceinline__ void enqueue_match_races(const Params& P, int r, int 
       const RaceView v = race_view(P, r, task.row, task.qrow, i, kRaceP, -1, s.m, s.c,
                                    s.inv_z, s.theta, s.z);
       P.race_best[row] = race_candidate(P, v, s.argmax);
-      P.race_counter[row] = 0u;
       P.race_list[at + (unsigned)__popc(m & ((1u << lane) - 1u))] = task;
     }
   }
@@ -241,7 +240,6 @@ k_accept(Params P) {
       // Only requests with a race own slot r (under sampler-match the slots
       // are rows, and greedy requests must not touch them).
       P.race_best[r] = seed_best;
-      P.race_counter[r] = 0u;
     }
     if (st & SPEC_STATUS_BAD_TOKEN) atomicOr(P.status, SPEC_STATUS_BAD_TOKEN);
   }

@@ -68,8 +68,7 @@ struct RaceTask {
   int mode;     // RaceMode
   int x;        // draft token at k*
   float m, c, inv_z, theta, z;  // RowStats of the row
-  int slot;     // index into race_best / race_counter (request, or row for
-                // sampler-match)
+  int slot;     // index into race_best (request, or row for sampler-match)
 };
 
 // One part of a row streamed by one CTA under early exit (rows are split
@@ -110,7 +109,6 @@ struct Params {
   unsigned* row_counter;
   RaceDesc* race;
   unsigned long long* race_best;  // per race slot: packed (score, ~index)
-  unsigned* race_counter;         // per race slot: finished slices
   RaceTask* race_list;   // races to draw (order not fixed)
   unsigned* race_count;  // entries in race_list
   unsigned* status;

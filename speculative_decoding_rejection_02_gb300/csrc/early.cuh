@@ -188,7 +188,6 @@ __device__ __noinline__ void early_decide(const Params& P, int r, int pos, int g
     task.z = s.z;
     task.slot = r;
     P.race_best[r] = race_candidate(P, v, s.argmax);
-    P.race_counter[r] = 0u;
     P.race_list[atomicAdd(P.race_count, 1u)] = task;
   }
   for (int i = k + 1; i <= gamma; ++i) P.out_tokens[row0 + i] = -1;

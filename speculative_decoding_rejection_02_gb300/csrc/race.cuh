@@ -24,7 +24,8 @@
 // lanes; after the draw, -ln U >= 1 - U bounds every score by w / (1 - U),
 // so the logarithm and the division run only for entries that can still
 // win. Slice winners meet in one 64-bit atomicMax of (score bits, ~index);
-// the last task of a race writes the token to the race row's output slot.
+// k_race_token, launched next, writes each race's token to the race row's
+// output slot.
 #pragma once
 #include "common.cuh"
 #include "philox.cuh"
@@ -472,8 +473,6 @@ __global__ void __launch_bounds__(kRaceThreads, 4)
 k_race(Params P) {
   pdl_wait();
   extern __shared__ __align__(128) unsigned char race_smem[];
-  __shared__ int s_last;
-  __shared__ unsigned long long s_packed;
   __shared__ __align__(8) uint64_t bar;
   __shared__ int s_staged;
   __shared__ unsigned long long s_lb;
@@ -602,39 +601,45 @@ k_race(Params P) {
     }
   }
   block_argmax(best, best_j);
-  if (threadIdx.x == 0) {
-    if (best_j != kNoIndex && best > 0.f)
-      atomicMax(P.race_best + slot, race_pack(best, best_j + v.v0));
-    __threadfence();
-    const unsigned prev = atomicAdd(P.race_counter + slot, 1u);
-    s_last = (prev == (unsigned)P.race_slices - 1u);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    s_packed = atomicAdd(P.race_best + slot, 0ull);
-  }
-  __syncthreads();
-  const unsigned long long packed = s_packed;
+  if (threadIdx.x == 0 && best_j != kNoIndex && best > 0.f)
+    atomicMax(P.race_best + slot, race_pack(best, best_j + v.v0));
+}
+
+// The token of race i (one CTA each), from the best that every slice of
+// the race has raised (the kernel runs after k_race); a race whose weights
+// were all 0 (rounding only) draws from p over the whole row instead. In a
+// sharded call the rank's winner is left for the caller to combine.
+__global__ void __launch_bounds__(kRaceThreads)
+k_race_token(Params P) {
+  pdl_wait();
+  __shared__ RaceItem gqueue[kRaceThreads * kRaceGroups];
+  const unsigned n_race = *P.race_count;
+  const unsigned i = blockIdx.x;
+  if (i >= n_race) return;
+  const RaceTask task = P.race_list[i];
+  const int r = task.r;
+  // Second race of a sharded call: only where every residual weight was 0.
+  if (P.sh_skip && P.sh_skip[r] != 0ull) return;
+  const unsigned long long packed = __ldcg(P.race_best + task.slot);
   if (P.shard) {
-    // Sharded call: this rank's winner, combined across ranks by the caller.
     if (threadIdx.x == 0) P.sh_best[r] = packed;
     return;
   }
-  int tok;
-  if (packed == 0ull) {
-    // Every weight was 0 (rounding only): draw from p over the whole row.
-    float b2 = 0.f;
-    int j2 = kNoIndex;
-    if (v.z > 0.f) race_range_global(P, v, kRaceP, 0u, groups, b2, j2, gqueue);
-    block_argmax(b2, j2);
-    tok = (j2 == kNoIndex) ? 0 : j2;
-    if (threadIdx.x == 0) atomicOr(P.status, SPEC_STATUS_EMPTY_RESIDUAL);
-  } else {
-    tok = (int)(0xFFFFFFFFu - (uint32_t)(packed & 0xFFFFFFFFull));
+  if (packed) {
+    if (threadIdx.x == 0) P.out_tokens[task.row] = (int)(0xFFFFFFFFu - (uint32_t)packed);
+    return;
   }
-  if (threadIdx.x == 0) P.out_tokens[v.row] = tok;
+  const RaceView v = race_view(P, r, task.row, task.qrow, task.kstar, task.mode, task.x, task.m,
+                               task.c, task.inv_z, task.theta, task.z);
+  float b2 = 0.f;
+  int j2 = kNoIndex;
+  if (v.z > 0.f)
+    race_range_global(P, v, kRaceP, 0u, (uint32_t)((P.V + 3) / 4), b2, j2, gqueue);
+  block_argmax(b2, j2);
+  if (threadIdx.x == 0) {
+    P.out_tokens[v.row] = (j2 == kNoIndex) ? 0 : j2;
+    atomicOr(P.status, SPEC_STATUS_EMPTY_RESIDUAL);
+  }
 }
 
 }  // namespace sv

@@ -120,10 +120,7 @@ k_shard_finish(Params P) {
 __global__ void k_shard_race_reset(Params P) {
   const int r = blockIdx.x * blockDim.x + threadIdx.x;
   if (r >= P.B) return;
-  if (P.sh_skip[r] == 0ull) {
-    P.race_best[r] = 0ull;
-    P.race_counter[r] = 0u;
-  }
+  if (P.sh_skip[r] == 0ull) P.race_best[r] = 0ull;
 }
 
 // The recovered / bonus token of each request from the combined winners.

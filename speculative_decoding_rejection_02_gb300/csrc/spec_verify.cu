@@ -28,7 +28,6 @@ struct spec_verify_handle {
   unsigned* row_counter;
   sv::RaceDesc* race;
   unsigned long long* race_best;
-  unsigned* race_counter;
   sv::RaceTask* race_list;
   unsigned* race_count;  // [3]: races listed, rows left to the slow kernel, row tickets
   long long* pending_rows;
@@ -226,7 +225,6 @@ sv::Params make_params(spec_verify_handle* h, const spec_verify_batch* b, bool g
   P.row_counter = h->row_counter;
   P.race = h->race;
   P.race_best = h->race_best;
-  P.race_counter = h->race_counter;
   P.race_list = h->race_list;
   P.race_count = h->race_count;
   P.pending_rows = h->pending_rows;
@@ -389,6 +387,7 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
     }
     launch_after(sv::k_race, (unsigned)(races * P.race_slices), sv::kRaceThreads,
                  sv::race_smem_bytes(P.bf16 ? 2 : 4, P.q != nullptr), stream, P);
+    launch_after(sv::k_race_token, (unsigned)races, sv::kRaceThreads, 0, stream, P);
     if (timed) cudaEventRecord(h->phase[3], stream);
     if (cudaPeekAtLastError() != cudaSuccess) {
       cudaGetLastError();
@@ -434,6 +433,7 @@ int launch(spec_verify_handle* h, const spec_verify_batch* b, cudaStream_t strea
   if (!greedy) {
     launch_after(sv::k_race, (unsigned)(races * P.race_slices), sv::kRaceThreads,
                  sv::race_smem_bytes(P.bf16 ? 2 : 4, P.q != nullptr), stream, P);
+    launch_after(sv::k_race_token, (unsigned)races, sv::kRaceThreads, 0, stream, P);
     if (match)
       launch_after(sv::k_match, (unsigned)((b->B + sv::kAcceptWarps - 1) / sv::kAcceptWarps),
                    sv::kAcceptWarps * 32, 0, stream, P);
@@ -507,7 +507,6 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   // Race slots and tasks: one per row covers sampler-match batches.
   const size_t sz_race = align_up(n_b * sizeof(sv::RaceDesc));
   const size_t sz_best = align_up(n_rows * sizeof(unsigned long long));
-  const size_t sz_rccnt = align_up(n_rows * sizeof(unsigned));
   const size_t sz_list = align_up(n_rows * sizeof(sv::RaceTask));
   const size_t sz_lcnt = align_up(3 * sizeof(unsigned));
   const size_t sz_pend = align_up(n_rows * sizeof(long long));
@@ -519,7 +518,7 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   const size_t sz_pdone = align_up(n_b * sizeof(unsigned));
   const size_t sz_phist = align_up(n_b * sizeof(sv::WinHist));
   const size_t sz_stat = align_up(sizeof(unsigned));
-  const size_t total = sz_rows + sz_part + sz_rcnt + sz_race + sz_best + sz_rccnt + sz_list +
+  const size_t total = sz_rows + sz_part + sz_rcnt + sz_race + sz_best + sz_list +
                        sz_lcnt + sz_pend + sz_queue + sz_qready + sz_qctl + sz_pstat + sz_pdone +
                        sz_phist + sz_stat;
   if (cudaMalloc(&h->ws, total) != cudaSuccess) {
@@ -537,7 +536,6 @@ int spec_verify_init(spec_verify_handle** out, const spec_verify_config* cfg) {
   h->row_counter = (unsigned*)p; p += sz_rcnt;
   h->race = (sv::RaceDesc*)p; p += sz_race;
   h->race_best = (unsigned long long*)p; p += sz_best;
-  h->race_counter = (unsigned*)p; p += sz_rccnt;
   h->race_list = (sv::RaceTask*)p; p += sz_list;
   h->race_count = (unsigned*)p; p += sz_lcnt;
   h->pending_rows = (long long*)p; p += sz_pend;
@@ -701,6 +699,7 @@ int spec_verify_shard_judge(spec_verify_handle* h, const spec_verify_batch* b,
       P);
   sv::k_race<<<(unsigned)((long long)b->B * P.race_slices), sv::kRaceThreads,
                sv::race_smem_bytes(P.bf16 ? 2 : 4, P.q != nullptr), s>>>(P);
+  sv::k_race_token<<<(unsigned)b->B, sv::kRaceThreads, 0, s>>>(P);
   return launched();
 }
 
@@ -719,6 +718,7 @@ int spec_verify_shard_race_p(spec_verify_handle* h, const spec_verify_batch* b,
   sv::k_shard_race_reset<<<(b->B + 255) / 256, 256, 0, s>>>(P);
   sv::k_race<<<(unsigned)((long long)b->B * P.race_slices), sv::kRaceThreads,
                sv::race_smem_bytes(P.bf16 ? 2 : 4, P.q != nullptr), s>>>(P);
+  sv::k_race_token<<<(unsigned)b->B, sv::kRaceThreads, 0, s>>>(P);
   return launched();
 }
 
@@ -764,8 +764,7 @@ constexpr size_t kNaOffPart = kNaOffRows + na_align(kNaRows * sizeof(sv::RowStat
 constexpr size_t kNaOffRcnt = kNaOffPart + na_align(kNaRows * kNaSlices * sizeof(sv::SlicePartial));
 constexpr size_t kNaOffRace = kNaOffRcnt + na_align(kNaRows * sizeof(unsigned));
 constexpr size_t kNaOffBest = kNaOffRace + na_align(kNaBatch * sizeof(sv::RaceDesc));
-constexpr size_t kNaOffRccnt = kNaOffBest + na_align(kNaRows * sizeof(unsigned long long));
-constexpr size_t kNaOffList = kNaOffRccnt + na_align(kNaRows * sizeof(unsigned));
+constexpr size_t kNaOffList = kNaOffBest + na_align(kNaRows * sizeof(unsigned long long));
 constexpr size_t kNaOffLcnt = kNaOffList + na_align(kNaRows * sizeof(sv::RaceTask));
 constexpr size_t kNaOffPend = kNaOffLcnt + na_align(3 * sizeof(unsigned));
 // Early exit without row parts: one queue slot per row, plus the spare.
@@ -859,7 +858,6 @@ extern "C" int spec_verify_run_noalloc(const spec_verify_batch* b, void* stream,
   h.row_counter = (unsigned*)(nd.base + kNaOffRcnt);
   h.race = (sv::RaceDesc*)(nd.base + kNaOffRace);
   h.race_best = (unsigned long long*)(nd.base + kNaOffBest);
-  h.race_counter = (unsigned*)(nd.base + kNaOffRccnt);
   h.race_list = (sv::RaceTask*)(nd.base + kNaOffList);
   h.race_count = (unsigned*)(nd.base + kNaOffLcnt);
   h.pending_rows = (long long*)(nd.base + kNaOffPend);

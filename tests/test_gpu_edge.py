@@ -318,6 +318,41 @@ def test_top_p_only_multi_stage_cases(case):
     assert gpu["status"] & ~np.uint32(0x8) == 0
 
 
+@pytest.mark.parametrize("schedule", ["full", "queue", "resident"])
+@pytest.mark.parametrize("V,dtype", [(300, "f32"), (20008, "bf16"), (20011, "bf16")])
+def test_all_residual_weights_zero_draw_from_p(V, dtype, schedule):
+    """Draft probabilities of 1 at every token: after a rejection every
+    residual weight max(p - q, 0) is 0, so the token is drawn from p over the
+    whole row and the empty-residual status bit is set, as the oracle reads
+    a residual of zero mass. V = 20011 bf16 rows are not 16-byte aligned (the
+    race reads them from global memory)."""
+    import speculative_decoding_rejection_02_gb300 as sv
+    rng = np.random.default_rng(11)
+    B = 24
+    g = rng.integers(1, 5, size=B)
+    N = int(g.sum())
+    logits = rng.normal(0, 2, size=(N + B, V))
+    q = np.ones((N, V), np.float32)
+    ids = rng.integers(0, V, size=N).astype(np.int32)
+    early = schedule != "full"
+    b = make_batch(logits, g, ids, np.ones(B, np.float32), q, dtype=dtype, seed=7,
+                   flags=sv.FLAG_EARLY_EXIT if early else 0)
+    config = {"full": 0, "queue": sv.CONFIG_EARLY_QUEUE,
+              "resident": sv.CONFIG_EARLY_RESIDENT}[schedule]
+    ver = sv.Verifier(max_batch=B, max_rows=N + B, max_vocab=V, config_flags=config)
+    try:
+        gpu = run_gpu(b, verifier=ver)
+    finally:
+        ver.close()
+    ref = oracle.verify(b)
+    check_structure(b, gpu)
+    assert_parity(compare(b, gpu, ref))
+    empty = (ref["req_status"] & 0x8) != 0
+    assert empty.sum() >= B // 2
+    assert gpu["status"] & 0x8
+    assert gpu["status"] & ~np.uint32(0x8) == 0
+
+
 def test_masked_races_repeat_exactly():
     """Every draft token is its row's argmax and one-hot, so each rejection
     races with the argmax masked and no seeded best: the race's first slice
