@@ -335,6 +335,49 @@ def ncu_traffic(config: str):
     return None
 
 
+# The race's instruction count per raced entry, from ncu on c5 resized to
+# B = 256 (profiles/k_race_c5.md: smsp__inst_executed.sum 42.25 M warp
+# instructions for 128 races of 256000 entries), valid while the race's
+# sources hash to the recorded value.
+RACE_SOURCES = ("common.cuh", "pipe.cuh", "philox.cuh", "race.cuh")
+RACE_SOURCES_SHA = "3112193ef603ac92"
+RACE_INSTR_PER_ENTRY = 42.25e6 * 32 / (128 * 256000)
+ISSUE_PER_SM_CLOCK = 4  # warp instructions: one per scheduler per clock, four schedulers
+
+
+def race_source_sha() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "speculative_decoding_rejection_02_gb300", "csrc")
+    for fn in RACE_SOURCES:
+        with open(os.path.join(d, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def race_issue(batch, num_accepted, race_ms, args, clock_info, dev):
+    """The race against its instruction-issue bound: warp instructions per
+    second (ncu's instructions per raced entry x the entries this call
+    raced, over the race phase) against SMs x four schedulers x the SM
+    clock sampled during the run. Only for the workload the count was
+    measured on (c5 with the rejection rule), and null once the race's
+    sources differ from the measured ones."""
+    import torch
+    if (args.config != "c5" or args.accept != "rejection" or args.resident or
+            args.V is not None or args.top_p is not None or args.top_k is not None or
+            race_source_sha() != RACE_SOURCES_SHA or not (clock_info or {}).get("sm_mhz")):
+        return None
+    races = int((batch["temperature"] > 0).sum())  # one race per request with T > 0
+    entries = races * batch["V"]
+    warp_instr = RACE_INSTR_PER_ENTRY * entries / 32
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peak = sms * ISSUE_PER_SM_CLOCK * clock_info["sm_mhz"] * 1e6 / 1e9
+    achieved = warp_instr / (race_ms * 1e-3) / 1e9
+    return {"bound": "issue", "kernel": "race (k_race + k_race_token)",
+            "achieved": achieved, "peak": peak, "unit": "G warp instructions/s",
+            "frac": achieved / peak, "instr_per_entry": RACE_INSTR_PER_ENTRY,
+            "entries": entries, "peak_from": f"{sms} SMs x {ISSUE_PER_SM_CLOCK} x sampled SM clock"}
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -573,14 +616,14 @@ def main():
             and args.config == "c5" and args.accept == "rejection" and not args.early_exit):
         per_cfg = per_config_timings(sv, dev, stream, peak, batch)
 
-    # row pass, accept scan, race; with top-k / top-p also the exact kernel
-    # for the rows the row pass leaves unsettled
+    # row pass, accept scan, race, race tokens; with top-k / top-p also the
+    # kernel for the rows the row pass leaves unsettled
     filters = batch.get("top_k") is not None or batch.get("top_p") is not None
-    launches_per_step = 3 + (1 if filters else 0)
+    launches_per_step = 4 + (1 if filters else 0)
     if args.accept == "sampler-match":
         launches_per_step += 1  # k_match
     if args.early_exit:
-        launches_per_step = 3  # queue init, row pass, race
+        launches_per_step = 4  # queue init, row pass, race, race tokens
         if args.resident and not filters:
             launches_per_step = 1  # the cluster kernel
     if rank == 0:
@@ -609,6 +652,7 @@ def main():
                          "frac_nominal": fr["rows_frac_nominal"],
                          "nominal_peak": NOMINAL_HBM_GBS,
                          "traffic": ncu_traffic(args.config)},
+            "race_issue": race_issue(batch, n_acc, phases["race"], args, clock_info, dev),
             "per_config": per_cfg,
             "cpu_baseline": cpu,
             "cpu_baseline_all_cores": cpu_all,

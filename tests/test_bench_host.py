@@ -63,3 +63,30 @@ def test_all_cores_baseline_reports_its_sample():
     assert rate > 0 and secs > 0
     assert 1 <= threads <= bench.host_cores()
     assert "threads on disjoint request sets" in desc
+
+
+def test_race_issue_arithmetic_and_its_guards(monkeypatch):
+    """The race's issue figure: warp instructions = instructions per entry x
+    entries / 32 over the race phase, against SMs x 4 x the sampled clock;
+    absent for other workloads, changed race sources or missing clocks."""
+    import types
+
+    import torch
+
+    monkeypatch.setattr(torch.cuda, "get_device_properties",
+                        lambda dev: types.SimpleNamespace(multi_processor_count=152))
+    args = types.SimpleNamespace(config="c5", accept="rejection", resident=False, V=None,
+                                 top_p=None, top_k=None)
+    batch = {"temperature": np.array([0.0, 0.8] * 8, np.float32), "V": 1000}
+    r = bench.race_issue(batch, None, 0.5, args, {"sm_mhz": 2000.0}, None)
+    want = bench.RACE_INSTR_PER_ENTRY * 8 * 1000 / 32 / 0.5e-3 / 1e9
+    assert abs(r["achieved"] - want) < 1e-9 * want
+    assert abs(r["peak"] - 152 * 4 * 2000e6 / 1e9) < 1e-9
+    assert r["entries"] == 8000 and r["bound"] == "issue"
+    assert bench.race_source_sha() == bench.RACE_SOURCES_SHA
+    assert bench.race_issue(batch, None, 0.5, args, None, None) is None
+    for k, v in (("config", "c4"), ("accept", "sampler-match"), ("V", 5000)):
+        other = types.SimpleNamespace(**{**vars(args), k: v})
+        assert bench.race_issue(batch, None, 0.5, other, {"sm_mhz": 2000.0}, None) is None
+    monkeypatch.setattr(bench, "RACE_SOURCES_SHA", "0" * 16)
+    assert bench.race_issue(batch, None, 0.5, args, {"sm_mhz": 2000.0}, None) is None
