@@ -44,3 +44,30 @@ def test_race_is_scale_free():
     w = rng.random(50)
     for r in range(200):
         assert oracle.race(w, 9, r, 0)[0] == oracle.race(w * 1e-30, 9, r, 0)[0]
+
+
+def test_zero_residual_mass_draws_from_p():
+    """Draft probabilities of 1 at every token: p <= q everywhere, so after a
+    rejection the residual max(p - q, 0) has zero mass; the reading is that
+    the token is then drawn from p (the race on w = p) and the request is
+    flagged (status bit 3). With the draft drawn uniformly over the 5 toy
+    tokens, acceptance is mean p(x) = 1/5 and the first emitted token
+    follows p exactly: P(j) = p_j / 5 (accepted) + (4/5) p_j (drawn from p)."""
+    import synth
+    rounds = 400_000
+    b = synth.toy_batch("prob", rounds, seed=17, q=[1.0] * 5)
+    o = oracle.verify(b)
+    acc = o["num_accepted"].astype(np.float64)
+    assert abs(acc.mean() - 0.2) < 5 * math.sqrt(0.2 * 0.8 / rounds)
+    rejected = acc < 1
+    flagged = (o["req_status"] & 0x8) != 0
+    assert np.array_equal(flagged, rejected)
+    first = o["out_tokens"].reshape(-1, 2)[:, 0]
+    p = np.asarray(synth.TOY_P)
+    expect = p * rounds
+    counts = np.bincount(first, minlength=5)
+    assert ((counts - expect) ** 2 / expect).sum() < 18.47  # 4 dof, 1e-3
+    # and the tokens drawn after a rejection alone follow p too
+    counts_r = np.bincount(first[rejected], minlength=5)
+    expect_r = p * rejected.sum()
+    assert ((counts_r - expect_r) ** 2 / expect_r).sum() < 18.47
