@@ -77,6 +77,9 @@ def parse():
     ap.add_argument("--top-k", type=int, default=None,
                     help="set every request's top_k (profiling of the filtered-row paths)")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-chunks", type=int, default=4,
+                    help="end to end: verify the batch as this many request ranges, each "
+                         "range's copies overlapping the previous range's verification")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
@@ -378,6 +381,15 @@ def race_issue(batch, num_accepted, race_ms, args, clock_info, dev):
             "entries": entries, "peak_from": f"{sms} SMs x {ISSUE_PER_SM_CLOCK} x sampled SM clock"}
 
 
+def request_chunks(cu, k):
+    """k contiguous, non-empty request ranges [r0, r1) covering the batch,
+    about equal in requests (fewer when the batch has fewer requests)."""
+    B = len(cu) - 1
+    k = max(1, min(int(k), B))
+    edges = [round(i * B / k) for i in range(k + 1)]
+    return [(edges[i], edges[i + 1]) for i in range(k) if edges[i + 1] > edges[i]]
+
+
 def host_cores() -> int:
     try:
         return len(os.sched_getaffinity(0))
@@ -577,16 +589,65 @@ def main():
         out_acc = torch.empty(B, dtype=torch.int32).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values()) + q_read
         d2h = out_tok.numel() * 4 + out_acc.numel() * 4
+        tok_ref = db.out_tokens.cpu().numpy()
+        chunks = request_chunks(batch["cu_num_draft"], args.e2e_chunks)
+        parts = []
+        if len(chunks) > 1:
+            # Each request range is its own call (request_base = its first
+            # request, so the draws are those of the whole batch); a copy
+            # stream moves range c + 1 while range c is verified.
+            cu_np = batch["cu_num_draft"]
+            h2d = q_read
+            for r0, r1 in chunks:
+                a, z = int(cu_np[r0]), int(cu_np[r1])
+                row0, row1 = a + r0, z + r1
+                cu_h = torch.from_numpy((cu_np[r0:r1 + 1] - cu_np[r0]).astype(np.int32))
+                cu_h = cu_h.pin_memory()
+                cu_d = torch.empty(r1 - r0 + 1, dtype=torch.int32, device=dev)
+                sl = {"target_logits": (row0, row1), "draft_token_ids": (a, z)}
+                copies = [(cu_d, cu_h)]
+                for k, t in host.items():
+                    if k == "cu_num_draft":
+                        continue
+                    i0, i1 = sl.get(k, (r0, r1))
+                    copies.append((dst[k][i0:i1], t[i0:i1]))
+                h2d += sum(t.numel() * t.element_size() for _, t in copies)
+                part = sv.DeviceBatch(
+                    cu_num_draft=cu_d, draft_token_ids=db.draft_token_ids[a:z],
+                    target_logits=db.target_logits[row0:row1],
+                    draft_probs=None if hb.draft_probs is None else hb.draft_probs[a:z],
+                    temperature=db.temperature[r0:r1],
+                    top_k=None if db.top_k is None else db.top_k[r0:r1],
+                    top_p=None if db.top_p is None else db.top_p[r0:r1],
+                    seed=db.seed, request_base=db.request_base + r0, flags=db.flags,
+                    out_tokens=db.out_tokens[row0:row1], num_accepted=db.num_accepted[r0:r1],
+                    N=z - a, V=db.V)
+                parts.append((part, copies, torch.cuda.Event(), torch.cuda.Event()))
+            cs = torch.cuda.Stream(dev)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         if world > 1:
             dist.barrier()
         torch.cuda.synchronize(dev)
         e0.record(stream)
+        if parts:
+            cs.wait_event(e0)
         for _ in range(args.e2e_steps):
-            for k, t in host.items():
-                d = dst[k]
-                d.view(t.dtype).reshape(-1).copy_(t.reshape(-1), non_blocking=True)
-            ver.run(hb, stream)
+            if parts:
+                for part, copies, copied, done in parts:
+                    with torch.cuda.stream(cs):
+                        # the previous step's call on this range has finished with it
+                        cs.wait_event(done)
+                        for d, t in copies:
+                            d.view(t.dtype).reshape(-1).copy_(t.reshape(-1), non_blocking=True)
+                        copied.record(cs)
+                    stream.wait_event(copied)
+                    ver.run(part, stream)
+                    done.record(stream)
+            else:
+                for k, t in host.items():
+                    d = dst[k]
+                    d.view(t.dtype).reshape(-1).copy_(t.reshape(-1), non_blocking=True)
+                ver.run(hb, stream)
             out_tok.copy_(db.out_tokens, non_blocking=True)
             out_acc.copy_(db.num_accepted, non_blocking=True)
         e1.record(stream)
@@ -595,9 +656,10 @@ def main():
         torch.cuda.synchronize(dev)
         assert ver.status() == 0, "device status bits set (end-to-end calls)"
         assert np.array_equal(out_acc.numpy(), n_acc), "end-to-end outcome differs"
+        assert np.array_equal(out_tok.numpy(), tok_ref), "end-to-end tokens differ"
         e2e = {"value": world * positions / (e2e_ms * 1e-3), "unit": "draft_positions/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e2e_ms,
+               "ms_per_step": e2e_ms, "request_ranges": len(chunks),
                "draft_probs": ("page-locked host memory read in place" if q_read
                                else "none (one-hot draft)")}
 

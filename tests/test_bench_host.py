@@ -90,3 +90,13 @@ def test_race_issue_arithmetic_and_its_guards(monkeypatch):
         assert bench.race_issue(batch, None, 0.5, other, {"sm_mhz": 2000.0}, None) is None
     monkeypatch.setattr(bench, "RACE_SOURCES_SHA", "0" * 16)
     assert bench.race_issue(batch, None, 0.5, args, {"sm_mhz": 2000.0}, None) is None
+
+
+def test_request_chunks_cover_the_batch_in_order():
+    for B, k in ((1, 4), (5, 1), (7, 3), (1024, 4), (3, 8)):
+        cu = np.arange(B + 1, dtype=np.int32) * 2
+        ch = bench.request_chunks(cu, k)
+        assert ch[0][0] == 0 and ch[-1][1] == B
+        assert all(r1 > r0 for r0, r1 in ch)
+        assert all(ch[i][1] == ch[i + 1][0] for i in range(len(ch) - 1))
+        assert len(ch) == min(k, B)
