@@ -6,7 +6,8 @@
 // with the draft token masked; "드래프트가 제안하고 타깃이 판정한다": the bonus
 // token comes from p of the last row).
 //
-// One CTA per task (race, 8192-entry slice), numbered slice-major so that
+// One CTA per task (race, slice of 8192 entries with draft probabilities,
+// 16384 without, fewer for small batches), numbered slice-major so that
 // later slices of a race start from the best score its earlier slices
 // published (and from the argmax token's score seeded by the accept scan).
 // A race is one request's k* row, or, under sampler-match acceptance, every
@@ -23,9 +24,9 @@
 // their draw are packed into a per-warp queue so the draws run on dense
 // lanes; after the draw, -ln U >= 1 - U bounds every score by w / (1 - U),
 // so the logarithm and the division run only for entries that can still
-// win. Slice winners meet in one 64-bit atomicMax of (score bits, ~index);
-// k_race_token, launched next, writes each race's token to the race row's
-// output slot.
+// win. Each warp raises its race's best with one 64-bit atomicMax of
+// (score bits, ~index); k_race_token, launched next, writes each race's
+// token to the race row's output slot.
 #pragma once
 #include "common.cuh"
 #include "philox.cuh"
